@@ -1,0 +1,59 @@
+// Host-side declarations shared by the C-ABI layer (api.cu) and the kernel files.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace cosa {
+
+constexpr uint8_t kVisitComputed = 0;
+constexpr uint8_t kVisitSkipped = 1;
+constexpr uint8_t kVisitIgnored = 2;
+
+// ---------------------------------------------------------------------------
+// OSK
+// ---------------------------------------------------------------------------
+struct OskLaunch {
+  CUtensorMap qmap;  // q   bf16 [T, Hq, d]: dims {d, Hq, T}, box {64, 1, block_size}, SW128
+  CUtensorMap kmap;  // K   bf16 [pages, P, Hkv, d]: dims {d, Hkv, P, pages}, box {64, 1, P, 1}, SW128
+  CUtensorMap vmap;  // V   same as K
+  const int32_t* cu_seqlens;
+  const int32_t* page_table;
+  const int32_t* mask;
+  const int32_t* mask_len;
+  void* out;
+  uint8_t* visit_flags;
+  int32_t* status;
+  int num_reqs, num_q_heads, num_kv_heads, head_dim, block_size, page_size;
+  int total_tokens, max_seqlen, num_pages, max_pages_per_req, mask_pitch;
+  double sm_scale, skip_delta;
+};
+
+size_t osk_smem_bytes(int block_size, int head_dim);
+cudaError_t launch_osk(const OskLaunch& L, cudaStream_t stream);
+
+// ---------------------------------------------------------------------------
+// KAP
+// ---------------------------------------------------------------------------
+struct KapLaunch {
+  const uint16_t* q;
+  const int32_t* cu_seqlens;
+  const uint16_t* k_cache;
+  const int32_t* page_table;
+  int32_t* mask;
+  int32_t* mask_len;
+  int32_t* status;
+  void* workspace;
+  size_t workspace_bytes;
+  int num_reqs, num_q_heads, num_kv_heads, head_dim, block_size, page_size, stride;
+  int total_tokens, max_seqlen, num_pages, max_pages_per_req, mask_pitch, budget_ppm;
+  double sm_scale;
+};
+
+size_t kap_workspace_bytes(int num_reqs, int num_q_heads, int num_kv_heads, int block_size, int stride,
+                           int total_tokens, int max_seqlen);
+cudaError_t launch_kap(const KapLaunch& L, cudaStream_t stream);
+
+}  // namespace cosa

@@ -1,0 +1,614 @@
+// Ordered-Skipping Kernel (OSK): block-sparse prefill attention over a paged KV cache.
+//
+// CoSA (arXiv 2607.25291), Sec. 4.3 and Algorithm A lines 7-22.  One CTA owns one
+// (request, query head, query block) work item: the 128-row tile of the query block
+// (block_size 64 is padded to 128 rows), its ordered list of key blocks (the
+// computation-order mask M_KAP), and the online-softmax state of its rows.
+//
+// Warp roles (224 threads):
+//   warps 0-3  softmax: thread t owns tile row t (TMEM lane t).  Per visit it reads the
+//              row of S = Q K^T from TMEM, applies the causal / length / missing-page
+//              masks, updates the running max, takes part in the tile-wide skip vote
+//              (Eq. (5): skip iff every row has m_loc - m < ln(Delta/L)), and for computed
+//              blocks writes P = exp(S - m_ref) as bf16 into TMEM for the P.V product.
+//   warp 4     K producer: scans the mask row (drops invalid and repeated IDs, keeps the
+//              first occurrence), resolves each kept block to physical pages through the
+//              page table, and TMA-gathers the K pages in mask order ("physical page
+//              jumping" and "any-order page visiting" of Sec. 4.3).
+//   warp 5     MMA: allocates TMEM, issues tcgen05.mma for S = Q K^T (double-buffered S)
+//              and O += P V (P read from TMEM, V from shared memory).
+//   warp 6     V producer: TMA-gathers V pages only for blocks the vote computed.
+//
+// The running max m used by the skip rule is exact for the fp32 logits.  The reference
+// max m_ref used for the exponentials lags it by up to 2^8 (rescaling O in TMEM only
+// when m rises further), which changes rounding, not the result.
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace cosa {
+namespace {
+
+constexpr int kThreads = 224;
+constexpr int kMaxBlocksPerReq = 32768;  // dedupe bitmap capacity (blocks of one request)
+constexpr int kMaxPagesPerBlock = 8;
+constexpr float kRescaleLog2 = 8.0f;     // lazy-rescale threshold, log2 units
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO = 256, kTmemP0 = 384, kTmemP1 = 448;
+
+struct KInfo {
+  int32_t blk;     // block id, -1 = end of the list
+  uint32_t pages;  // bit u set: page u of the block exists
+  int32_t k;       // index of the entry in the mask row
+  int32_t phys[kMaxPagesPerBlock];
+};
+
+template <int BLK, int HD>
+struct alignas(1024) OskSmem {
+  static constexpr int NK = 3;
+  static constexpr int NV = 2;
+  static constexpr int TILE = BLK * HD * 2;   // bytes of one K or V tile
+  static constexpr int HALF = BLK * 128;     // bytes of one 64-wide d chunk of a tile
+  uint8_t q[128 * HD * 2];                    // [HD/64][128 rows][128 B], SW128
+  uint8_t k[NK][TILE];                        // [HD/64][BLK rows][128 B], SW128
+  uint8_t v[NV][TILE];
+  uint64_t q_full;
+  uint64_t k_full[NK], k_free[NK];
+  uint64_t v_full[NV], v_free[NV];
+  uint64_t s_full[2], s_free[2];
+  uint64_t p_full[2];
+  uint64_t o_done[2];
+  uint64_t vreq_full[4];
+  uint64_t cleanup;
+  KInfo kinfo[NK];
+  KInfo sinfo[2];
+  KInfo vreq[4];
+  int32_t dec[2];
+  int32_t vote[2][4];
+  uint32_t tmem_base;
+  int32_t abort_flag;
+  uint32_t seen[kMaxBlocksPerReq / 32];
+};
+
+struct OskArgs {
+  const int32_t* cu_seqlens;
+  const int32_t* page_table;
+  const int32_t* mask;
+  const int32_t* mask_len;
+  uint16_t* out;
+  uint8_t* visit_flags;
+  int32_t* status;
+  int num_reqs, num_q_heads, num_kv_heads, total_tokens, max_seqlen, nqb_max;
+  int page_size, num_pages, max_pages_per_req, mask_pitch;
+  float scale_log2;
+  double skip_delta;
+};
+
+__device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
+
+// Bounded wait taken by every lane of a warp; the warp agrees on the outcome.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status) {
+  return __all_sync(0xffffffffu, wait_parity_bounded(bar, parity, abort_flag, status));
+}
+
+template <int BLK, int HD>
+__global__ void __launch_bounds__(kThreads, 1)
+    osk_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+               const __grid_constant__ CUtensorMap vmap, const OskArgs a) {
+  using S = OskSmem<BLK, HD>;
+  constexpr int NK = S::NK, NV = S::NV;
+  constexpr int DH = HD / 64;  // 64-wide d chunks
+  extern __shared__ uint8_t smem_raw[];
+  S& sm = *reinterpret_cast<S*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  // ---------------- work item: kv-head major, heaviest query blocks first ----------------
+  const int G = a.num_q_heads / a.num_kv_heads;
+  int idx = blockIdx.x;
+  const int hg = idx % G;
+  idx /= G;
+  const int b = idx % a.num_reqs;
+  idx /= a.num_reqs;
+  const int i = a.nqb_max - 1 - (idx % a.nqb_max);
+  const int kvh = idx / a.nqb_max;
+  const int h = kvh * G + hg;
+  const int tok0 = a.cu_seqlens[b];
+  const int L = a.cu_seqlens[b + 1] - tok0;
+  if (L < 0 || L > a.max_seqlen || tok0 < 0 || tok0 + L > a.total_tokens) {
+    if (threadIdx.x == 0) report_status(a.status, kStatusBadInput);
+    return;
+  }
+  const int nblk = (L + BLK - 1) / BLK;
+  if (i >= nblk) return;  // absent query block of a shorter request
+
+  const int warp = threadIdx.x >> 5;
+  const int P = a.page_size;
+  const int pages_per_blk = BLK / P;
+  const int req_pages = (L + P - 1) / P;
+  const size_t row_base = ((static_cast<size_t>(b) * a.num_q_heads + h) * a.nqb_max + i);
+  const int32_t* mask_row = a.mask + row_base * a.mask_pitch;
+  uint8_t* flags_row = a.visit_flags ? a.visit_flags + row_base * a.mask_pitch : nullptr;
+  int n_entries = a.mask_len[row_base];
+  n_entries = n_entries < 0 ? 0 : (n_entries > a.mask_pitch ? a.mask_pitch : n_entries);
+  volatile int* abort_flag = &sm.abort_flag;
+
+  // ---------------- set-up ----------------
+  if (threadIdx.x == 0) {
+    mbar_init(&sm.q_full, 1);
+    for (int s = 0; s < NK; ++s) { mbar_init(&sm.k_full[s], 1); mbar_init(&sm.k_free[s], 1); }
+    for (int s = 0; s < NV; ++s) { mbar_init(&sm.v_full[s], 1); mbar_init(&sm.v_free[s], 1); }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sm.s_full[s], 2);   // plain arrive (visit info) + UMMA commit
+      mbar_init(&sm.s_free[s], 4);   // one per softmax warp
+      mbar_init(&sm.p_full[s], 4);
+      mbar_init(&sm.o_done[s], 1);
+    }
+    for (int s = 0; s < 4; ++s) mbar_init(&sm.vreq_full[s], 1);
+    mbar_init(&sm.cleanup, 1);
+    sm.abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&sm.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  // zero the operand tiles once: pages that do not exist are never loaded, and padding
+  // rows of a 64-row query block must hold finite values
+  {
+    uint4* z = reinterpret_cast<uint4*>(&sm.q[0]);
+    const int n16 = (128 * HD * 2 + NK * S::TILE + NV * S::TILE) / 16;
+    for (int e = threadIdx.x; e < n16; e += kThreads) z[e] = make_uint4(0, 0, 0, 0);
+  }
+  if (warp == 4) {
+    for (int w = lane_id(); w < (nblk + 31) / 32; w += 32) sm.seen[w] = 0u;
+    if (flags_row)
+      for (int k = n_entries + lane_id(); k < a.mask_pitch; k += 32) flags_row[k] = kVisitIgnored;
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp == 4) {
+    // =========================== K producer ===========================
+    const uint32_t lane = lane_id();
+    if (lane == 0) {
+      tma_prefetch_desc(&qmap);
+      tma_prefetch_desc(&kmap);
+      tma_prefetch_desc(&vmap);
+      mbar_arrive_expect_tx(&sm.q_full, BLK * HD * 2);
+      for (int dh = 0; dh < DH; ++dh) tma_load_3d(&sm.q[dh * 128 * 128], &qmap, &sm.q_full, dh * 64, h, tok0 + i * BLK);
+    }
+    const int32_t* pt_row = a.page_table + static_cast<size_t>(b) * a.max_pages_per_req;
+    int v = 0;  // visits issued
+    bool ok = true;
+    for (int k0 = 0; k0 < n_entries && ok; k0 += 32) {
+      const int k = k0 + static_cast<int>(lane);
+      const int j = (k < n_entries) ? mask_row[k] : -1;
+      const bool valid = (k < n_entries) && j >= 0 && j <= i && j < nblk;
+      const unsigned peers = __match_any_sync(0xffffffffu, valid ? j : -1 - static_cast<int>(lane));
+      const bool first = valid && (static_cast<int>(lane) == __ffs(peers) - 1);
+      const bool dup = first && ((sm.seen[j >> 5] >> (j & 31)) & 1u);
+      const bool keep = first && !dup;
+      __syncwarp();
+      if (keep) atomicOr(&sm.seen[j >> 5], 1u << (j & 31));
+      if (flags_row && k < n_entries && !keep) flags_row[k] = kVisitIgnored;
+      // physical pages of this lane's block
+      int phys[kMaxPagesPerBlock];
+      uint32_t pages = 0;
+#pragma unroll
+      for (int u = 0; u < kMaxPagesPerBlock; ++u) {
+        phys[u] = -1;
+        if (keep && u < pages_per_blk) {
+          const int lp = j * pages_per_blk + u;
+          const int pp = (lp < req_pages) ? pt_row[lp] : -1;
+          if (pp >= 0 && pp < a.num_pages) { phys[u] = pp; pages |= 1u << u; }
+        }
+      }
+      __syncwarp();
+      unsigned todo = __ballot_sync(0xffffffffu, keep);
+      while (todo && ok) {
+        const int src = __ffs(todo) - 1;
+        todo &= todo - 1;
+        const int jj = __shfl_sync(0xffffffffu, j, src);
+        const uint32_t pg = __shfl_sync(0xffffffffu, pages, src);
+        int ph[kMaxPagesPerBlock];
+#pragma unroll
+        for (int u = 0; u < kMaxPagesPerBlock; ++u) ph[u] = __shfl_sync(0xffffffffu, phys[u], src);
+        const int slot = v % NK;
+        if (v >= NK) ok = warp_wait(&sm.k_free[slot], ((v / NK) - 1) & 1, abort_flag, a.status);
+        if (!ok) break;
+        if (lane == 0) {
+          KInfo& ki = sm.kinfo[slot];
+          ki.blk = jj;
+          ki.pages = pg;
+          ki.k = k0 + src;
+#pragma unroll
+          for (int u = 0; u < kMaxPagesPerBlock; ++u) ki.phys[u] = ph[u];
+          const uint32_t bytes = static_cast<uint32_t>(__popc(pg)) * DH * P * 128u;
+          mbar_arrive_expect_tx(&sm.k_full[slot], bytes);
+          for (int u = 0; u < pages_per_blk; ++u) {
+            if (!((pg >> u) & 1u)) continue;
+            for (int dh = 0; dh < DH; ++dh)
+              tma_load_4d(&sm.k[slot][dh * S::HALF + u * P * 128], &kmap, &sm.k_full[slot], dh * 64, kvh, 0, ph[u]);
+          }
+        }
+        __syncwarp();
+        ++v;
+      }
+    }
+    // end marker
+    if (ok) {
+      const int slot = v % NK;
+      if (v >= NK) ok = warp_wait(&sm.k_free[slot], ((v / NK) - 1) & 1, abort_flag, a.status);
+      if (ok && lane == 0) {
+        sm.kinfo[slot].blk = -1;
+        mbar_arrive(&sm.k_full[slot]);
+      }
+    }
+    __syncwarp();
+    // on abort, let every issued copy land before the CTA exits
+    if (*abort_flag && lane == 0) {
+      wait_parity_bounded(&sm.q_full, 0, nullptr, nullptr);
+      for (int s = 0; s < NK; ++s) {
+        const int issued = (v - s + NK - 1) / NK;  // loads issued into slot s
+        if (issued > 0) wait_parity_bounded(&sm.k_full[s], (issued - 1) & 1, nullptr, nullptr);
+      }
+    }
+  } else if (warp == 5) {
+    // =========================== MMA issuer ===========================
+    const uint32_t lane = lane_id();
+    constexpr uint32_t idesc_qk = idesc_bf16_f32(128, BLK, false, false);
+    constexpr uint32_t idesc_pv = idesc_bf16_f32(128, HD, false, true);
+    bool ok = warp_wait(&sm.q_full, 0, abort_flag, a.status);
+    tc_fence_after();
+    // issue S(v) = Q K_v^T; returns 1 if issued, 0 at the end of the list, -1 on abort
+    auto issue_qk = [&](int vv) -> int {
+      const int slot = vv % NK;
+      if (!warp_wait(&sm.k_full[slot], (vv / NK) & 1, abort_flag, a.status)) return -1;
+      const int sb = vv & 1;
+      if (vv >= 2 && !warp_wait(&sm.s_free[sb], ((vv >> 1) - 1) & 1, abort_flag, a.status)) return -1;
+      const KInfo ki = sm.kinfo[slot];
+      if (lane == 0) {
+        sm.sinfo[sb] = ki;
+        mbar_arrive(&sm.s_full[sb]);
+      }
+      if (ki.blk < 0) {
+        if (lane == 0) mbar_arrive(&sm.s_full[sb]);
+        return 0;
+      }
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t d = tmem + (sb ? kTmemS1 : kTmemS0);
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint64_t ad = smem_desc_sw128(smem_u32(&sm.q[(kk >> 2) * 128 * 128 + (kk & 3) * 32]), 16, 1024);
+          const uint64_t bd = smem_desc_sw128(smem_u32(&sm.k[slot][(kk >> 2) * S::HALF + (kk & 3) * 32]), 16, 1024);
+          umma_ss(d, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&sm.s_full[sb]);
+        umma_commit(&sm.k_free[slot]);
+      }
+      __syncwarp();
+      return 1;
+    };
+    int c = 0;  // computed visits so far
+    if (ok) {
+      int more = issue_qk(0);
+      int v = 0;
+      while (more == 1) {
+        more = issue_qk(v + 1);
+        if (more < 0) break;
+        if (!warp_wait(&sm.p_full[v & 1], (v >> 1) & 1, abort_flag, a.status)) break;
+        if (sm.dec[v & 1]) {
+          const int slot = c % NV;
+          if (!warp_wait(&sm.v_full[slot], (c / NV) & 1, abort_flag, a.status)) break;
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t pcol = (c & 1) ? kTmemP1 : kTmemP0;
+#pragma unroll
+            for (int kk = 0; kk < BLK / 16; ++kk) {
+              const uint64_t bd = smem_desc_sw128(smem_u32(&sm.v[slot][kk * 16 * 128]), S::HALF, 1024);
+              umma_ts(tmem + kTmemO, tmem + pcol + kk * 8, bd, idesc_pv, (c > 0 || kk > 0) ? 1u : 0u);
+            }
+            umma_commit(&sm.v_free[slot]);
+            umma_commit(&sm.o_done[c & 1]);
+          }
+          __syncwarp();
+          ++c;
+        }
+        ++v;
+      }
+    }
+    // make sure every issued UMMA finished before TMEM is released
+    if (lane == 0) {
+      umma_commit(&sm.cleanup);
+      wait_parity_bounded(&sm.cleanup, 0, nullptr, nullptr);
+    }
+    __syncwarp();
+  } else if (warp == 6) {
+    // =========================== V producer ===========================
+    const uint32_t lane = lane_id();
+    int c = 0;
+    bool ok = true;
+    while (ok) {
+      if (!warp_wait(&sm.vreq_full[c & 3], (c >> 2) & 1, abort_flag, a.status)) { ok = false; break; }
+      const KInfo r = sm.vreq[c & 3];
+      if (r.blk < 0) break;
+      const int slot = c % NV;
+      if (c >= NV && !warp_wait(&sm.v_free[slot], ((c / NV) - 1) & 1, abort_flag, a.status)) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) {
+        const uint32_t bytes = static_cast<uint32_t>(__popc(r.pages)) * DH * P * 128u;
+        mbar_arrive_expect_tx(&sm.v_full[slot], bytes);
+        for (int u = 0; u < pages_per_blk; ++u) {
+          if (!((r.pages >> u) & 1u)) continue;
+          for (int dh = 0; dh < DH; ++dh)
+            tma_load_4d(&sm.v[slot][dh * S::HALF + u * P * 128], &vmap, &sm.v_full[slot], dh * 64, kvh, 0, r.phys[u]);
+        }
+      }
+      __syncwarp();
+      ++c;
+    }
+    if (*abort_flag && lane == 0) {
+      for (int s = 0; s < NV; ++s) {
+        const int issued = (c - s + NV - 1) / NV;
+        if (issued > 0) wait_parity_bounded(&sm.v_full[s], (issued - 1) & 1, nullptr, nullptr);
+      }
+    }
+  } else {
+    // =========================== softmax warpgroup (warps 0-3) ===========================
+    const int t = threadIdx.x;            // tile row == TMEM lane
+    const uint32_t lane = lane_id();
+    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+    const int pos = i * BLK + t;          // token position of this row inside the request
+    const bool row_valid = (t < BLK) && (pos < L);
+    const bool use_skip = a.skip_delta > 0.0;
+    const float tau2 = use_skip ? static_cast<float>(log2(a.skip_delta / static_cast<double>(L))) : 0.0f;
+    const float sl2 = a.scale_log2;
+    const uint32_t all_pages = (pages_per_blk >= 32) ? 0xffffffffu : ((1u << pages_per_blk) - 1u);
+    const int pshift = __ffs(P) - 1;
+    float m_run = -INFINITY;   // running max (log2 units), Algorithm A line 13
+    float m_ref = -INFINITY;   // max the exponentials are taken against
+    float l_sum = 0.0f;
+    int c = 0;                 // computed visits
+    bool ok = true;
+    bool local_fail = false;   // a wait of this warp ran out after the last vote
+    for (int v = 0;; ++v) {
+      const int sb = v & 1;
+      // vote code of this warp: bit 0 some row wants the block computed, bit 1 abort, bit 2 end of list
+      int code = 0;
+      KInfo ki;
+      float s[BLK];
+      float m_loc = -INFINITY, m_new = m_run;
+      bool okw = !local_fail && wait_parity_bounded(&sm.s_full[sb], (v >> 1) & 1, abort_flag, a.status);
+      okw = __all_sync(0xffffffffu, okw);
+      if (!okw) {
+        code = 2;
+      } else {
+        ki = sm.sinfo[sb];
+        if (ki.blk < 0) {
+          code = 4;
+        } else {
+          tc_fence_after();
+          const uint32_t sbase = tmem + lane_addr + (sb ? kTmemS1 : kTmemS0);
+#pragma unroll
+          for (int cc = 0; cc < BLK / 32; ++cc) {
+            uint32_t r[32];
+            tmem_ld32(sbase + cc * 32, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) s[cc * 32 + e] = __uint_as_float(r[e]);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.s_free[sb]);
+          // masks: causal on the diagonal block, length on the last block, missing pages
+          const int key0 = ki.blk * BLK;
+          const bool need_mask = (ki.blk == i) || (key0 + BLK > L) || (ki.pages != all_pages) || !row_valid;
+          if (need_mask) {
+            const int lim = row_valid ? min(pos, L - 1) - key0 : -1;  // last visible column
+#pragma unroll
+            for (int e = 0; e < BLK; ++e) {
+              const bool page_ok = (ki.pages >> (e >> pshift)) & 1u;
+              if (e > lim || !page_ok) s[e] = -INFINITY;
+            }
+          }
+          float mx = s[0];
+#pragma unroll
+          for (int e = 1; e < BLK; ++e) mx = fmaxf(mx, s[e]);
+          m_loc = (mx == -INFINITY) ? -INFINITY : mx * sl2;
+          m_new = fmaxf(m_run, m_loc);
+          bool want = true;
+          if (use_skip) want = row_valid && (m_loc != -INFINITY) && (m_loc - m_new >= tau2);
+          code = (__ballot_sync(0xffffffffu, want) != 0u) ? 1 : 0;
+        }
+      }
+      if (lane == 0) sm.vote[sb][warp] = code;
+      named_bar_sync(1, 128);
+      const int all = sm.vote[sb][0] | sm.vote[sb][1] | sm.vote[sb][2] | sm.vote[sb][3];
+      if (all & 2) { ok = false; break; }
+      if (all & 4) break;
+      const bool compute = (all & 1) != 0;
+      m_run = m_new;
+      if (t == 0 && flags_row) flags_row[ki.k] = compute ? kVisitComputed : kVisitSkipped;
+      if (!compute) {
+        if (t == 0) sm.dec[sb] = 0;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.p_full[sb]);
+        continue;
+      }
+      if (t == 0) {
+        sm.dec[sb] = 1;
+        sm.vreq[c & 3] = ki;
+        mbar_arrive(&sm.vreq_full[c & 3]);
+      }
+      // lazy rescale of O and l when the max rises by more than 2^8
+      const bool first_mass = (m_ref == -INFINITY) && (m_new != -INFINITY);
+      const bool rescale = (m_ref != -INFINITY) && (m_new > m_ref + kRescaleLog2);
+      float alpha = 1.0f;
+      if (first_mass) m_ref = m_new;
+      if (rescale) {
+        alpha = ex2_approx(m_ref - m_new);
+        m_ref = m_new;
+        l_sum *= alpha;
+      }
+      if (__any_sync(0xffffffffu, rescale) && c > 0) {
+        // O must hold every earlier P.V before it is scaled
+        bool okr = wait_parity_bounded(&sm.o_done[(c - 1) & 1], ((c - 1) >> 1) & 1, abort_flag, a.status);
+        if (!__all_sync(0xffffffffu, okr)) { local_fail = true; continue; }
+        tc_fence_after();
+        const uint32_t ob = tmem + lane_addr + kTmemO;
+#pragma unroll
+        for (int cc = 0; cc < HD / 32; ++cc) {
+          uint32_t r[32];
+          tmem_ld32(ob + cc * 32, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+          tmem_st32(ob + cc * 32, r);
+        }
+        tmem_wait_st();
+      }
+      // the P buffer written now was read by the P.V two computed visits ago
+      if (c >= 2) {
+        bool okp = wait_parity_bounded(&sm.o_done[c & 1], ((c - 2) >> 1) & 1, abort_flag, a.status);
+        if (!__all_sync(0xffffffffu, okp)) { local_fail = true; continue; }
+      }
+      tc_fence_after();
+      // P = exp2(S * scale * log2(e) - m_ref), bf16 pairs, 64 columns per TMEM store
+      const float base = (m_ref == -INFINITY) ? 0.0f : m_ref;
+      float rs = 0.0f;
+      const uint32_t pb = tmem + lane_addr + ((c & 1) ? kTmemP1 : kTmemP0);
+#pragma unroll
+      for (int cc = 0; cc < BLK / 64; ++cc) {
+        uint32_t r[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float x0 = s[cc * 64 + 2 * e], x1 = s[cc * 64 + 2 * e + 1];
+          const float p0 = (x0 == -INFINITY) ? 0.0f : ex2_approx(fmaf(x0, sl2, -base));
+          const float p1 = (x1 == -INFINITY) ? 0.0f : ex2_approx(fmaf(x1, sl2, -base));
+          rs += p0 + p1;
+          r[e] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32(pb + cc * 32, r);
+      }
+      tmem_wait_st();
+      l_sum += rs;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.p_full[sb]);
+      ++c;
+    }
+    if (t == 0) {
+      sm.vreq[c & 3].blk = -1;
+      mbar_arrive(&sm.vreq_full[c & 3]);
+    }
+    // ---------------- epilogue: O / l -> bf16 -> global ----------------
+    if (ok && c > 0) ok = wait_parity_bounded(&sm.o_done[(c - 1) & 1], ((c - 1) >> 1) & 1, abort_flag, a.status);
+    tc_fence_after();
+    const float inv_l = (l_sum > 0.0f) ? 1.0f / l_sum : 0.0f;
+    uint8_t* stage = &sm.q[0];  // every UMMA reading Q has completed
+    {
+      const uint32_t ob = tmem + lane_addr + kTmemO;
+#pragma unroll
+      for (int cc = 0; cc < HD / 32; ++cc) {
+        uint32_t r[32];
+        if (c > 0) {
+          tmem_ld32(ob + cc * 32, r);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) r[e] = 0u;
+        }
+        // 32 fp32 -> 16 packed bf16 pairs -> four 16-byte chunks, XOR-swizzled by row
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(r[q4 * 8 + 0]) * inv_l, __uint_as_float(r[q4 * 8 + 1]) * inv_l);
+          w.y = pack_bf16x2(__uint_as_float(r[q4 * 8 + 2]) * inv_l, __uint_as_float(r[q4 * 8 + 3]) * inv_l);
+          w.z = pack_bf16x2(__uint_as_float(r[q4 * 8 + 4]) * inv_l, __uint_as_float(r[q4 * 8 + 5]) * inv_l);
+          w.w = pack_bf16x2(__uint_as_float(r[q4 * 8 + 6]) * inv_l, __uint_as_float(r[q4 * 8 + 7]) * inv_l);
+          const int chunk = cc * 4 + q4;                       // 16-byte chunk of the row
+          const int phys_chunk = chunk ^ (t & (HD / 8 - 1));
+          *reinterpret_cast<uint4*>(stage + t * (HD * 2) + phys_chunk * 16) = w;
+        }
+      }
+    }
+    named_bar_sync(1, 128);
+    {
+      constexpr int CH = HD / 8;  // 16-byte chunks per row
+      const int rows = min(BLK, L - i * BLK);
+      uint8_t* out = reinterpret_cast<uint8_t*>(a.out);
+      for (int e = t; e < rows * CH; e += 128) {
+        const int r = e / CH, chunk = e % CH;
+        const uint4 w = *reinterpret_cast<const uint4*>(stage + r * (HD * 2) + ((chunk ^ (r & (CH - 1))) * 16));
+        const size_t tok = static_cast<size_t>(tok0) + static_cast<size_t>(i) * BLK + r;
+        *reinterpret_cast<uint4*>(out + ((tok * a.num_q_heads + h) * HD) * 2 + chunk * 16) = w;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int BLK, int HD>
+cudaError_t launch_osk_t(const OskLaunch& L, cudaStream_t stream) {
+  OskArgs a;
+  a.cu_seqlens = L.cu_seqlens;
+  a.page_table = L.page_table;
+  a.mask = L.mask;
+  a.mask_len = L.mask_len;
+  a.out = reinterpret_cast<uint16_t*>(L.out);
+  a.visit_flags = L.visit_flags;
+  a.status = L.status;
+  a.num_reqs = L.num_reqs;
+  a.num_q_heads = L.num_q_heads;
+  a.num_kv_heads = L.num_kv_heads;
+  a.total_tokens = L.total_tokens;
+  a.max_seqlen = L.max_seqlen;
+  a.nqb_max = (L.max_seqlen + BLK - 1) / BLK;
+  a.page_size = L.page_size;
+  a.num_pages = L.num_pages;
+  a.max_pages_per_req = L.max_pages_per_req;
+  a.mask_pitch = L.mask_pitch;
+  a.scale_log2 = static_cast<float>(L.sm_scale * 1.4426950408889634);
+  a.skip_delta = L.skip_delta;
+  const size_t smem = sizeof(OskSmem<BLK, HD>) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(osk_kernel<BLK, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const long long items = static_cast<long long>(L.num_kv_heads) * a.nqb_max * L.num_reqs * (L.num_q_heads / L.num_kv_heads);
+  if (items <= 0) return cudaSuccess;
+  osk_kernel<BLK, HD><<<static_cast<unsigned>(items), kThreads, smem, stream>>>(L.qmap, L.kmap, L.vmap, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t osk_smem_bytes(int block_size, int head_dim) {
+  if (block_size == 128 && head_dim == 128) return sizeof(OskSmem<128, 128>) + 1024;
+  if (block_size == 128 && head_dim == 64) return sizeof(OskSmem<128, 64>) + 1024;
+  if (block_size == 64 && head_dim == 128) return sizeof(OskSmem<64, 128>) + 1024;
+  return sizeof(OskSmem<64, 64>) + 1024;
+}
+
+cudaError_t launch_osk(const OskLaunch& L, cudaStream_t stream) {
+  if (L.block_size == 128 && L.head_dim == 128) return launch_osk_t<128, 128>(L, stream);
+  if (L.block_size == 128 && L.head_dim == 64) return launch_osk_t<128, 64>(L, stream);
+  if (L.block_size == 64 && L.head_dim == 128) return launch_osk_t<64, 128>(L, stream);
+  if (L.block_size == 64 && L.head_dim == 64) return launch_osk_t<64, 64>(L, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace cosa

@@ -1,0 +1,183 @@
+"""Helpers shared by the GPU parity tests: device copies of seeded workloads, calls through
+the C ABI, and comparisons against the float64 oracle."""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+from typing import Dict, List, Optional, Tuple
+
+import numpy as np
+import torch
+
+import synth
+from block_sparse_long_gb300 import cosa as C
+from oracle import cosa_oracle as orc
+
+# tolerances of the output comparison (bf16 output, fp32 accumulation)
+O_MAX_ABS = 2e-2
+O_MEAN_ABS = 2e-3
+# skip decisions: agreement rate, and the largest |margin| (nats) at which they may differ
+SKIP_AGREE = 0.999
+SKIP_MARGIN_TOL = 1e-3
+# two oracle scores closer than this (relative) are a float64 tie: either order is valid
+SCORE_TIE_RTOL = 1e-12
+
+
+def bf16_tensor(bits: np.ndarray, dev) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+
+def i32_tensor(x: np.ndarray, dev) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.int32)).to(dev)
+
+
+@dataclass
+class DevWorkload:
+    w: synth.Workload
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    pt: torch.Tensor
+    cu: torch.Tensor
+
+
+def to_device(w: synth.Workload, dev="cuda") -> DevWorkload:
+    return DevWorkload(w, bf16_tensor(w.q, dev), bf16_tensor(w.k_cache, dev), bf16_tensor(w.v_cache, dev),
+                       i32_tensor(w.page_table, dev), i32_tensor(w.cu_seqlens, dev))
+
+
+def oracle_params(spec, delta: float, budget_ppm: Optional[int] = None) -> orc.Params:
+    return orc.Params(spec.block_size, spec.page_size, spec.stride,
+                      spec.budget_ppm if budget_ppm is None else budget_ppm, 1.0 / math.sqrt(spec.head_dim),
+                      float(delta))
+
+
+def cosa_params(dw: DevWorkload, *, delta: float, mask_pitch: int, budget_ppm: Optional[int] = None):
+    sp = dw.w.spec
+    return C.params_for(dw.q, dw.k, dw.pt, dw.cu, block_size=sp.block_size, max_seqlen=sp.max_seqlen,
+                        stride=sp.stride, budget_ppm=sp.budget_ppm if budget_ppm is None else budget_ppm,
+                        mask_pitch=mask_pitch, skip_delta=delta)
+
+
+def run_kap(dw: DevWorkload, p) -> Tuple[np.ndarray, np.ndarray]:
+    status = torch.zeros(1, dtype=torch.int32, device=dw.q.device)
+    mask, mask_len = C.cosa_proxy_select(p, dw.q, dw.cu, dw.k, dw.pt, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, C.cosa_status_string(int(status.item()))
+    return mask.cpu().numpy(), mask_len.cpu().numpy()
+
+
+def run_osk(dw: DevWorkload, p, mask: np.ndarray, mask_len: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
+    dev = dw.q.device
+    m = i32_tensor(mask, dev)
+    ml = i32_tensor(mask_len, dev)
+    flags = torch.full(mask.shape, 255, dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = torch.full_like(dw.q, float("nan"))
+    C.cosa_sparse_prefill(p, dw.q, dw.cu, dw.k, dw.v, dw.pt, m, ml, out=out, visit_flags=flags, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, C.cosa_status_string(int(status.item()))
+    return out.float().cpu().numpy(), flags.cpu().numpy()
+
+
+def items_of(spec, heads=None, qblocks=None) -> List[Tuple[int, int, int]]:
+    out = []
+    for b, L in enumerate(spec.lengths):
+        nqb = -(-L // spec.block_size)
+        for h in (range(spec.num_q_heads) if heads is None else heads):
+            for i in (range(nqb) if qblocks is None else [x for x in qblocks if x < nqb]):
+                out.append((b, h, i))
+    return out
+
+
+@dataclass
+class OskReport:
+    n_items: int
+    n_tested: int
+    n_disagree: int
+    max_disagree_margin: float
+    max_abs: float
+    mean_abs: float
+    disagreements: list
+
+
+def compare_osk(w: synth.Workload, prm: orc.Params, mask, mask_len, out_gpu, flags_gpu,
+                items) -> OskReport:
+    """Oracle vs GPU on the given items.  Skip decisions may differ only near a zero margin;
+    the oracle is then replayed with the GPU's decisions so outputs compare like for like."""
+    sp = w.spec
+    ref = orc.osk_all(w.q, w.k_cache, w.v_cache, w.page_table, w.cu_seqlens, sp.num_q_heads, sp.num_kv_heads,
+                      prm, mask, mask_len, items=items)
+    n_tested = 0
+    dis = []
+    force = {}
+    for it, r in ref.items():
+        b, h, i = it
+        n = int(mask_len[b, h, i])
+        g = flags_gpu[b, h, i, :n]
+        assert ((g == orc.IGNORED) == (r.flags == orc.IGNORED)).all(), f"ignored entries differ at {it}"
+        tested = r.flags != orc.IGNORED
+        n_tested += int(tested.sum())
+        bad = np.nonzero(tested & (g != r.flags))[0]
+        for k in bad:
+            dis.append((it, int(k), float(r.margins[k])))
+        if len(bad):
+            force[it] = g.astype(np.int8)
+        # entries past mask_len are reported ignored
+        assert (flags_gpu[b, h, i, n:] == orc.IGNORED).all()
+    if force:
+        ref.update(orc.osk_all(w.q, w.k_cache, w.v_cache, w.page_table, w.cu_seqlens, sp.num_q_heads,
+                               sp.num_kv_heads, prm, mask, mask_len, items=list(force), force=force))
+    errs = []
+    cu = w.cu_seqlens
+    for (b, h, i), r in ref.items():
+        t0 = int(cu[b]) + i * sp.block_size
+        got = out_gpu[t0:t0 + r.out.shape[0], h, :]
+        errs.append(np.abs(got - r.out).ravel())
+    e = np.concatenate(errs) if errs else np.zeros(1)
+    return OskReport(len(ref), n_tested, len(dis), max([abs(x[2]) for x in dis], default=0.0),
+                     float(e.max()), float(e.mean()), dis)
+
+
+def assert_osk_ok(rep: OskReport):
+    assert np.isfinite(rep.max_abs)
+    assert rep.max_abs <= O_MAX_ABS, rep
+    assert rep.mean_abs <= O_MEAN_ABS, rep
+    if rep.n_tested:
+        assert 1.0 - rep.n_disagree / rep.n_tested >= SKIP_AGREE, rep
+    assert rep.max_disagree_margin <= SKIP_MARGIN_TOL, rep
+
+
+def compare_masks(mask_gpu, len_gpu, rows: Dict, lengths, block_size) -> List:
+    """Bit-exact comparison of M_KAP rows; a difference is accepted only between blocks whose
+    oracle keys (HRM flag, score) are equal within a float64 tie.  Returns accepted ties;
+    raises on a real mismatch."""
+    ties = []
+    for (b, h, i), row in rows.items():
+        K = row.K
+        assert int(len_gpu[b, h, i]) == K, ((b, h, i), int(len_gpu[b, h, i]), K)
+        g = mask_gpu[b, h, i, :K]
+        o = row.order[:K]
+        if np.array_equal(g, o):
+            assert (mask_gpu[b, h, i, K:] == -1).all()
+            continue
+        # accept only float64 ties: same multiset of keys position by position
+        sc = row.scores
+        for p in range(K):
+            if g[p] == o[p]:
+                continue
+            a, c = int(g[p]), int(o[p])
+            assert 0 <= a <= i, ((b, h, i), p, a)
+            same_flag = bool(row.hrm[a]) == bool(row.hrm[c])
+            tie = abs(sc[a] - sc[c]) <= SCORE_TIE_RTOL * max(abs(sc[a]), abs(sc[c]), 1e-300)
+            assert same_flag and tie, f"mask mismatch at {(b, h, i)} pos {p}: gpu {a} ({sc[a]!r}, hrm {row.hrm[a]}) " \
+                                      f"oracle {c} ({sc[c]!r}, hrm {row.hrm[c]})"
+            ties.append(((b, h, i), p, a, c, float(sc[a]), float(sc[c])))
+        assert len(set(g.tolist())) == K
+        assert (mask_gpu[b, h, i, K:] == -1).all()
+    # absent query blocks
+    for b, L in enumerate(lengths):
+        nqb = -(-L // block_size)
+        assert (len_gpu[b, :, nqb:] == 0).all()
+        assert (mask_gpu[b, :, nqb:, :] == -1).all()
+    return ties
