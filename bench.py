@@ -1,0 +1,451 @@
+"""Benchmark of CoSA sparse prefill (KAP + OSK) on one or more GB300s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 4] [--impl cosa|reference]
+
+One step is one pass of the whole hot path over the workload's batch:
+cosa_proxy_select (KAP: sampled logits, block scores, HRM-first ordered mask) followed by
+cosa_sparse_prefill (OSK: ordered visits through the page table, in-kernel skip, online
+softmax).  Inputs are resident in HBM when the timed region starts; the end-to-end variant
+(`e2e`) also copies the step's inputs from pinned host memory and reads the output back.
+
+Work accounting (algorithmic FLOPs, the same for every implementation):
+  OSK  2*b*b*d per visited block (Q K^T, diagonal blocks counted whole) plus 2*b*b*d per
+       computed block (P V), b = block size, d = head dim;
+  KAP  2*d per causal (sampled row, sampled key) pair.
+Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+# BLAS threads pinned to one, so the oracle's core count is exactly the pool size
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "OSK sparse prefill ms and effective TFLOP/s at 128K; % bf16 tensor peak"
+UNIT = "TFLOP/s"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# --------------------------------------------------------------------------- #
+# workload and work accounting
+# --------------------------------------------------------------------------- #
+def delta_for(config: int) -> float:
+    cal = json.load(open(os.path.join(ROOT, "tests", "golden", "delta_calibration.json")))
+    return float(cal["configs"][str(config)]["delta"])
+
+
+def kap_flops(spec) -> float:
+    total = 0.0
+    for L in spec.lengths:
+        R = -(-L // spec.stride)
+        total += spec.num_q_heads * 2.0 * spec.head_dim * R * (R + 1) / 2.0
+    return total
+
+
+def osk_flops_from_flags(spec, flags: np.ndarray) -> tuple:
+    tile = 2.0 * spec.block_size * spec.block_size * spec.head_dim
+    visited = int((flags != 2).sum())
+    computed = int((flags == 0).sum())
+    return tile * (visited + computed), visited, computed
+
+
+def dense_equiv_flops(spec) -> float:
+    total = 0.0
+    for L in spec.lengths:
+        nqb = -(-L // spec.block_size)
+        total += spec.num_q_heads * 4.0 * spec.block_size ** 2 * spec.head_dim * nqb * (nqb + 1) / 2.0
+    return total
+
+
+# --------------------------------------------------------------------------- #
+# CPU baseline: the float64 oracle on a bounded sample (process pool, one item group per task)
+# --------------------------------------------------------------------------- #
+_W = None  # workload inherited by forked workers
+
+
+def _oracle_group(args):
+    b, h, qblocks, delta = args
+    os.environ["OMP_NUM_THREADS"] = "1"
+    from oracle import cosa_oracle as orc
+    w = _W
+    sp = w.spec
+    G = sp.num_q_heads // sp.num_kv_heads
+    t0 = time.perf_counter()
+    prm = orc.Params(sp.block_size, sp.page_size, sp.stride, sp.budget_ppm, 1.0 / math.sqrt(sp.head_dim), delta)
+    L = sp.lengths[b]
+    Q = orc.request_queries(w.q, w.cu_seqlens, b, h)
+    K, ex = orc.request_keys(w.k_cache, w.page_table[b], L, sp.page_size, h // G)
+    V, _ = orc.request_keys(w.v_cache, w.page_table[b], L, sp.page_size, h // G)
+    rows = orc.kap_request_head(Q, K, ex, prm, qblocks)
+    tile = 2.0 * sp.block_size ** 2 * sp.head_dim
+    flops = 0.0
+    for i, row in rows.items():
+        r = orc.osk_qblock(Q, K, V, ex, i, row.order[:row.K], row.K, prm)
+        flops += tile * (int((r.flags != orc.IGNORED).sum()) + int((r.flags == orc.COMPUTED).sum()))
+        nrows = len(range(i * sp.block_size, min(L, (i + 1) * sp.block_size), sp.stride))
+        first = i * sp.block_size // sp.stride
+        flops += 2.0 * sp.head_dim * sum(first + k + 1 for k in range(nrows))
+    return flops, time.perf_counter() - t0
+
+
+def sample_groups(spec, n_groups: int, per_group: int, delta: float, seed: int = 99):
+    rng = np.random.default_rng(seed)
+    groups = []
+    b = int(np.argmax(spec.lengths))
+    nqb = -(-spec.lengths[b] // spec.block_size)
+    heads = rng.choice(spec.num_q_heads, size=min(n_groups, spec.num_q_heads), replace=False)
+    for gi, h in enumerate(heads):
+        # stratified over the query-block axis, the last block always included
+        qs = sorted({int(nqb - 1 - gi % 2)} | {int(x) for x in rng.integers(0, nqb, per_group - 1)})
+        groups.append((b, int(h), qs, delta))
+    return groups
+
+
+def cpu_oracle_run(w, groups, cores: int):
+    global _W
+    _W = w
+    ctx = mp.get_context("fork")          # forked before this process touches CUDA
+    t0 = time.perf_counter()
+    with ctx.Pool(cores) as pool:
+        res = pool.map(_oracle_group, groups)
+    wall = time.perf_counter() - t0
+    flops = sum(r[0] for r in res)
+    cpu_s = sum(r[1] for r in res)
+    return flops, wall, cpu_s
+
+
+# --------------------------------------------------------------------------- #
+# clocks during the timed region
+# --------------------------------------------------------------------------- #
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id: str):
+        self.bus_id = bus_id
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", self.bus_id, f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- #
+# helpers
+# --------------------------------------------------------------------------- #
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def kernel_sha() -> str:
+    h = hashlib.sha256()
+    for f in ("osk.cu", "ptx.cuh"):
+        h.update(open(os.path.join(ROOT, "block_sparse_long_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_per_launch(workload: str):
+    """DRAM bytes per OSK launch from the committed ncu summary, if it is for this kernel source."""
+    path = os.path.join(ROOT, "profiles", "osk_traffic.json")
+    if not os.path.exists(path):
+        return None
+    d = json.load(open(path))
+    if d.get("kernel_sha") != kernel_sha() or d.get("workload") != workload:
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# --------------------------------------------------------------------------- #
+# reference arm: the oracle, as it stands, on the host cores
+# --------------------------------------------------------------------------- #
+def run_reference(args, spec, workload_name, delta):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    cores = os.cpu_count() or 1
+    w = synth.make_workload(spec)
+    groups = sample_groups(spec, n_groups=cores, per_group=10, delta=delta)
+    sample = (f"{sum(len(g[2]) for g in groups)} (head, query block) items of the {workload_name} workload, "
+              f"{len(groups)} heads x up to 10 blocks stratified over the block axis, KAP + OSK each")
+    for _ in range(args.warmup):
+        cpu_oracle_run(w, groups, cores)
+    walls, flops = [], 0.0
+    for _ in range(args.steps):
+        f, wall, _ = cpu_oracle_run(w, groups, cores)
+        walls.append(wall)
+        flops = f
+    ms = 1e3 * sum(walls) / len(walls)
+    value = flops / (ms * 1e-3) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_name, "skip_delta": delta, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# --------------------------------------------------------------------------- #
+# CUDA arm
+# --------------------------------------------------------------------------- #
+def run_cosa(args, spec, workload_name, delta):
+    world, rank, local = dist_env()
+    w = synth.make_workload(spec)
+    # CPU baseline first: the oracle pool is forked before this process touches CUDA
+    cpu = None
+    if rank == 0 and world >= 1 and not args.no_cpu_baseline:
+        cores = os.cpu_count() or 1
+        groups = sample_groups(spec, n_groups=cores, per_group=10, delta=delta)
+        f, wall, cpu_s = cpu_oracle_run(w, groups, cores)
+        cpu = {"value": f / wall / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"{sum(len(g[2]) for g in groups)} (head, query block) items of the {workload_name} "
+                         f"workload ({len(groups)} heads x up to 10 blocks, KAP + OSK each), {wall:.1f} s wall, "
+                         f"{cpu_s:.1f} s CPU"}
+
+    import torch
+    from block_sparse_long_gb300 import cosa as C
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+
+    def bf(x):
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    q, k, v = bf(w.q), bf(w.k_cache), bf(w.v_cache)
+    pt = torch.from_numpy(w.page_table).to(dev)
+    cu = torch.from_numpy(w.cu_seqlens).to(dev)
+    pitch = C.stage1_pitch(spec.budget_ppm, spec.max_seqlen, spec.block_size)
+    p = C.params_for(q, k, pt, cu, block_size=spec.block_size, max_seqlen=spec.max_seqlen, stride=spec.stride,
+                     budget_ppm=spec.budget_ppm, mask_pitch=pitch, skip_delta=delta)
+    nqb = -(-spec.max_seqlen // spec.block_size)
+    mask = torch.empty((spec.num_reqs, spec.num_q_heads, nqb, pitch), dtype=torch.int32, device=dev)
+    mask_len = torch.empty((spec.num_reqs, spec.num_q_heads, nqb), dtype=torch.int32, device=dev)
+    ws = torch.empty(C.cosa_proxy_workspace_size(p), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(q)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flags = torch.empty((spec.num_reqs, spec.num_q_heads, nqb, pitch), dtype=torch.uint8, device=dev)
+
+    def kap():
+        C.cosa_proxy_select(p, q, cu, k, pt, mask=mask, mask_len=mask_len, workspace=ws, status=status)
+
+    def osk(record=False):
+        C.cosa_sparse_prefill(p, q, cu, k, v, pt, mask, mask_len, out=out, visit_flags=flags if record else None,
+                              status=status)
+
+    # one untimed pass with visit recording: the work of a step (deterministic)
+    kap()
+    osk(record=True)
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(C.cosa_status_string(int(status.item())))
+    fl = flags.cpu().numpy()
+    ofl, visited, computed = osk_flops_from_flags(spec, fl)
+    kfl = kap_flops(spec)
+    step_flops = ofl + kfl
+    causal = sum(spec.num_q_heads * (-(-L // spec.block_size)) * (-(-L // spec.block_size) + 1) / 2
+                 for L in spec.lengths)
+
+    for _ in range(args.warmup):
+        kap()
+        osk()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    bus = torch.cuda.get_device_properties(dev)
+    bus_id = f"{getattr(bus, 'pci_domain_id', 0):08X}:{getattr(bus, 'pci_bus_id', 0):02X}:" \
+             f"{getattr(bus, 'pci_device_id', 0):02X}.0"
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(bus_id) as clk:
+        start.record(stream)
+        for s in range(args.steps):
+            e0, e1, e2 = ev[s]
+            e0.record(stream)
+            kap()
+            e1.record(stream)
+            osk()
+            e2.record(stream)
+        stop.record(stream)
+        torch.cuda.synchronize()
+    total_ms = start.elapsed_time(stop)
+    kap_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(args.steps)]
+    osk_ms = [ev[s][1].elapsed_time(ev[s][2]) for s in range(args.steps)]
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    if int(status.item()) != 0:
+        raise RuntimeError(C.cosa_status_string(int(status.item())))
+    ms_step = total_ms / args.steps
+    value = world * step_flops / (ms_step * 1e-3) / 1e12
+
+    # end to end through the public API with host buffers (pinned), copies inside the timed region
+    hq = torch.from_numpy(np.ascontiguousarray(w.q).view(np.int16)).pin_memory()
+    hk = torch.from_numpy(np.ascontiguousarray(w.k_cache).view(np.int16)).pin_memory()
+    hv = torch.from_numpy(np.ascontiguousarray(w.v_cache).view(np.int16)).pin_memory()
+    hpt = torch.from_numpy(w.page_table).pin_memory()
+    hcu = torch.from_numpy(w.cu_seqlens).pin_memory()
+    hout = torch.empty(out.shape, dtype=torch.int16).pin_memory()
+    qi, ki, vi = q.view(torch.int16), k.view(torch.int16), v.view(torch.int16)
+
+    def e2e_step():
+        qi.copy_(hq, non_blocking=True)
+        ki.copy_(hk, non_blocking=True)
+        vi.copy_(hv, non_blocking=True)
+        pt.copy_(hpt, non_blocking=True)
+        cu.copy_(hcu, non_blocking=True)
+        kap()
+        osk()
+        hout.copy_(out.view(torch.int16), non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_start, e_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_start.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e_stop.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e_start.elapsed_time(e_stop) / args.steps
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hpt, hcu))
+    d2h = hout.numel() * hout.element_size()
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+    pk, pk_src = peaks()
+    osk_avg = statistics.mean(osk_ms)
+    achieved = ofl / (osk_avg * 1e-3) / 1e12
+    peak = float(pk["bf16_tflops"])
+    traffic = traffic_per_launch(workload_name)
+    cl = clk.summary()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_name, "num_reqs": spec.num_reqs, "seq_lens": list(spec.lengths),
+                   "num_q_heads": spec.num_q_heads, "num_kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim,
+                   "block_size": spec.block_size, "page_size": spec.page_size, "stride": spec.stride,
+                   "stage1_budget": spec.budget_ppm / 1e6, "skip_delta": delta,
+                   "l2": "inputs larger than L2 (q, k, v = %.2f GiB)" % ((q.numel() + k.numel() + v.numel()) * 2 / 2**30),
+                   "parallelism": f"independent replicas per GPU x{world}"},
+        "osk_ms": osk_avg, "kap_ms": statistics.mean(kap_ms),
+        "osk_tflops": achieved, "osk_pct_bf16_peak": 100.0 * achieved / peak,
+        "dense_equiv_tflops": dense_equiv_flops(spec) / (osk_avg * 1e-3) / 1e12,
+        "visits": visited, "computed": computed, "realized_stage1": visited / causal,
+        "realized_stage2": computed / causal,
+        "roofline": {"bound": "tensor", "kernel": "osk_kernel<128,128>", "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"bf16_tflops ({pk_src}, burst)"},
+        "e2e": {"value": world * step_flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 7 * args.steps,
+        "clocks": cl,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", type=int, default=4, help="workload number (1-5); 4 = 128K GQA")
+    ap.add_argument("--impl", choices=["cosa", "reference"], default="cosa")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    spec = synth.spec_for(args.workload)
+    delta = delta_for(args.workload) if args.workload != 1 else 2000.0
+    name = spec.name
+    if args.impl == "reference":
+        return run_reference(args, spec, name, delta)
+    return run_cosa(args, spec, name, delta)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -13,13 +13,12 @@
 //
 // Exactness.  The logits run on tcgen05 tensor cores in fp32; every decision that fp32 could
 // get wrong is settled in float64:
-//   pass 1 (kap_logits<ROWMAX>)  per row: largest and second-largest fp32 logit and the
-//                                 argmax key;
+//   pass 1 (kap_logits<ROWMAX>)  per row: the four largest fp32 logits and their keys;
 //   kap_exact                    per row: error bound e_r >= |fp32 logit - exact logit| for every
 //                                 key of the row (from ||q_r|| * max ||k|| and the accumulation
 //                                 length); if the runner-up is more than 2 e_r below the maximum
 //                                 the argmax key is certain and M_r is its float64 logit;
-//                                 otherwise every near-maximal key is re-evaluated in float64;
+//                                 otherwise every key within 2 e_r is re-evaluated in float64;
 //                                 the HRM blocks of the row follow exactly;
 //   pass 2 (kap_logits<SCORES>)  per (query block, key block): fp32 score and a rigorous bound
 //                                 on its error, given the float64 M_r;
@@ -39,9 +38,15 @@ namespace {
 constexpr int kRowTile = 128;           // sampled rows per CTA of the logits kernel
 constexpr int kKeyTile = 128;           // sampled keys per UMMA
 constexpr int kSelectThreads = 256;
-// |fp32 logit - exact| <= kKappa * ||q|| * ||k|| * scale, for d <= 128 (at most 128 products
-// accumulated in fp32; a worst-case 2^-23 relative loss per accumulation step is 2^-16).
-constexpr float kKappa = 1.0f / 32768.0f;
+// |fp32 logit - exact| <= kKappa * ||q|| * ||k|| * scale for d <= 128.  The products of bf16
+// inputs are exact in fp32; summing them in groups of at most 16 aligned to the group's largest
+// term and truncated to fp32 width, then adding each group to a truncating fp32 accumulator,
+// loses at most (16 + 8) * 2^-23 = 48 * 2^-24 of sum |q_k k_k| <= ||q|| ||k||.  kKappa = 64 * 2^-24
+// covers that model; on GB300 the largest error measured over normal, Student-t, mixed-magnitude
+// and one-large-many-small inputs was 13 * 2^-24 of sum |q_k k_k|.  The CUDA-core fp32 dot
+// products (4 sequential FMAs per lane, a 5-level shuffle tree) stay within 9 * 2^-24.
+constexpr float kKappa = 1.0f / 262144.0f;
+constexpr int kTop = 4;                 // candidates per row kept by the row-max pass
 
 struct KapArgs {
   const uint16_t* q;
@@ -55,12 +60,14 @@ struct KapArgs {
   int64_t* row_off;      // [B+1]: first sampled-row record of request b (times Hq)
   int64_t* sc_off;       // [B+1]: first score of request b (times Hq)
   float* knorm;          // [B * Hkv]: max ||k~|| of the request's existing sampled keys
-  float* v1;             // per sampled row: largest fp32 logit (scaled), -inf if none
-  float* v2;             // per sampled row: second largest fp32 logit (scaled)
-  int32_t* c1;           // per sampled row: argmax key index
+  float* kbnorm;         // [B * Hkv * nqb_max]: max ||k~|| over the sampled keys of each block
+  float* topv;           // per sampled row: kTop largest fp32 logits (scaled, descending), -inf pad
+  int32_t* topc;         // per sampled row: their key indices
+  float* qnorm;          // per sampled row: ||q~_r|| rounded up
   double* M;             // per sampled row: exact maximum logit (scaled), -inf if none
   float* err;            // per sampled row: error bound e_r of its fp32 logits (scaled)
-  int32_t* rflags;       // per sampled row: bit 0 = ties resolved by scan (HRM bitmap valid), bit 1 = empty
+  int32_t* rflags;       // per sampled row: bit 0 = several HRM candidates (bitmap valid), bit 1 = empty
+  int32_t* c1;           // per sampled row: the exact argmax key (the first one if several tie)
   uint32_t* hrm_bits;    // per sampled row: bitmap of HRM blocks, words_per_row words (ambiguous rows only)
   float* score;          // per (request, head): nqb x nqb fp32 scores, row i = query block
   float* score_err;      // same shape: bound on |score - exact score|
@@ -159,6 +166,7 @@ __global__ void kap_setup_kernel(KapArgs a) {
     a.sc_off[a.num_reqs] = so;
   }
   for (int e = threadIdx.x; e < a.num_reqs * a.num_kv_heads; e += blockDim.x) a.knorm[e] = 0.0f;
+  for (int e = threadIdx.x; e < a.num_reqs * a.num_kv_heads * a.nqb_max; e += blockDim.x) a.kbnorm[e] = 0.0f;
 }
 
 // max ||k~_c|| over the existing sampled keys of (request, kv head); rounded up
@@ -176,6 +184,11 @@ __global__ void kap_knorm_kernel(KapArgs a) {
       s2 = fmaf(x, x, s2);
     }
     n = sqrtf(s2) * (1.0f + 1.0f / 65536.0f);
+  }
+  if (n > 0.0f) {
+    const int j = (c * a.stride) / a.block_size;
+    atomicMax(reinterpret_cast<int*>(&a.kbnorm[(static_cast<size_t>(b) * a.num_kv_heads + kvh) * a.nqb_max + j]),
+              __float_as_int(n));
   }
   for (int o = 16; o > 0; o >>= 1) n = fmaxf(n, __shfl_xor_sync(0xffffffffu, n, o));
   if ((threadIdx.x & 31) == 0 && n > 0.0f)
@@ -271,17 +284,18 @@ __global__ void __launch_bounds__(128) kap_logits_kernel(KapArgs a) {
   if (nkt > 1) load_keys(1, 1);
 
   // per-row state
-  float best = -INFINITY, second = -INFINITY;   // raw (unscaled) fp32 logits
-  int best_c = -1;
-  double Mexact = 0.0;
-  float M32 = -INFINITY, erow = 0.0f;
+  float topv[kTop];                             // kTop largest raw fp32 logits, descending
+  int topc[kTop];
+#pragma unroll
+  for (int m = 0; m < kTop; ++m) { topv[m] = -INFINITY; topc[m] = -1; }
+  float M32 = -INFINITY, ebase = 0.0f;
   int64_t sbase = 0;
   int nqb = ri.nqb;
+  const float* kbn = a.kbnorm + (static_cast<size_t>(b) * a.num_kv_heads + kvh) * a.nqb_max;
   if (MODE == kModeScores) {
     if (row_ok) {
-      Mexact = a.M[rec];
-      M32 = static_cast<float>(Mexact);
-      erow = a.err[rec];
+      M32 = static_cast<float>(a.M[rec]);
+      ebase = kKappa * scale * a.qnorm[rec] * 1.001f;
     }
     sbase = a.sc_off[b] + static_cast<int64_t>(h) * nqb * nqb;
   }
@@ -321,12 +335,23 @@ __global__ void __launch_bounds__(128) kap_logits_kernel(KapArgs a) {
           const int col = cc * 32 + e;
           if (!row_ok || col > last_col || !((vbits >> e) & 1u)) continue;
           const float x = __uint_as_float(rv[e]);
-          if (x > best) {
-            second = best;
-            best = x;
-            best_c = kt * kKeyTile + col;
-          } else if (x > second) {
-            second = x;
+          if (x > topv[3]) {                    // insertion into the sorted top-4 (ties keep the first)
+            const int key = kt * kKeyTile + col;
+            if (x > topv[2]) {
+              topv[3] = topv[2]; topc[3] = topc[2];
+              if (x > topv[1]) {
+                topv[2] = topv[1]; topc[2] = topc[1];
+                if (x > topv[0]) {
+                  topv[1] = topv[0]; topc[1] = topc[0]; topv[0] = x; topc[0] = key;
+                } else {
+                  topv[1] = x; topc[1] = key;
+                }
+              } else {
+                topv[2] = x; topc[2] = key;
+              }
+            } else {
+              topv[3] = x; topc[3] = key;
+            }
           }
         }
       } else {
@@ -338,13 +363,15 @@ __global__ void __launch_bounds__(128) kap_logits_kernel(KapArgs a) {
             const int col = cc * 32 + e;
             if (row_ok && col <= last_col && ((vbits >> e) & 1u)) bm = fmaxf(bm, __uint_as_float(rv[e]));
           }
+          const int j = kt * (kKeyTile / KB) + cc * (32 / KB) + g;
           float x = 0.0f, xe = 0.0f;
           if (bm != -INFINITY && M32 != -INFINITY) {
             const float u = fmaf(bm, scale, -M32);
             x = expf(u);
-            // |u - exact| <= e_r + rounding of the scaled logit, of M_r and of the subtraction;
-            // expf adds at most 2 ulp; a value below exp(-80) is only bounded absolutely
-            const float du = erow + 1.2e-7f * (2.0f * fabsf(M32) + fabsf(u) + 1.0f);
+            // |u - exact| <= kappa * scale * ||q|| * (largest ||k|| of block j) plus the rounding of
+            // the scaled logit, of M_r and of the subtraction; expf adds at most 2 ulp; a value
+            // below exp(-80) is only bounded absolutely
+            const float du = ebase * __ldg(kbn + j) + 1.2e-7f * (2.0f * fabsf(M32) + fabsf(u) + 1.0f);
             xe = x * (expm1f(du) * 1.01f + 3.0e-7f) + ((u < -80.0f) ? 2.0e-35f : 0.0f);
           }
 #pragma unroll
@@ -352,7 +379,6 @@ __global__ void __launch_bounds__(128) kap_logits_kernel(KapArgs a) {
             x += __shfl_xor_sync(0xffffffffu, x, o);
             xe += __shfl_xor_sync(0xffffffffu, xe, o);
           }
-          const int j = kt * (kKeyTile / KB) + cc * (32 / KB) + g;
           if ((lane % KB) == 0 && qblk < nqb && j <= qblk) {
             const int64_t o = sbase + static_cast<int64_t>(qblk) * nqb + j;
             a.score[o] = x;
@@ -364,9 +390,11 @@ __global__ void __launch_bounds__(128) kap_logits_kernel(KapArgs a) {
     tc_fence_before();
   }
   if (MODE == kModeRowMax && row_ok) {
-    a.v1[rec] = (best == -INFINITY) ? -INFINITY : best * scale;
-    a.v2[rec] = (second == -INFINITY) ? -INFINITY : second * scale;
-    a.c1[rec] = best_c;
+#pragma unroll
+    for (int m = 0; m < kTop; ++m) {
+      a.topv[rec * kTop + m] = (topv[m] == -INFINITY) ? -INFINITY : topv[m] * scale;
+      a.topc[rec * kTop + m] = topc[m];
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -403,46 +431,69 @@ __global__ void __launch_bounds__(256) kap_exact_kernel(KapArgs a) {
   }
   for (int o = 16; o > 0; o >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
   const float qn = sqrtf(s2) * (1.0f + 1.0f / 65536.0f);
+  // bound on |fp32 logit - exact| for every key of the row (largest key norm of the request)
   const float e_r = kKappa * static_cast<float>(a.sm_scale) * qn * a.knorm[b * a.num_kv_heads + kvh] * 1.001f + 1e-30f;
-  const float v1 = a.v1[gw], v2 = a.v2[gw];
   const double scale = a.sm_scale;
-  if (v1 == -INFINITY) {
-    if (lane == 0) { a.M[gw] = -INFINITY; a.err[gw] = e_r; a.rflags[gw] = 2; }
+  float tv[kTop];
+  int tc[kTop];
+#pragma unroll
+  for (int m = 0; m < kTop; ++m) { tv[m] = a.topv[gw * kTop + m]; tc[m] = a.topc[gw * kTop + m]; }
+  if (lane == 0) { a.qnorm[gw] = qn; a.err[gw] = e_r; }
+  if (tv[0] == -INFINITY) {
+    if (lane == 0) { a.M[gw] = -INFINITY; a.rflags[gw] = 2; a.c1[gw] = -1; }
     return;
   }
-  if (v2 < v1 - 2.0f * e_r) {
-    const uint16_t* kc = key_ptr(a, ri, b, kvh, a.c1[gw]);
-    const double lx = warp_dot_f64<HD>(qr, kc) * scale;
-    if (lane == 0) { a.M[gw] = lx; a.err[gw] = e_r; a.rflags[gw] = 0; }
+  // a key can hold the exact maximum only if its fp32 logit is within 2 e_r of the largest one
+  const float window = tv[0] - 2.0f * e_r;
+  if (tv[1] < window) {
+    const double lx = warp_dot_f64<HD>(qr, key_ptr(a, ri, b, kvh, tc[0])) * scale;
+    if (lane == 0) { a.M[gw] = lx; a.rflags[gw] = 0; a.c1[gw] = tc[0]; }
     return;
-  }
-  // near-tie at the top: every key whose fp32 logit is within 3 e_r of v1 is evaluated in float64
-  const float thr = v1 - 3.0f * e_r;
-  double best = -INFINITY;
-  for (int c = 0; c <= r; ++c) {
-    const uint16_t* kc = key_ptr(a, ri, b, kvh, c);
-    if (kc == nullptr) continue;
-    const float x = warp_dot_f32<HD>(qr, kc) * static_cast<float>(scale);
-    if (x < thr) continue;
-    const double lx = warp_dot_f64<HD>(qr, kc) * scale;
-    best = fmax(best, lx);
   }
   uint32_t* bits = a.hrm_bits + gw * a.words_per_row;
   for (int w = lane; w < a.words_per_row; w += 32) bits[w] = 0u;
   __syncwarp();
-  for (int c = 0; c <= r; ++c) {
-    const uint16_t* kc = key_ptr(a, ri, b, kvh, c);
-    if (kc == nullptr) continue;
-    const float x = warp_dot_f32<HD>(qr, kc) * static_cast<float>(scale);
-    if (x < thr) continue;
-    const double lx = warp_dot_f64<HD>(qr, kc) * scale;
-    if (lx == best && lane == 0) {
-      const int j = (c * a.stride) / a.block_size;
-      bits[j >> 5] |= 1u << (j & 31);
+  double best = -INFINITY;
+  int best_c = -1;
+  if (tv[kTop - 1] < window) {
+    // every candidate is among the kept top keys: evaluate them in float64
+    double ex[kTop];
+#pragma unroll
+    for (int m = 0; m < kTop; ++m) {
+      ex[m] = -INFINITY;
+      if (tv[m] >= window) ex[m] = warp_dot_f64<HD>(qr, key_ptr(a, ri, b, kvh, tc[m])) * scale;
+      if (ex[m] > best) { best = ex[m]; best_c = tc[m]; }
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int m = 0; m < kTop; ++m)
+        if (ex[m] == best) {
+          const int j = (tc[m] * a.stride) / a.block_size;
+          bits[j >> 5] |= 1u << (j & 31);
+        }
+    }
+  } else {
+    // more near-ties than kept: scan the row; fp32 screen, float64 for the survivors
+    const float thr = tv[0] - 3.0f * e_r;
+    for (int c = 0; c <= r; ++c) {
+      const uint16_t* kc = key_ptr(a, ri, b, kvh, c);
+      if (kc == nullptr) continue;
+      if (warp_dot_f32<HD>(qr, kc) * static_cast<float>(scale) < thr) continue;
+      const double lx = warp_dot_f64<HD>(qr, kc) * scale;
+      if (lx > best) { best = lx; best_c = c; }
+    }
+    for (int c = 0; c <= r; ++c) {
+      const uint16_t* kc = key_ptr(a, ri, b, kvh, c);
+      if (kc == nullptr) continue;
+      if (warp_dot_f32<HD>(qr, kc) * static_cast<float>(scale) < thr) continue;
+      if (warp_dot_f64<HD>(qr, kc) * scale == best && lane == 0) {
+        const int j = (c * a.stride) / a.block_size;
+        bits[j >> 5] |= 1u << (j & 31);
+      }
     }
   }
   __syncwarp();
-  if (lane == 0) { a.M[gw] = best; a.err[gw] = e_r; a.rflags[gw] = 1; }
+  if (lane == 0) { a.M[gw] = best; a.rflags[gw] = 1; a.c1[gw] = best_c; }
 }
 
 // ---------------------------------------------------------------------------
@@ -720,7 +771,9 @@ size_t kap_workspace_bytes(int num_reqs, int num_q_heads, int num_kv_heads, int 
   add(sizeof(int64_t) * (num_reqs + 1));
   add(sizeof(int64_t) * (num_reqs + 1));
   add(sizeof(float) * num_reqs * num_kv_heads);
-  add(sizeof(float) * w.rows);
+  add(sizeof(float) * static_cast<size_t>(num_reqs) * num_kv_heads * ((max_seqlen + block_size - 1) / block_size));
+  add(sizeof(float) * w.rows * kTop);
+  add(sizeof(int32_t) * w.rows * kTop);
   add(sizeof(float) * w.rows);
   add(sizeof(int32_t) * w.rows);
   add(sizeof(double) * w.rows);
@@ -765,8 +818,10 @@ cudaError_t launch_kap(const KapLaunch& L, cudaStream_t stream) {
   a.row_off = carve<int64_t>(p, L.num_reqs + 1);
   a.sc_off = carve<int64_t>(p, L.num_reqs + 1);
   a.knorm = carve<float>(p, static_cast<size_t>(L.num_reqs) * L.num_kv_heads);
-  a.v1 = carve<float>(p, w.rows);
-  a.v2 = carve<float>(p, w.rows);
+  a.kbnorm = carve<float>(p, static_cast<size_t>(L.num_reqs) * L.num_kv_heads * a.nqb_max);
+  a.topv = carve<float>(p, w.rows * kTop);
+  a.topc = carve<int32_t>(p, w.rows * kTop);
+  a.qnorm = carve<float>(p, w.rows);
   a.c1 = carve<int32_t>(p, w.rows);
   a.M = carve<double>(p, w.rows);
   a.err = carve<float>(p, w.rows);

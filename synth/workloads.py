@@ -308,43 +308,46 @@ def make_workload(spec: WorkloadSpec, *, with_values: bool = True) -> Workload:
 # mask noise (config 5): duplicates and invalid IDs, injected after selection
 # --------------------------------------------------------------------------- #
 def inject_mask_noise(mask: np.ndarray, mask_len: np.ndarray, lengths: Sequence[int], block_size: int,
-                      frac: float, seed: int) -> tuple:
+                      frac: float, seed: int, rows=None) -> tuple:
     """Return copies of (mask, mask_len) with duplicate and invalid block IDs spliced into
     a seeded ``frac`` of the rows.
 
     mask: int32 [B, H, nqb_max, Kmax] (-1 padded), mask_len: int32 [B, H, nqb_max].
-    Each chosen row (request b, head h, query block i < nqb_b) gets up to four extra
-    entries inserted at random positions, each one of: a copy of an entry already in
-    the row, -2, an ID >= ceil(L_b / b), or an ID > i.  Rows keep their pitch; the
-    inserted entries only use free slots past mask_len.
+    Each row (request b, head h, query block i < nqb_b) draws from its own generator, seeded by
+    (seed, b, h, i), so a row's noise depends only on the row: it is selected with probability
+    ``frac`` and then gets up to four extra entries inserted at random positions, each one of:
+    a copy of an entry already in the row, -2, an ID >= ceil(L_b / b), or an ID > i.  Rows keep
+    their pitch; inserted entries only use free slots past mask_len.  ``rows`` restricts the
+    work to the given (b, h, i) triples (others are copied unchanged).
     """
-    g = np.random.Generator(np.random.PCG64(seed))
     mask = mask.copy()
     mask_len = mask_len.copy()
     B, H, NQ, KM = mask.shape
-    for b in range(B):
+    if rows is None:
+        rows = [(b, h, i) for b in range(B) for h in range(H) for i in range(-(-int(lengths[b]) // block_size))]
+    for (b, h, i) in rows:
+        g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, b, h, i])))
+        if g.random() >= frac:
+            continue
         nqb = -(-int(lengths[b]) // block_size)
-        for h in range(H):
-            rows = np.nonzero(g.random(nqb) < frac)[0]
-            for i in rows:
-                n = int(mask_len[b, h, i])
-                room = KM - n
-                if room <= 0:
-                    continue
-                extra = []
-                for _ in range(int(min(room, g.integers(1, 5)))):
-                    kind = int(g.integers(0, 4))
-                    if kind == 0 and n > 0:
-                        extra.append(int(mask[b, h, i, g.integers(0, n)]))
-                    elif kind == 1:
-                        extra.append(-2)
-                    elif kind == 2:
-                        extra.append(nqb + int(g.integers(0, 3)))
-                    else:
-                        extra.append(i + 1 + int(g.integers(0, 3)))
-                row = list(mask[b, h, i, :n])
-                for e in extra:
-                    row.insert(int(g.integers(0, len(row) + 1)), e)
-                mask[b, h, i, :len(row)] = row
-                mask_len[b, h, i] = len(row)
+        n = int(mask_len[b, h, i])
+        room = KM - n
+        if room <= 0:
+            continue
+        extra = []
+        for _ in range(int(min(room, g.integers(1, 5)))):
+            kind = int(g.integers(0, 4))
+            if kind == 0 and n > 0:
+                extra.append(int(mask[b, h, i, g.integers(0, n)]))
+            elif kind == 1:
+                extra.append(-2)
+            elif kind == 2:
+                extra.append(nqb + int(g.integers(0, 3)))
+            else:
+                extra.append(i + 1 + int(g.integers(0, 3)))
+        row = list(mask[b, h, i, :n])
+        for e in extra:
+            row.insert(int(g.integers(0, len(row) + 1)), e)
+        mask[b, h, i, :len(row)] = row
+        mask_len[b, h, i] = len(row)
     return mask, mask_len

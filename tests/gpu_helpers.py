@@ -148,6 +148,11 @@ def assert_osk_ok(rep: OskReport):
     assert rep.max_disagree_margin <= SKIP_MARGIN_TOL, rep
 
 
+def compare_masks_rows(mask_gpu, len_gpu, rows: Dict) -> List:
+    """compare_masks restricted to the oracle's rows (no check of absent query blocks)."""
+    return compare_masks(mask_gpu, len_gpu, rows, None, None)
+
+
 def compare_masks(mask_gpu, len_gpu, rows: Dict, lengths, block_size) -> List:
     """Bit-exact comparison of M_KAP rows; a difference is accepted only between blocks whose
     oracle keys (HRM flag, score) are equal within a float64 tie.  Returns accepted ties;
@@ -176,7 +181,7 @@ def compare_masks(mask_gpu, len_gpu, rows: Dict, lengths, block_size) -> List:
         assert len(set(g.tolist())) == K
         assert (mask_gpu[b, h, i, K:] == -1).all()
     # absent query blocks
-    for b, L in enumerate(lengths):
+    for b, L in enumerate(lengths or []):
         nqb = -(-L // block_size)
         assert (len_gpu[b, :, nqb:] == 0).all()
         assert (mask_gpu[b, :, nqb:, :] == -1).all()

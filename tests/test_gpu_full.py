@@ -1,0 +1,80 @@
+"""Parity at the workloads' full sizes, in the launch configuration bench.py times: the GPU
+runs every (request, head, query block); the float64 oracle checks a seeded sample of items
+(mask rows bit-exact, skip decisions, outputs), always including each request's last block."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import synth
+from oracle import cosa_oracle as orc
+from tests import gpu_helpers as gh
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "delta_calibration.json")
+
+
+def sampled_items(spec, n, seed):
+    rng = np.random.default_rng(seed)
+    items = set()
+    for b, L in enumerate(spec.lengths):
+        nqb = -(-L // spec.block_size)
+        items.add((b, int(rng.integers(spec.num_q_heads)), nqb - 1))
+    while len(items) < n:
+        b = int(rng.integers(spec.num_reqs))
+        nqb = -(-spec.lengths[b] // spec.block_size)
+        # stratified: half the draws from the last quarter of the blocks (the heaviest rows)
+        lo = 0 if rng.random() < 0.5 else (3 * nqb) // 4
+        items.add((b, int(rng.integers(spec.num_q_heads)), int(rng.integers(lo, nqb))))
+    return sorted(items)
+
+
+def run_full(config, n_items, seed):
+    sp = synth.spec_for(config)
+    delta = json.load(open(GOLDEN))["configs"][str(config)]["delta"]
+    w = synth.make_workload(sp)
+    prm = gh.oracle_params(sp, delta)
+    pitch = gh.C.stage1_pitch(sp.budget_ppm, sp.max_seqlen, sp.block_size)
+    items = sampled_items(sp, n_items, seed)
+    dw = gh.to_device(w)
+    p = gh.cosa_params(dw, delta=delta, mask_pitch=pitch + (4 if sp.mask_noise_frac else 0))
+    mask_g, len_g = gh.run_kap(dw, p)
+    # oracle KAP on the sampled items only
+    by = {}
+    for (b, h, i) in items:
+        by.setdefault((b, h), []).append(i)
+    mask_o, len_o, rows = orc.kap_mask(w.q, w.k_cache, w.page_table, w.cu_seqlens, sp.num_q_heads,
+                                       sp.num_kv_heads, prm, p.mask_pitch, qblocks=by)
+    ties = gh.compare_masks_rows(mask_g, len_g, rows)
+    if sp.mask_noise_frac:
+        mask_g, len_g = synth.inject_mask_noise(mask_g, len_g, sp.lengths, sp.block_size, sp.mask_noise_frac,
+                                                seed=sp.seed)
+        mask_o, len_o = synth.inject_mask_noise(mask_o, len_o, sp.lengths, sp.block_size, sp.mask_noise_frac,
+                                                seed=sp.seed, rows=items)
+    out, flags = gh.run_osk(dw, p, mask_g, len_g)
+    # rows with float64 ties may legitimately differ; compare outputs on the exact rows
+    tied = {t[0] for t in ties}
+    exact = [it for it in items if it not in tied]
+    rep = gh.compare_osk(w, prm, mask_o, len_o, out, flags, exact)
+    gh.assert_osk_ok(rep)
+    return rep, flags
+
+
+def test_full_config3():
+    """32K tokens, shuffled physical pages, budgets 15 % / 5 %."""
+    rep, flags = run_full(3, 48, seed=3)
+    assert (flags == orc.SKIPPED).any()
+
+
+def test_full_config4():
+    """128K tokens, Student-t keys, budgets 10 % / 3 %: the benchmark workload."""
+    rep, flags = run_full(4, 64, seed=4)
+    assert (flags == orc.SKIPPED).any()
+
+
+def test_full_config5():
+    """Ragged batch {16K, 48K, 96K, 128K}, duplicate and invalid IDs in 5 % of the mask rows."""
+    rep, flags = run_full(5, 64, seed=5)
+    assert (flags == orc.IGNORED).sum() > 0
