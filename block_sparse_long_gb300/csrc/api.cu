@@ -9,7 +9,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
-#include "../../include/cosa.h"
+#include "cosa.h"
 #include "internal.h"
 
 namespace {

@@ -5,19 +5,21 @@
 // (block_size 64 is padded to 128 rows), its ordered list of key blocks (the
 // computation-order mask M_KAP), and the online-softmax state of its rows.
 //
-// Warp roles (224 threads):
-//   warps 0-3  softmax: thread t owns tile row t (TMEM lane t).  Per visit it reads the
-//              row of S = Q K^T from TMEM, applies the causal / length / missing-page
-//              masks, updates the running max, takes part in the tile-wide skip vote
-//              (Eq. (5): skip iff every row has m_loc - m < ln(Delta/L)), and for computed
-//              blocks writes P = exp(S - m_ref) as bf16 into TMEM for the P.V product.
-//   warp 4     K producer: scans the mask row (drops invalid and repeated IDs, keeps the
-//              first occurrence), resolves each kept block to physical pages through the
-//              page table, and TMA-gathers the K pages in mask order ("physical page
-//              jumping" and "any-order page visiting" of Sec. 4.3).
-//   warp 5     MMA: allocates TMEM, issues tcgen05.mma for S = Q K^T (double-buffered S)
-//              and O += P V (P read from TMEM, V from shared memory).
-//   warp 6     V producer: TMA-gathers V pages only for blocks the vote computed.
+// Warp roles (352 threads):
+//   warps 0-7  softmax, two warpgroups.  Thread (g, t) with g = warp / 4 and t the TMEM lane
+//              (row) owns columns [g*b/2, (g+1)*b/2) of row t.  Per visit: read the row's half of
+//              S = Q K^T from TMEM, apply the causal / length / missing-page masks, exchange the
+//              partial row maxima, update the running max, vote on the skip (Eq. (5): skip iff
+//              every row has m_loc - m < ln(Delta/L)), and for computed blocks write
+//              P = exp(S - m_ref) as bf16 into TMEM for the P.V product.
+//   warp 8     K producer: scans the mask row (drops invalid and repeated IDs, keeps the first
+//              occurrence), resolves each kept block to physical pages through the page table
+//              and TMA-gathers the K pages in mask order ("physical page jumping" and "any-order
+//              page visiting" of Sec. 4.3).
+//   warp 9     MMA: owns TMEM; issues tcgen05.mma for S = Q K^T (double-buffered S) and
+//              O += P V (P from TMEM, V from shared memory), each as soon as its own inputs
+//              are ready, polling without blocking.
+//   warp 10    V producer: TMA-gathers V pages only for blocks the vote computed.
 //
 // The running max m used by the skip rule is exact for the fp32 logits.  The reference
 // max m_ref used for the exponentials lags it by up to 2^8 (rescaling O in TMEM only
@@ -32,7 +34,9 @@
 namespace cosa {
 namespace {
 
-constexpr int kThreads = 224;
+constexpr int kThreads = 352;
+constexpr int kSoftmaxThreads = 256;
+constexpr int kWarpK = 8, kWarpMma = 9, kWarpV = 10;
 constexpr int kMaxBlocksPerReq = 32768;  // dedupe bitmap capacity (blocks of one request)
 constexpr int kMaxPagesPerBlock = 8;
 constexpr float kRescaleLog2 = 8.0f;     // lazy-rescale threshold, log2 units
@@ -66,8 +70,10 @@ struct alignas(1024) OskSmem {
   KInfo kinfo[NK];
   KInfo sinfo[2];
   KInfo vreq[4];
+  float pmax[2][128];                         // partial row maxima of the two column halves
+  float lsum[2][128];                         // partial row sums, exchanged at the end
   int32_t dec[2];
-  int32_t vote[2][4];
+  int32_t vote[2][8];
   uint32_t tmem_base;
   int32_t abort_flag;
   uint32_t seen[kMaxBlocksPerReq / 32];
@@ -94,13 +100,25 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __all_sync(0xffffffffu, wait_parity_bounded(bar, parity, abort_flag, status));
 }
 
+template <int N>
+__device__ __forceinline__ void tmem_st_n(uint32_t taddr, const uint32_t (&r)[N]) {
+  if constexpr (N == 32) {
+    tmem_st32(taddr, r);
+  } else {
+    static_assert(N == 16, "16 or 32 columns");
+    tmem_st16(taddr, r);
+  }
+}
+
 template <int BLK, int HD>
 __global__ void __launch_bounds__(kThreads, 1)
     osk_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                const __grid_constant__ CUtensorMap vmap, const OskArgs a) {
   using S = OskSmem<BLK, HD>;
   constexpr int NK = S::NK, NV = S::NV;
-  constexpr int DH = HD / 64;  // 64-wide d chunks
+  constexpr int DH = HD / 64;       // 64-wide d chunks
+  constexpr int SC = BLK / 2;       // S columns per softmax thread
+  constexpr int OC = HD / 2;        // O columns per softmax thread
   extern __shared__ uint8_t smem_raw[];
   S& sm = *reinterpret_cast<S*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -126,6 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int P = a.page_size;
   const int pages_per_blk = BLK / P;
+  const uint32_t all_pages = (1u << pages_per_blk) - 1u;
   const int req_pages = (L + P - 1) / P;
   const size_t row_base = ((static_cast<size_t>(b) * a.num_q_heads + h) * a.nqb_max + i);
   const int32_t* mask_row = a.mask + row_base * a.mask_pitch;
@@ -141,8 +160,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < NV; ++s) { mbar_init(&sm.v_full[s], 1); mbar_init(&sm.v_free[s], 1); }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&sm.s_full[s], 2);   // plain arrive (visit info) + UMMA commit
-      mbar_init(&sm.s_free[s], 4);   // one per softmax warp
-      mbar_init(&sm.p_full[s], 4);
+      mbar_init(&sm.s_free[s], 8);   // one per softmax warp
+      mbar_init(&sm.p_full[s], 8);
       mbar_init(&sm.o_done[s], 1);
     }
     for (int s = 0; s < 4; ++s) mbar_init(&sm.vreq_full[s], 1);
@@ -150,18 +169,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     sm.abort_flag = 0;
     fence_mbarrier_init();
   }
-  if (warp == 5) {
+  if (warp == kWarpMma) {
     tmem_alloc(&sm.tmem_base, kTmemCols);
     tmem_relinquish();
   }
-  // zero the operand tiles once: pages that do not exist are never loaded, and padding
-  // rows of a 64-row query block must hold finite values
-  {
-    uint4* z = reinterpret_cast<uint4*>(&sm.q[0]);
-    const int n16 = (128 * HD * 2 + NK * S::TILE + NV * S::TILE) / 16;
-    for (int e = threadIdx.x; e < n16; e += kThreads) z[e] = make_uint4(0, 0, 0, 0);
+  // padding rows 64..127 of a 64-row query block must hold finite values (their S rows are
+  // discarded, but the UMMA reads them)
+  if (BLK < 128) {
+    for (int e = threadIdx.x; e < DH * 64 * 8; e += kThreads) {
+      const int dh = e / (64 * 8), rem = e % (64 * 8);
+      reinterpret_cast<uint4*>(&sm.q[dh * 128 * 128 + 64 * 128])[rem] = make_uint4(0, 0, 0, 0);
+    }
   }
-  if (warp == 4) {
+  if (warp == kWarpK) {
     for (int w = lane_id(); w < (nblk + 31) / 32; w += 32) sm.seen[w] = 0u;
     if (flags_row)
       for (int k = n_entries + lane_id(); k < a.mask_pitch; k += 32) flags_row[k] = kVisitIgnored;
@@ -172,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
 
-  if (warp == 4) {
+  if (warp == kWarpK) {
     // =========================== K producer ===========================
     const uint32_t lane = lane_id();
     if (lane == 0) {
@@ -258,56 +278,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (issued > 0) wait_parity_bounded(&sm.k_full[s], (issued - 1) & 1, nullptr, nullptr);
       }
     }
-  } else if (warp == 5) {
-    // =========================== MMA issuer ===========================
-    const uint32_t lane = lane_id();
-    constexpr uint32_t idesc_qk = idesc_bf16_f32(128, BLK, false, false);
-    constexpr uint32_t idesc_pv = idesc_bf16_f32(128, HD, false, true);
-    bool ok = warp_wait(&sm.q_full, 0, abort_flag, a.status);
-    tc_fence_after();
-    // issue S(v) = Q K_v^T; returns 1 if issued, 0 at the end of the list, -1 on abort
-    auto issue_qk = [&](int vv) -> int {
-      const int slot = vv % NK;
-      if (!warp_wait(&sm.k_full[slot], (vv / NK) & 1, abort_flag, a.status)) return -1;
-      const int sb = vv & 1;
-      if (vv >= 2 && !warp_wait(&sm.s_free[sb], ((vv >> 1) - 1) & 1, abort_flag, a.status)) return -1;
-      const KInfo ki = sm.kinfo[slot];
-      if (lane == 0) {
-        sm.sinfo[sb] = ki;
-        mbar_arrive(&sm.s_full[sb]);
-      }
-      if (ki.blk < 0) {
-        if (lane == 0) mbar_arrive(&sm.s_full[sb]);
-        return 0;
-      }
+  } else if (warp == kWarpMma) {
+    // =========================== MMA issuer (lane 0) ===========================
+    if (lane_id() == 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, BLK, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, HD, false, true);
+      bool ok = wait_parity_bounded(&sm.q_full, 0, abort_flag, a.status);
       tc_fence_after();
-      if (lane == 0) {
-        const uint32_t d = tmem + (sb ? kTmemS1 : kTmemS0);
+      int nq = 0;           // next visit whose S = Q K^T is to be issued
+      int np = 0;           // next visit whose decision is to be consumed
+      int c = 0;            // computed visits so far (P.V issued)
+      int n_total = -1;     // number of visits, known once the end marker arrives
+      bool pending_pv = false;
+      uint64_t last = 0;
+      uint32_t idle = 0;
+      while (ok) {
+        bool progress = false;
+        // S(nq) = Q K_nq^T as soon as K_nq has landed and the S buffer is free
+        if (n_total < 0 && nq <= np + 1) {
+          const int slot = nq % NK, sb = nq & 1;
+          if (mbar_test_wait(&sm.k_full[slot], (nq / NK) & 1) &&
+              (nq < 2 || mbar_test_wait(&sm.s_free[sb], ((nq >> 1) - 1) & 1))) {
+            const KInfo ki = sm.kinfo[slot];
+            sm.sinfo[sb] = ki;
+            mbar_arrive(&sm.s_full[sb]);
+            if (ki.blk < 0) {
+              mbar_arrive(&sm.s_full[sb]);
+              n_total = nq;
+            } else {
+              tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint64_t ad = smem_desc_sw128(smem_u32(&sm.q[(kk >> 2) * 128 * 128 + (kk & 3) * 32]), 16, 1024);
-          const uint64_t bd = smem_desc_sw128(smem_u32(&sm.k[slot][(kk >> 2) * S::HALF + (kk & 3) * 32]), 16, 1024);
-          umma_ss(d, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+              for (int kk = 0; kk < HD / 16; ++kk) {
+                const uint64_t ad = smem_desc_sw128(smem_u32(&sm.q[(kk >> 2) * 128 * 128 + (kk & 3) * 32]), 16, 1024);
+                const uint64_t bd =
+                    smem_desc_sw128(smem_u32(&sm.k[slot][(kk >> 2) * S::HALF + (kk & 3) * 32]), 16, 1024);
+                umma_ss(tmem + (sb ? kTmemS1 : kTmemS0), ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+              }
+              umma_commit(&sm.s_full[sb]);
+              umma_commit(&sm.k_free[slot]);
+              ++nq;
+            }
+            progress = true;
+          }
         }
-        umma_commit(&sm.s_full[sb]);
-        umma_commit(&sm.k_free[slot]);
-      }
-      __syncwarp();
-      return 1;
-    };
-    int c = 0;  // computed visits so far
-    if (ok) {
-      int more = issue_qk(0);
-      int v = 0;
-      while (more == 1) {
-        more = issue_qk(v + 1);
-        if (more < 0) break;
-        if (!warp_wait(&sm.p_full[v & 1], (v >> 1) & 1, abort_flag, a.status)) break;
-        if (sm.dec[v & 1]) {
-          const int slot = c % NV;
-          if (!warp_wait(&sm.v_full[slot], (c / NV) & 1, abort_flag, a.status)) break;
-          tc_fence_after();
-          if (lane == 0) {
+        // O += P V for visit np once the vote computed it and V has landed
+        if (np < nq) {
+          if (!pending_pv && mbar_test_wait(&sm.p_full[np & 1], (np >> 1) & 1)) {
+            if (sm.dec[np & 1]) pending_pv = true;
+            else ++np;
+            progress = true;
+          }
+          if (pending_pv && mbar_test_wait(&sm.v_full[c % NV], (c / NV) & 1)) {
+            tc_fence_after();
+            const int slot = c % NV;
             const uint32_t pcol = (c & 1) ? kTmemP1 : kTmemP0;
 #pragma unroll
             for (int kk = 0; kk < BLK / 16; ++kk) {
@@ -316,20 +339,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             umma_commit(&sm.v_free[slot]);
             umma_commit(&sm.o_done[c & 1]);
+            ++c;
+            ++np;
+            pending_pv = false;
+            progress = true;
           }
-          __syncwarp();
-          ++c;
         }
-        ++v;
+        if (n_total >= 0 && np >= n_total) break;
+        if (progress) {
+          idle = 0;
+        } else if ((++idle & 255u) == 0) {
+          const uint64_t now = global_timer_ns();
+          if (idle == 256) last = now;
+          if (*abort_flag) break;
+          if (now - last > COSA_WAIT_BUDGET_NS) {
+            *abort_flag = 1;
+            report_status(a.status, kStatusDeviceTimeout);
+            break;
+          }
+        }
       }
-    }
-    // make sure every issued UMMA finished before TMEM is released
-    if (lane == 0) {
+      // every issued UMMA finishes before TMEM is released
       umma_commit(&sm.cleanup);
       wait_parity_bounded(&sm.cleanup, 0, nullptr, nullptr);
     }
     __syncwarp();
-  } else if (warp == 6) {
+  } else if (warp == kWarpV) {
     // =========================== V producer ===========================
     const uint32_t lane = lane_id();
     int c = 0;
@@ -342,6 +377,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (c >= NV && !warp_wait(&sm.v_free[slot], ((c / NV) - 1) & 1, abort_flag, a.status)) {
         ok = false;
         break;
+      }
+      if (r.pages != all_pages) {
+        // rows of pages that do not exist are zero: P is 0 there, and 0 * V must stay 0
+        for (int u = 0; u < pages_per_blk; ++u) {
+          if ((r.pages >> u) & 1u) continue;
+          for (int dh = 0; dh < DH; ++dh) {
+            uint4* z = reinterpret_cast<uint4*>(&sm.v[slot][dh * S::HALF + u * P * 128]);
+            for (int e = lane; e < P * 8; e += 32) z[e] = make_uint4(0, 0, 0, 0);
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
       }
       if (lane == 0) {
         const uint32_t bytes = static_cast<uint32_t>(__popc(r.pages)) * DH * P * 128u;
@@ -362,30 +409,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // =========================== softmax warpgroup (warps 0-3) ===========================
-    const int t = threadIdx.x;            // tile row == TMEM lane
+    // =========================== softmax warpgroups (warps 0-7) ===========================
+    const int g = warp >> 2;              // column half
+    const int t = (warp & 3) * 32 + static_cast<int>(lane_id());   // tile row == TMEM lane
     const uint32_t lane = lane_id();
-    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int col0 = g * SC;              // first S column of this thread
     const int pos = i * BLK + t;          // token position of this row inside the request
     const bool row_valid = (t < BLK) && (pos < L);
     const bool use_skip = a.skip_delta > 0.0;
     const float tau2 = use_skip ? static_cast<float>(log2(a.skip_delta / static_cast<double>(L))) : 0.0f;
     const float sl2 = a.scale_log2;
-    const uint32_t all_pages = (pages_per_blk >= 32) ? 0xffffffffu : ((1u << pages_per_blk) - 1u);
     const int pshift = __ffs(P) - 1;
+    const bool leader = threadIdx.x == 0;
     float m_run = -INFINITY;   // running max (log2 units), Algorithm A line 13
     float m_ref = -INFINITY;   // max the exponentials are taken against
-    float l_sum = 0.0f;
+    float l_part = 0.0f;       // this half's share of the row sum l
     int c = 0;                 // computed visits
     bool ok = true;
     bool local_fail = false;   // a wait of this warp ran out after the last vote
     for (int v = 0;; ++v) {
       const int sb = v & 1;
-      // vote code of this warp: bit 0 some row wants the block computed, bit 1 abort, bit 2 end of list
+      const uint32_t sbase = tmem + lane_addr + (sb ? kTmemS1 : kTmemS0) + col0;
+      // vote code of this warp: bit 0 some row wants the block computed, bit 1 abort, bit 2 end
       int code = 0;
       KInfo ki;
-      float s[BLK];
-      float m_loc = -INFINITY, m_new = m_run;
+      float sv[SC];
       bool okw = !local_fail && wait_parity_bounded(&sm.s_full[sb], (v >> 1) & 1, abort_flag, a.status);
       okw = __all_sync(0xffffffffu, okw);
       if (!okw) {
@@ -396,15 +445,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           code = 4;
         } else {
           tc_fence_after();
-          const uint32_t sbase = tmem + lane_addr + (sb ? kTmemS1 : kTmemS0);
 #pragma unroll
-          for (int cc = 0; cc < BLK / 32; ++cc) {
+          for (int cc = 0; cc < SC / 32; ++cc) {
             uint32_t r[32];
             tmem_ld32(sbase + cc * 32, r);
-            tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) s[cc * 32 + e] = __uint_as_float(r[e]);
+            for (int e = 0; e < 32; ++e) sv[cc * 32 + e] = __uint_as_float(r[e]);
           }
+          tmem_wait_ld();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm.s_free[sb]);
@@ -414,36 +462,45 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (need_mask) {
             const int lim = row_valid ? min(pos, L - 1) - key0 : -1;  // last visible column
 #pragma unroll
-            for (int e = 0; e < BLK; ++e) {
-              const bool page_ok = (ki.pages >> (e >> pshift)) & 1u;
-              if (e > lim || !page_ok) s[e] = -INFINITY;
-            }
+            for (int e = 0; e < SC; ++e)
+              if (col0 + e > lim || !((ki.pages >> ((col0 + e) >> pshift)) & 1u)) sv[e] = -INFINITY;
           }
-          float mx = s[0];
+          float m8[8];
 #pragma unroll
-          for (int e = 1; e < BLK; ++e) mx = fmaxf(mx, s[e]);
-          m_loc = (mx == -INFINITY) ? -INFINITY : mx * sl2;
-          m_new = fmaxf(m_run, m_loc);
-          bool want = true;
-          if (use_skip) want = row_valid && (m_loc != -INFINITY) && (m_loc - m_new >= tau2);
-          code = (__ballot_sync(0xffffffffu, want) != 0u) ? 1 : 0;
+          for (int q = 0; q < 8; ++q) m8[q] = sv[q];
+#pragma unroll
+          for (int e = 8; e < SC; ++e) m8[e & 7] = fmaxf(m8[e & 7], sv[e]);
+          sm.pmax[g][t] = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
         }
       }
+      named_bar_sync(1, kSoftmaxThreads);   // partial maxima of both halves are in
+      float m_new = m_run;
+      if (code == 0) {
+        const float mx = fmaxf(sm.pmax[0][t], sm.pmax[1][t]);
+        const float m_loc = (mx == -INFINITY) ? -INFINITY : mx * sl2;
+        m_new = fmaxf(m_run, m_loc);
+        bool want = true;
+        if (use_skip) want = row_valid && (m_loc != -INFINITY) && (m_loc - m_new >= tau2);
+        code = (__ballot_sync(0xffffffffu, want) != 0u) ? 1 : 0;
+      }
       if (lane == 0) sm.vote[sb][warp] = code;
-      named_bar_sync(1, 128);
-      const int all = sm.vote[sb][0] | sm.vote[sb][1] | sm.vote[sb][2] | sm.vote[sb][3];
+      named_bar_sync(2, kSoftmaxThreads);   // every warp's vote is in
+      int all = 0;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) all |= sm.vote[sb][w];
       if (all & 2) { ok = false; break; }
       if (all & 4) break;
       const bool compute = (all & 1) != 0;
       m_run = m_new;
-      if (t == 0 && flags_row) flags_row[ki.k] = compute ? kVisitComputed : kVisitSkipped;
+      if (leader && flags_row) flags_row[ki.k] = compute ? kVisitComputed : kVisitSkipped;
       if (!compute) {
-        if (t == 0) sm.dec[sb] = 0;
+        if (leader) sm.dec[sb] = 0;
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.p_full[sb]);
         continue;
       }
-      if (t == 0) {
+      if (leader) {
         sm.dec[sb] = 1;
         sm.vreq[c & 3] = ki;
         mbar_arrive(&sm.vreq_full[c & 3]);
@@ -456,16 +513,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (rescale) {
         alpha = ex2_approx(m_ref - m_new);
         m_ref = m_new;
-        l_sum *= alpha;
+        l_part *= alpha;
       }
       if (__any_sync(0xffffffffu, rescale) && c > 0) {
-        // O must hold every earlier P.V before it is scaled
+        // O must hold every earlier P.V before it is scaled (this half's O columns)
         bool okr = wait_parity_bounded(&sm.o_done[(c - 1) & 1], ((c - 1) >> 1) & 1, abort_flag, a.status);
         if (!__all_sync(0xffffffffu, okr)) { local_fail = true; continue; }
         tc_fence_after();
-        const uint32_t ob = tmem + lane_addr + kTmemO;
+        const uint32_t ob = tmem + lane_addr + kTmemO + g * OC;
 #pragma unroll
-        for (int cc = 0; cc < HD / 32; ++cc) {
+        for (int cc = 0; cc < OC / 32; ++cc) {
           uint32_t r[32];
           tmem_ld32(ob + cc * 32, r);
           tmem_wait_ld();
@@ -475,49 +532,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_wait_st();
       }
+      // P = exp2(S * scale * log2(e) - m_ref) as bf16 pairs; masked entries are -inf -> 0
+      const float base = (m_ref == -INFINITY) ? 0.0f : m_ref;
+      uint32_t pk[SC / 2];
+      float rs4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int e = 0; e < SC / 2; ++e) {
+        const float p0 = ex2_approx(fmaf(sv[2 * e], sl2, -base));
+        const float p1 = ex2_approx(fmaf(sv[2 * e + 1], sl2, -base));
+        rs4[e & 3] += p0 + p1;
+        pk[e] = pack_bf16x2(p0, p1);
+      }
+      l_part += (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
       // the P buffer written now was read by the P.V two computed visits ago
       if (c >= 2) {
         bool okp = wait_parity_bounded(&sm.o_done[c & 1], ((c - 2) >> 1) & 1, abort_flag, a.status);
         if (!__all_sync(0xffffffffu, okp)) { local_fail = true; continue; }
       }
       tc_fence_after();
-      // P = exp2(S * scale * log2(e) - m_ref), bf16 pairs, 64 columns per TMEM store
-      const float base = (m_ref == -INFINITY) ? 0.0f : m_ref;
-      float rs = 0.0f;
-      const uint32_t pb = tmem + lane_addr + ((c & 1) ? kTmemP1 : kTmemP0);
-#pragma unroll
-      for (int cc = 0; cc < BLK / 64; ++cc) {
-        uint32_t r[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float x0 = s[cc * 64 + 2 * e], x1 = s[cc * 64 + 2 * e + 1];
-          const float p0 = (x0 == -INFINITY) ? 0.0f : ex2_approx(fmaf(x0, sl2, -base));
-          const float p1 = (x1 == -INFINITY) ? 0.0f : ex2_approx(fmaf(x1, sl2, -base));
-          rs += p0 + p1;
-          r[e] = pack_bf16x2(p0, p1);
-        }
-        tmem_st32(pb + cc * 32, r);
-      }
+      tmem_st_n<SC / 2>(tmem + lane_addr + ((c & 1) ? kTmemP1 : kTmemP0) + g * (SC / 2), pk);
       tmem_wait_st();
-      l_sum += rs;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.p_full[sb]);
       ++c;
     }
-    if (t == 0) {
+    if (leader) {
       sm.vreq[c & 3].blk = -1;
       mbar_arrive(&sm.vreq_full[c & 3]);
     }
     // ---------------- epilogue: O / l -> bf16 -> global ----------------
     if (ok && c > 0) ok = wait_parity_bounded(&sm.o_done[(c - 1) & 1], ((c - 1) >> 1) & 1, abort_flag, a.status);
     tc_fence_after();
+    sm.lsum[g][t] = l_part;
+    named_bar_sync(1, kSoftmaxThreads);
+    const float l_sum = sm.lsum[0][t] + sm.lsum[1][t];
     const float inv_l = (l_sum > 0.0f) ? 1.0f / l_sum : 0.0f;
     uint8_t* stage = &sm.q[0];  // every UMMA reading Q has completed
+    constexpr int CH = HD / 8;  // 16-byte chunks per output row
     {
-      const uint32_t ob = tmem + lane_addr + kTmemO;
+      const uint32_t ob = tmem + lane_addr + kTmemO + g * OC;
 #pragma unroll
-      for (int cc = 0; cc < HD / 32; ++cc) {
+      for (int cc = 0; cc < OC / 32; ++cc) {
         uint32_t r[32];
         if (c > 0) {
           tmem_ld32(ob + cc * 32, r);
@@ -534,18 +590,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           w.y = pack_bf16x2(__uint_as_float(r[q4 * 8 + 2]) * inv_l, __uint_as_float(r[q4 * 8 + 3]) * inv_l);
           w.z = pack_bf16x2(__uint_as_float(r[q4 * 8 + 4]) * inv_l, __uint_as_float(r[q4 * 8 + 5]) * inv_l);
           w.w = pack_bf16x2(__uint_as_float(r[q4 * 8 + 6]) * inv_l, __uint_as_float(r[q4 * 8 + 7]) * inv_l);
-          const int chunk = cc * 4 + q4;                       // 16-byte chunk of the row
-          const int phys_chunk = chunk ^ (t & (HD / 8 - 1));
+          const int chunk = (g * OC) / 8 + cc * 4 + q4;   // 16-byte chunk of the row
+          const int phys_chunk = chunk ^ (t & (CH - 1));
           *reinterpret_cast<uint4*>(stage + t * (HD * 2) + phys_chunk * 16) = w;
         }
       }
     }
-    named_bar_sync(1, 128);
+    named_bar_sync(2, kSoftmaxThreads);
     {
-      constexpr int CH = HD / 8;  // 16-byte chunks per row
       const int rows = min(BLK, L - i * BLK);
       uint8_t* out = reinterpret_cast<uint8_t*>(a.out);
-      for (int e = t; e < rows * CH; e += 128) {
+      const int tid = g * 128 + t;
+      for (int e = tid; e < rows * CH; e += kSoftmaxThreads) {
         const int r = e / CH, chunk = e % CH;
         const uint4 w = *reinterpret_cast<const uint4*>(stage + r * (HD * 2) + ((chunk ^ (r & (CH - 1))) * 16));
         const size_t tok = static_cast<size_t>(tok0) + static_cast<size_t>(i) * BLK + r;
@@ -556,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -588,7 +644,8 @@ cudaError_t launch_osk_t(const OskLaunch& L, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(osk_kernel<BLK, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  const long long items = static_cast<long long>(L.num_kv_heads) * a.nqb_max * L.num_reqs * (L.num_q_heads / L.num_kv_heads);
+  const long long items =
+      static_cast<long long>(L.num_kv_heads) * a.nqb_max * L.num_reqs * (L.num_q_heads / L.num_kv_heads);
   if (items <= 0) return cudaSuccess;
   osk_kernel<BLK, HD><<<static_cast<unsigned>(items), kThreads, smem, stream>>>(L.qmap, L.kmap, L.vmap, a);
   return cudaGetLastError();
