@@ -16,9 +16,8 @@
 //              occurrence), resolves each kept block to physical pages through the page table
 //              and TMA-gathers the K pages in mask order ("physical page jumping" and "any-order
 //              page visiting" of Sec. 4.3).
-//   warp 9     MMA: owns TMEM; issues tcgen05.mma for S = Q K^T (double-buffered S) and
-//              O += P V (P from TMEM, V from shared memory), each as soon as its own inputs
-//              are ready, polling without blocking.
+//   warp 9     MMA: owns TMEM; issues tcgen05.mma for S = Q K^T (double-buffered S, two
+//              visits ahead of the softmax) and O += P V (P from TMEM, V from shared memory).
 //   warp 10    V producer: TMA-gathers V pages only for blocks the vote computed.
 //
 // The running max m used by the skip rule is exact for the fp32 logits.  The reference
@@ -63,16 +62,17 @@ struct alignas(1024) OskSmem {
   uint64_t k_full[NK], k_free[NK];
   uint64_t v_full[NV], v_free[NV];
   uint64_t s_full[2], s_free[2];
-  uint64_t p_full[2];
+  uint64_t p_full[4];
   uint64_t o_done[2];
   uint64_t vreq_full[4];
   uint64_t cleanup;
   KInfo kinfo[NK];
   KInfo sinfo[2];
   KInfo vreq[4];
+  KInfo stash[2];                             // visit info kept by the softmax leader past s_free
   float pmax[2][128];                         // partial row maxima of the two column halves
   float lsum[2][128];                         // partial row sums, exchanged at the end
-  int32_t dec[2];
+  int32_t dec[4];
   int32_t vote[2][8];
   uint32_t tmem_base;
   int32_t abort_flag;
@@ -161,9 +161,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&sm.s_full[s], 2);   // plain arrive (visit info) + UMMA commit
       mbar_init(&sm.s_free[s], 8);   // one per softmax warp
-      mbar_init(&sm.p_full[s], 8);
       mbar_init(&sm.o_done[s], 1);
     }
+    for (int s = 0; s < 4; ++s) mbar_init(&sm.p_full[s], 8);
     for (int s = 0; s < 4; ++s) mbar_init(&sm.vreq_full[s], 1);
     mbar_init(&sm.cleanup, 1);
     sm.abort_flag = 0;
@@ -280,83 +280,67 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kWarpMma) {
     // =========================== MMA issuer (lane 0) ===========================
+    // Event order per visit v: S(v+2) may start once the softmax has read S(v) (the buffer it
+    // reuses) and K(v+2) has landed; P.V for v follows the vote on v.  Waiting in that order
+    // with suspending waits keeps this warp off the issue slots the softmax warps need.
     if (lane_id() == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, BLK, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, HD, false, true);
       bool ok = wait_parity_bounded(&sm.q_full, 0, abort_flag, a.status);
       tc_fence_after();
-      int nq = 0;           // next visit whose S = Q K^T is to be issued
-      int np = 0;           // next visit whose decision is to be consumed
-      int c = 0;            // computed visits so far (P.V issued)
-      int n_total = -1;     // number of visits, known once the end marker arrives
-      bool pending_pv = false;
-      uint64_t last = 0;
-      uint32_t idle = 0;
-      while (ok) {
-        bool progress = false;
-        // S(nq) = Q K_nq^T as soon as K_nq has landed and the S buffer is free
-        if (n_total < 0 && nq <= np + 1) {
-          const int slot = nq % NK, sb = nq & 1;
-          if (mbar_test_wait(&sm.k_full[slot], (nq / NK) & 1) &&
-              (nq < 2 || mbar_test_wait(&sm.s_free[sb], ((nq >> 1) - 1) & 1))) {
-            const KInfo ki = sm.kinfo[slot];
-            sm.sinfo[sb] = ki;
-            mbar_arrive(&sm.s_full[sb]);
-            if (ki.blk < 0) {
-              mbar_arrive(&sm.s_full[sb]);
-              n_total = nq;
-            } else {
-              tc_fence_after();
-#pragma unroll
-              for (int kk = 0; kk < HD / 16; ++kk) {
-                const uint64_t ad = smem_desc_sw128(smem_u32(&sm.q[(kk >> 2) * 128 * 128 + (kk & 3) * 32]), 16, 1024);
-                const uint64_t bd =
-                    smem_desc_sw128(smem_u32(&sm.k[slot][(kk >> 2) * S::HALF + (kk & 3) * 32]), 16, 1024);
-                umma_ss(tmem + (sb ? kTmemS1 : kTmemS0), ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
-              }
-              umma_commit(&sm.s_full[sb]);
-              umma_commit(&sm.k_free[slot]);
-              ++nq;
-            }
-            progress = true;
-          }
+      // S(vv) = Q K_vv^T; 1 issued, 0 end of the list (softmax told), -1 abort
+      auto issue_qk = [&](int vv) -> int {
+        const int slot = vv % NK, sb = vv & 1;
+        if (!wait_parity_bounded(&sm.k_full[slot], (vv / NK) & 1, abort_flag, a.status)) return -1;
+        if (vv >= 2 && !wait_parity_bounded(&sm.s_free[sb], ((vv >> 1) - 1) & 1, abort_flag, a.status)) return -1;
+        const KInfo ki = sm.kinfo[slot];
+        sm.sinfo[sb] = ki;
+        mbar_arrive(&sm.s_full[sb]);
+        if (ki.blk < 0) {
+          mbar_arrive(&sm.s_full[sb]);
+          return 0;
         }
-        // O += P V for visit np once the vote computed it and V has landed
-        if (np < nq) {
-          if (!pending_pv && mbar_test_wait(&sm.p_full[np & 1], (np >> 1) & 1)) {
-            if (sm.dec[np & 1]) pending_pv = true;
-            else ++np;
-            progress = true;
-          }
-          if (pending_pv && mbar_test_wait(&sm.v_full[c % NV], (c / NV) & 1)) {
-            tc_fence_after();
-            const int slot = c % NV;
-            const uint32_t pcol = (c & 1) ? kTmemP1 : kTmemP0;
+        tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < BLK / 16; ++kk) {
-              const uint64_t bd = smem_desc_sw128(smem_u32(&sm.v[slot][kk * 16 * 128]), S::HALF, 1024);
-              umma_ts(tmem + kTmemO, tmem + pcol + kk * 8, bd, idesc_pv, (c > 0 || kk > 0) ? 1u : 0u);
-            }
-            umma_commit(&sm.v_free[slot]);
-            umma_commit(&sm.o_done[c & 1]);
-            ++c;
-            ++np;
-            pending_pv = false;
-            progress = true;
-          }
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint64_t ad = smem_desc_sw128(smem_u32(&sm.q[(kk >> 2) * 128 * 128 + (kk & 3) * 32]), 16, 1024);
+          const uint64_t bd = smem_desc_sw128(smem_u32(&sm.k[slot][(kk >> 2) * S::HALF + (kk & 3) * 32]), 16, 1024);
+          umma_ss(tmem + (sb ? kTmemS1 : kTmemS0), ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
         }
-        if (n_total >= 0 && np >= n_total) break;
-        if (progress) {
-          idle = 0;
-        } else if ((++idle & 255u) == 0) {
-          const uint64_t now = global_timer_ns();
-          if (idle == 256) last = now;
-          if (*abort_flag) break;
-          if (now - last > COSA_WAIT_BUDGET_NS) {
-            *abort_flag = 1;
-            report_status(a.status, kStatusDeviceTimeout);
-            break;
+        umma_commit(&sm.s_full[sb]);
+        umma_commit(&sm.k_free[slot]);
+        return 1;
+      };
+      int issued = 0;       // visits whose Q K^T has been issued
+      bool ended = false;   // end of the list reached (no more Q K^T)
+      while (ok && !ended && issued < 2) {
+        const int r = issue_qk(issued);
+        if (r < 0) ok = false;
+        else if (r == 0) ended = true;
+        else ++issued;
+      }
+      int c = 0;  // computed visits so far (P.V issued)
+      for (int v = 0; ok && v < issued; ++v) {
+        if (!ended) {
+          const int r = issue_qk(v + 2);
+          if (r < 0) { ok = false; break; }
+          if (r == 0) ended = true;
+          else ++issued;
+        }
+        if (!wait_parity_bounded(&sm.p_full[v & 3], (v >> 2) & 1, abort_flag, a.status)) { ok = false; break; }
+        if (sm.dec[v & 3]) {
+          const int slot = c % NV;
+          if (!wait_parity_bounded(&sm.v_full[slot], (c / NV) & 1, abort_flag, a.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t pcol = (c & 1) ? kTmemP1 : kTmemP0;
+#pragma unroll
+          for (int kk = 0; kk < BLK / 16; ++kk) {
+            const uint64_t bd = smem_desc_sw128(smem_u32(&sm.v[slot][kk * 16 * 128]), S::HALF, 1024);
+            umma_ts(tmem + kTmemO, tmem + pcol + kk * 8, bd, idesc_pv, (c > 0 || kk > 0) ? 1u : 0u);
           }
+          umma_commit(&sm.v_free[slot]);
+          umma_commit(&sm.o_done[c & 1]);
+          ++c;
         }
       }
       // every issued UMMA finishes before TMEM is released
@@ -433,17 +417,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sbase = tmem + lane_addr + (sb ? kTmemS1 : kTmemS0) + col0;
       // vote code of this warp: bit 0 some row wants the block computed, bit 1 abort, bit 2 end
       int code = 0;
-      KInfo ki;
+      int ki_blk = -1, ki_k = 0;
+      uint32_t ki_pages = 0;
       float sv[SC];
       bool okw = !local_fail && wait_parity_bounded(&sm.s_full[sb], (v >> 1) & 1, abort_flag, a.status);
       okw = __all_sync(0xffffffffu, okw);
       if (!okw) {
         code = 2;
       } else {
-        ki = sm.sinfo[sb];
-        if (ki.blk < 0) {
+        ki_blk = sm.sinfo[sb].blk;
+        ki_pages = sm.sinfo[sb].pages;
+        ki_k = sm.sinfo[sb].k;
+        if (ki_blk < 0) {
           code = 4;
         } else {
+          if (leader) sm.stash[sb] = sm.sinfo[sb];   // sinfo is reused once S is released
           tc_fence_after();
 #pragma unroll
           for (int cc = 0; cc < SC / 32; ++cc) {
@@ -457,13 +445,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm.s_free[sb]);
           // masks: causal on the diagonal block, length on the last block, missing pages
-          const int key0 = ki.blk * BLK;
-          const bool need_mask = (ki.blk == i) || (key0 + BLK > L) || (ki.pages != all_pages) || !row_valid;
+          const int key0 = ki_blk * BLK;
+          const bool need_mask = (ki_blk == i) || (key0 + BLK > L) || (ki_pages != all_pages) || !row_valid;
           if (need_mask) {
             const int lim = row_valid ? min(pos, L - 1) - key0 : -1;  // last visible column
 #pragma unroll
             for (int e = 0; e < SC; ++e)
-              if (col0 + e > lim || !((ki.pages >> ((col0 + e) >> pshift)) & 1u)) sv[e] = -INFINITY;
+              if (col0 + e > lim || !((ki_pages >> ((col0 + e) >> pshift)) & 1u)) sv[e] = -INFINITY;
           }
           float m8[8];
 #pragma unroll
@@ -493,16 +481,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (all & 4) break;
       const bool compute = (all & 1) != 0;
       m_run = m_new;
-      if (leader && flags_row) flags_row[ki.k] = compute ? kVisitComputed : kVisitSkipped;
+      if (leader && flags_row) flags_row[ki_k] = compute ? kVisitComputed : kVisitSkipped;
       if (!compute) {
-        if (leader) sm.dec[sb] = 0;
+        if (leader) sm.dec[v & 3] = 0;
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.p_full[sb]);
+        if (lane == 0) mbar_arrive(&sm.p_full[v & 3]);
         continue;
       }
       if (leader) {
-        sm.dec[sb] = 1;
-        sm.vreq[c & 3] = ki;
+        sm.dec[v & 3] = 1;
+        sm.vreq[c & 3] = sm.stash[sb];
         mbar_arrive(&sm.vreq_full[c & 3]);
       }
       // lazy rescale of O and l when the max rises by more than 2^8
@@ -514,23 +502,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         alpha = ex2_approx(m_ref - m_new);
         m_ref = m_new;
         l_part *= alpha;
-      }
-      if (__any_sync(0xffffffffu, rescale) && c > 0) {
-        // O must hold every earlier P.V before it is scaled (this half's O columns)
-        bool okr = wait_parity_bounded(&sm.o_done[(c - 1) & 1], ((c - 1) >> 1) & 1, abort_flag, a.status);
-        if (!__all_sync(0xffffffffu, okr)) { local_fail = true; continue; }
-        tc_fence_after();
-        const uint32_t ob = tmem + lane_addr + kTmemO + g * OC;
-#pragma unroll
-        for (int cc = 0; cc < OC / 32; ++cc) {
-          uint32_t r[32];
-          tmem_ld32(ob + cc * 32, r);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-          tmem_st32(ob + cc * 32, r);
-        }
-        tmem_wait_st();
       }
       // P = exp2(S * scale * log2(e) - m_ref) as bf16 pairs; masked entries are -inf -> 0
       const float base = (m_ref == -INFINITY) ? 0.0f : m_ref;
@@ -552,9 +523,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       tmem_st_n<SC / 2>(tmem + lane_addr + ((c & 1) ? kTmemP1 : kTmemP0) + g * (SC / 2), pk);
       tmem_wait_st();
+      // O (this half's columns) is scaled once every earlier P.V has landed; P.V of this visit
+      // is issued only after p_full, so it accumulates onto the scaled O
+      if (__any_sync(0xffffffffu, rescale) && c > 0) {
+        bool okr = wait_parity_bounded(&sm.o_done[(c - 1) & 1], ((c - 1) >> 1) & 1, abort_flag, a.status);
+        if (!__all_sync(0xffffffffu, okr)) { local_fail = true; continue; }
+        tc_fence_after();
+        const uint32_t ob = tmem + lane_addr + kTmemO + g * OC;
+#pragma unroll 1
+        for (int cc = 0; cc < OC / 16; ++cc) {
+          uint32_t r[16];
+          tmem_ld16(ob + cc * 16, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+          tmem_st16(ob + cc * 16, r);
+          tmem_wait_st();
+        }
+      }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.p_full[sb]);
+      if (lane == 0) mbar_arrive(&sm.p_full[v & 3]);
       ++c;
     }
     if (leader) {
