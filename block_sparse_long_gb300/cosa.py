@@ -33,7 +33,8 @@ VISIT_COMPUTED, VISIT_SKIPPED, VISIT_IGNORED = 0, 1, 2
 
 # Every symbol include/cosa.h declares.
 EXPORTS = ("cosa_version", "cosa_status_string", "cosa_proxy_workspace_size", "cosa_proxy_select",
-           "cosa_prefill_workspace_size", "cosa_sparse_prefill")
+           "cosa_proxy_select_static", "cosa_prefill_workspace_size", "cosa_sparse_prefill")
+STATIC_SCRATCH_BYTES = 64 << 20   # COSA_STATIC_SCRATCH_BYTES
 
 
 class CosaParams(ctypes.Structure):
@@ -76,6 +77,8 @@ def library() -> ctypes.CDLL:
     lib.cosa_prefill_workspace_size.argtypes = [pp]
     lib.cosa_proxy_select.restype = ctypes.c_int
     lib.cosa_proxy_select.argtypes = [pp, vp, i32p, vp, i32p, i32p, i32p, vp, sz, i32p, vp]
+    lib.cosa_proxy_select_static.restype = ctypes.c_int
+    lib.cosa_proxy_select_static.argtypes = [pp, vp, i32p, vp, i32p, i32p, i32p, i32p, vp]
     lib.cosa_sparse_prefill.restype = ctypes.c_int
     lib.cosa_sparse_prefill.argtypes = [pp, vp, i32p, vp, vp, i32p, i32p, i32p, vp, u8p, vp, sz, i32p, vp]
     _lib = lib
@@ -174,6 +177,25 @@ def cosa_proxy_select(p: CosaParams, q: torch.Tensor, cu_seqlens: torch.Tensor, 
                                      _ptr(status), _stream_handle(stream))
     if rc != COSA_OK:
         raise CosaError(rc, "cosa_proxy_select")
+    return mask, mask_len
+
+
+def cosa_proxy_select_static(p: CosaParams, q: torch.Tensor, cu_seqlens: torch.Tensor, k_cache: torch.Tensor,
+                             page_table: torch.Tensor, mask: torch.Tensor, mask_len: torch.Tensor, *,
+                             status: Optional[torch.Tensor] = None,
+                             stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """KAP with the library's fixed device scratch instead of a workspace, for callers that cannot
+    allocate device memory.  ``mask`` and ``mask_len`` are caller-owned outputs; nothing is allocated
+    here.  Raises CosaError(COSA_ERR_WORKSPACE) when the problem needs more than STATIC_SCRATCH_BYTES."""
+    for t, n, dt in ((q, "q", torch.bfloat16), (k_cache, "k_cache", torch.bfloat16),
+                     (cu_seqlens, "cu_seqlens", torch.int32), (page_table, "page_table", torch.int32),
+                     (mask, "mask", torch.int32), (mask_len, "mask_len", torch.int32)):
+        _check(t, n, dt)
+    rc = library().cosa_proxy_select_static(ctypes.byref(p), _ptr(q), _ptr(cu_seqlens), _ptr(k_cache),
+                                            _ptr(page_table), _ptr(mask), _ptr(mask_len), _ptr(status),
+                                            _stream_handle(stream))
+    if rc != COSA_OK:
+        raise CosaError(rc, "cosa_proxy_select_static")
     return mask, mask_len
 
 

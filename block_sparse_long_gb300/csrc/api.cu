@@ -136,6 +136,19 @@ int cosa_proxy_select(const cosa_params* p, const void* q, const int32_t* cu_seq
   return e == cudaSuccess ? COSA_OK : COSA_ERR_CUDA;
 }
 
+int cosa_proxy_select_static(const cosa_params* p, const void* q, const int32_t* cu_seqlens, const void* k_cache,
+                             const int32_t* page_table, int32_t* mask, int32_t* mask_len, int32_t* device_status,
+                             void* stream) {
+  const int rc = check_common(p);
+  if (rc != COSA_OK) return rc;
+  const size_t need = cosa_proxy_workspace_size(p);
+  if (need > cosa::kStaticScratchBytes) return COSA_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  if (cosa::kap_static_scratch(&scratch) != cudaSuccess) return COSA_ERR_CUDA;
+  return cosa_proxy_select(p, q, cu_seqlens, k_cache, page_table, mask, mask_len, scratch, cosa::kStaticScratchBytes,
+                           device_status, stream);
+}
+
 size_t cosa_prefill_workspace_size(const cosa_params* p) {
   (void)p;
   return 0;

@@ -26,11 +26,17 @@
 //                                 order, and the budget cut, that the bounds cannot certify is
 //                                 recomputed with float64 logits and exp, and re-sorted.
 #include <cstdint>
+#include <mutex>
+
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "internal.h"
 #include "ptx.cuh"
+
+// Fixed scratch for callers that cannot allocate device memory (cosa_proxy_select_static).
+// Every GPU that loads this library holds it until the process exits; all calls share it.
+__device__ __align__(256) uint8_t cosa_kap_static_scratch[cosa::kStaticScratchBytes];
 
 namespace cosa {
 namespace {
@@ -783,6 +789,26 @@ size_t kap_workspace_bytes(int num_reqs, int num_q_heads, int num_kv_heads, int 
   add(sizeof(float) * w.scores);
   add(sizeof(float) * w.scores);
   return n + 256;
+}
+
+cudaError_t kap_static_scratch(void** ptr) {
+  // Host code cannot use the array's name as a device address: look the address up, once per
+  // device, with that device current.
+  static std::mutex mu;
+  static void* addr[kMaxStaticDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxStaticDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, cosa_kap_static_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = p;
+  }
+  *ptr = addr[dev];
+  return cudaSuccess;
 }
 
 cudaError_t launch_kap(const KapLaunch& L, cudaStream_t stream) {

@@ -85,7 +85,7 @@ typedef struct cosa_params {
   int32_t head_dim;          /* d: 64 or 128                                                  */
   int32_t block_size;        /* b: 64 or 128 (query and key block)                           */
   int32_t page_size;         /* P: 16, 32, 64 or 128, with b % P == 0                          */
-  int32_t stride;            /* s: KAP sampling stride, b % s == 0, b / s in {2,4,8,16,32}    */
+  int32_t stride;            /* s: KAP sampling stride, b % s == 0, b / s in {4, 8, 16}       */
   int32_t total_tokens;      /* T = cu_seqlens[B]                                             */
   int32_t max_seqlen;        /* >= every request length L_b; sizes grids and mask rows        */
   int32_t num_pages;         /* rows of k_cache / v_cache                                     */
@@ -127,6 +127,33 @@ size_t cosa_proxy_workspace_size(const cosa_params* p);
 int cosa_proxy_select(const cosa_params* p, const void* q, const int32_t* cu_seqlens, const void* k_cache,
                       const int32_t* page_table, int32_t* mask, int32_t* mask_len, void* workspace,
                       size_t workspace_bytes, int32_t* device_status, void* stream);
+
+/*
+ * KAP without a workspace argument, for callers that cannot allocate device memory.  (The
+ * paper has no counterpart; this is a deployment variant of cosa_proxy_select.)
+ *
+ * Some callers cannot call cudaMalloc or hand out a scratch buffer: code running inside a
+ * host framework that owns all device memory through its own allocator and exposes none to
+ * plug-ins, or a serving loop that must not enter an allocator while requests are in flight
+ * (allocation can block, synchronize the device, or fail once a pool has reserved most of
+ * HBM).  This entry point takes the same arguments as cosa_proxy_select minus the workspace
+ * and computes the same mask.  Its scratch is a fixed array of COSA_STATIC_SCRATCH_BYTES
+ * inside the library: every GPU that loads the library holds that much device memory until
+ * the process exits, and the call itself allocates nothing.
+ *
+ *   - Size limit: a problem whose cosa_proxy_workspace_size(p) exceeds COSA_STATIC_SCRATCH_BYTES
+ *     is rejected with COSA_ERR_WORKSPACE before anything is enqueued.
+ *   - The first call on a device looks up the array's device address with that device
+ *     current (a runtime call that does not allocate); make that first call before any stream
+ *     capture begins on that device.
+ *   - Every call shares the one array and leaves its contents behind; the kernels initialise
+ *     everything they read.  Calls whose work overlaps on the GPU (different streams, or
+ *     several host threads on one device) race on the array: order them on one stream.
+ */
+#define COSA_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
+int cosa_proxy_select_static(const cosa_params* p, const void* q, const int32_t* cu_seqlens, const void* k_cache,
+                             const int32_t* page_table, int32_t* mask, int32_t* mask_len, int32_t* device_status,
+                             void* stream);
 
 /*
  * OSK: ordered-skipping sparse prefill (CoSA Sec. 4.3; Algorithm A lines 7-22).

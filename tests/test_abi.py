@@ -27,7 +27,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     assert "cosa_proxy_select" in names and "cosa_sparse_prefill" in names
-    assert len(names) == 6
+    assert len(names) == 7
 
 
 def test_exports_every_declared_symbol(lib):
