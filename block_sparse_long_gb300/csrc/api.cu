@@ -54,8 +54,10 @@ int check_common(const cosa_params* p) {
   return COSA_OK;
 }
 
-bool encode_tiled(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
-                  const cuuint32_t* box) {
+}  // namespace
+
+bool cosa::encode_tiled_bf16(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
+                             const cuuint64_t* strides, const cuuint32_t* box) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint32_t es[5] = {1, 1, 1, 1, 1};
@@ -65,6 +67,11 @@ bool encode_tiled(CUtensorMap* map, const void* base, int rank, const cuuint64_t
   return r == CUDA_SUCCESS;
 }
 
+namespace {
+bool encode_tiled(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+                  const cuuint32_t* box) {
+  return cosa::encode_tiled_bf16(map, base, rank, dims, strides, box);
+}
 }  // namespace
 
 extern "C" {

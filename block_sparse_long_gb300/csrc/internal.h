@@ -12,6 +12,11 @@ constexpr uint8_t kVisitComputed = 0;
 constexpr uint8_t kVisitSkipped = 1;
 constexpr uint8_t kVisitIgnored = 2;
 
+// bf16 tiled TMA descriptor with 128-byte swizzle (dims/strides innermost first, strides in bytes
+// for dims 1..rank-1).  Returns false if the driver entry point is missing or rejects the map.
+bool encode_tiled_bf16(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
+                       const cuuint64_t* strides, const cuuint32_t* box);
+
 // ---------------------------------------------------------------------------
 // OSK
 // ---------------------------------------------------------------------------

@@ -13,13 +13,15 @@
 //
 // Exactness.  The logits run on tcgen05 tensor cores in fp32; every decision that fp32 could
 // get wrong is settled in float64:
-//   pass 1 (kap_logits<ROWMAX>)  per row: the four largest fp32 logits and their keys;
+//   gather                       the sampled queries and keys are packed into contiguous arrays;
+//   pass 1 (kap_logits<ROWMAX>)  per row: largest fp32 logit, its key, and the largest over the
+//                                 other keys (branch-free);
 //   kap_exact                    per row: error bound e_r >= |fp32 logit - exact logit| for every
 //                                 key of the row (from ||q_r|| * max ||k|| and the accumulation
 //                                 length); if the runner-up is more than 2 e_r below the maximum
 //                                 the argmax key is certain and M_r is its float64 logit;
-//                                 otherwise every key within 2 e_r is re-evaluated in float64;
-//                                 the HRM blocks of the row follow exactly;
+//   kap_rescan                   rows where it is not: every key within 3 e_r of the largest is
+//                                 re-evaluated in float64; the HRM blocks of the row follow exactly;
 //   pass 2 (kap_logits<SCORES>)  per (query block, key block): fp32 score and a rigorous bound
 //                                 on its error, given the float64 M_r;
 //   kap_select                   flag-grouped sort of the fp32 scores; every adjacent pair whose
@@ -52,7 +54,6 @@ constexpr int kSelectThreads = 256;
 // and one-large-many-small inputs was 13 * 2^-24 of sum |q_k k_k|.  The CUDA-core fp32 dot
 // products (4 sequential FMAs per lane, a 5-level shuffle tree) stay within 9 * 2^-24.
 constexpr float kKappa = 1.0f / 262144.0f;
-constexpr int kTop = 4;                 // candidates per row kept by the row-max pass
 
 struct KapArgs {
   const uint16_t* q;
@@ -67,16 +68,23 @@ struct KapArgs {
   int64_t* sc_off;       // [B+1]: first score of request b (times Hq)
   float* knorm;          // [B * Hkv]: max ||k~|| of the request's existing sampled keys
   float* kbnorm;         // [B * Hkv * nqb_max]: max ||k~|| over the sampled keys of each block
-  float* topv;           // per sampled row: kTop largest fp32 logits (scaled, descending), -inf pad
-  int32_t* topc;         // per sampled row: their key indices
+  float* v1;             // per sampled row: largest fp32 logit (scaled), -inf if none
+  float* v2;             // per sampled row: largest fp32 logit over the other keys (scaled)
+  int32_t* c1;           // per sampled row: key of v1, then the exact argmax key (first if several tie)
+  int64_t* amb;          // [0] = count, [1..] = rows whose maximum is not certain from fp32
+
   float* qnorm;          // per sampled row: ||q~_r|| rounded up
   double* M;             // per sampled row: exact maximum logit (scaled), -inf if none
   float* err;            // per sampled row: error bound e_r of its fp32 logits (scaled)
   int32_t* rflags;       // per sampled row: bit 0 = several HRM candidates (bitmap valid), bit 1 = empty
-  int32_t* c1;           // per sampled row: the exact argmax key (the first one if several tie)
   uint32_t* hrm_bits;    // per sampled row: bitmap of HRM blocks, words_per_row words (ambiguous rows only)
   float* score;          // per (request, head): nqb x nqb fp32 scores, row i = query block
   float* score_err;      // same shape: bound on |score - exact score|
+  int64_t* qs_off;       // [B+1]: first gathered query row of request b (times Hq), rows padded to 128
+  int64_t* ks_off;       // [B+1]: first gathered key row of request b (times Hkv), rows padded to 128
+  uint16_t* qs;          // gathered sampled queries, bf16 [rows, d]: row qs_off[b] + h * Rp + r
+  uint16_t* ks;          // gathered sampled keys, bf16 [rows, d]: row ks_off[b] + kvh * Rp + c (zero if absent)
+  uint32_t* kvalid;      // one bit per gathered key row: the key exists
   int num_reqs, num_q_heads, num_kv_heads, head_dim, block_size, page_size, stride, kb;
   int total_tokens, max_seqlen, num_pages, max_pages_per_req, mask_pitch, budget_ppm;
   int nqb_max, nrow_tiles_max, words_per_row;
@@ -118,15 +126,16 @@ __device__ __forceinline__ const uint16_t* query_ptr(const KapArgs& a, const Req
 
 __device__ __forceinline__ float bf16_to_f32(uint16_t x) { return __uint_as_float(static_cast<uint32_t>(x) << 16); }
 
-// 16-byte async copy; with valid == false nothing is read and the destination is zero-filled
-// (`fallback` is any mapped global address, passed so the operand is never null).
-__device__ __forceinline__ void cp_async_16(void* dst, const void* src, bool valid, const void* fallback) {
-  const uint32_t n = valid ? 16u : 0u;
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(valid ? src : fallback),
-               "r"(n)
-               : "memory");
+// eight bf16 values from a 16-byte aligned address, widened to fp32
+__device__ __forceinline__ void load8_bf16(const uint16_t* p, float (&f)[8]) {
+  const uint4 v = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
 }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // warp dot products over d (lanes split d into contiguous slices)
 template <int HD>
@@ -159,46 +168,82 @@ __device__ __forceinline__ double warp_dot_f64(const uint16_t* x, const uint16_t
 // ---------------------------------------------------------------------------
 __global__ void kap_setup_kernel(KapArgs a) {
   if (threadIdx.x == 0) {
-    int64_t ro = 0, so = 0;
+    int64_t ro = 0, so = 0, qo = 0, ko = 0;
     for (int b = 0; b < a.num_reqs; ++b) {
       a.row_off[b] = ro;
       a.sc_off[b] = so;
+      a.qs_off[b] = qo;
+      a.ks_off[b] = ko;
       const ReqInfo ri = req_info(a, b);
       if (!ri.ok) report_status(a.status, kStatusBadInput);
+      const int64_t rp = (ri.R + kRowTile - 1) / kRowTile * kRowTile;
       ro += static_cast<int64_t>(a.num_q_heads) * ri.R;
       so += static_cast<int64_t>(a.num_q_heads) * ri.nqb * ri.nqb;
+      qo += static_cast<int64_t>(a.num_q_heads) * rp;
+      ko += static_cast<int64_t>(a.num_kv_heads) * rp;
     }
     a.row_off[a.num_reqs] = ro;
     a.sc_off[a.num_reqs] = so;
+    a.qs_off[a.num_reqs] = qo;
+    a.ks_off[a.num_reqs] = ko;
+    a.amb[0] = 0;
   }
   for (int e = threadIdx.x; e < a.num_reqs * a.num_kv_heads; e += blockDim.x) a.knorm[e] = 0.0f;
   for (int e = threadIdx.x; e < a.num_reqs * a.num_kv_heads * a.nqb_max; e += blockDim.x) a.kbnorm[e] = 0.0f;
 }
 
-// max ||k~_c|| over the existing sampled keys of (request, kv head); rounded up
+// Gather the stride-sampled queries and keys of every (request, head) into contiguous, 128-row
+// padded arrays (absent keys and padding rows are zero), record which keys exist, and the largest
+// key norm per (request, kv head) and per key block.  One warp per 32 rows; grid.y walks the
+// requests' q heads then kv heads.
 template <int HD>
-__global__ void kap_knorm_kernel(KapArgs a) {
-  const int b = blockIdx.y / a.num_kv_heads, kvh = blockIdx.y % a.num_kv_heads;
+__global__ void __launch_bounds__(256) kap_gather_kernel(KapArgs a) {
+  const int nh = a.num_q_heads + a.num_kv_heads;
+  const int b = blockIdx.y / nh, hh = blockIdx.y % nh;
+  const bool is_key = hh >= a.num_q_heads;
   const ReqInfo ri = req_info(a, b);
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
-  const uint16_t* k = key_ptr(a, ri, b, kvh, c);
-  float n = 0.0f;
-  if (k != nullptr) {
+  const int rp = (ri.R + kRowTile - 1) / kRowTile * kRowTile;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r0 = (blockIdx.x * 8 + warp) * 32;
+  if (r0 >= rp) return;
+  const int head = is_key ? hh - a.num_q_heads : hh;
+  const int64_t base = is_key ? a.ks_off[b] + static_cast<int64_t>(head) * rp : a.qs_off[b] + static_cast<int64_t>(head) * rp;
+  uint16_t* dst_base = (is_key ? a.ks : a.qs) + base * HD;
+  constexpr int PER = HD / 32;  // bf16 per lane per row
+  uint32_t valid_bits = 0;
+  float blk_norm = 0.0f;        // running max over the rows of the current key block
+  for (int rr = 0; rr < 32; ++rr) {
+    const int r = r0 + rr;
+    const uint16_t* src = nullptr;
+    if (r < ri.R) src = is_key ? key_ptr(a, ri, b, head, r) : query_ptr(a, ri, head, r);
+    uint16_t v[PER];
     float s2 = 0.0f;
-    for (int e = 0; e < HD; ++e) {
-      const float x = bf16_to_f32(k[e]);
+#pragma unroll
+    for (int e = 0; e < PER; ++e) {
+      v[e] = src ? src[lane * PER + e] : static_cast<uint16_t>(0);
+      const float x = bf16_to_f32(v[e]);
       s2 = fmaf(x, x, s2);
     }
-    n = sqrtf(s2) * (1.0f + 1.0f / 65536.0f);
+    uint16_t* dst = dst_base + static_cast<int64_t>(r) * HD + lane * PER;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) dst[e] = v[e];
+    if (is_key) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+      const float n = src ? sqrtf(s2) * (1.0f + 1.0f / 65536.0f) : 0.0f;
+      if (src) valid_bits |= 1u << rr;
+      blk_norm = fmaxf(blk_norm, n);
+      const int j = (r * a.stride) / a.block_size;
+      const bool last_of_block = (rr == 31) || (((r + 1) * a.stride) / a.block_size != j);
+      if (last_of_block && lane == 0 && blk_norm > 0.0f) {
+        atomicMax(reinterpret_cast<int*>(&a.kbnorm[(static_cast<size_t>(b) * a.num_kv_heads + head) * a.nqb_max + j]),
+                  __float_as_int(blk_norm));
+        atomicMax(reinterpret_cast<int*>(&a.knorm[b * a.num_kv_heads + head]), __float_as_int(blk_norm));
+      }
+      if (last_of_block) blk_norm = 0.0f;
+    }
   }
-  if (n > 0.0f) {
-    const int j = (c * a.stride) / a.block_size;
-    atomicMax(reinterpret_cast<int*>(&a.kbnorm[(static_cast<size_t>(b) * a.num_kv_heads + kvh) * a.nqb_max + j]),
-              __float_as_int(n));
-  }
-  for (int o = 16; o > 0; o >>= 1) n = fmaxf(n, __shfl_xor_sync(0xffffffffu, n, o));
-  if ((threadIdx.x & 31) == 0 && n > 0.0f)
-    atomicMax(reinterpret_cast<int*>(&a.knorm[b * a.num_kv_heads + kvh]), __float_as_int(n));
+  if (is_key && lane == 0) a.kvalid[(base + r0) >> 5] = valid_bits;
 }
 
 // ---------------------------------------------------------------------------
@@ -206,30 +251,38 @@ __global__ void kap_knorm_kernel(KapArgs a) {
 // ---------------------------------------------------------------------------
 enum { kModeRowMax = 0, kModeScores = 1 };
 
+constexpr int kKeyStages = 4;           // K~ tiles in flight
+constexpr int kLogitsThreads = 320;      // warp 0 TMA, warp 1 UMMA, warps 2-9 epilogue
+
 template <int HD>
 struct alignas(1024) KapTileSmem {
-  uint8_t q[kRowTile * HD * 2];        // [HD/64][128][128 B] SW128
-  uint8_t k[2][kKeyTile * HD * 2];
-  uint32_t kvalid[2][kKeyTile / 32];
-  uint64_t bar[2];
+  uint8_t q[kRowTile * HD * 2];          // [HD/64][128][128 B] SW128
+  uint8_t k[kKeyStages][kKeyTile * HD * 2];
+  uint64_t q_full;
+  uint64_t k_full[kKeyStages], k_free[kKeyStages];
+  uint64_t acc_full[2], acc_free[2];
+  uint64_t cleanup;
+  float hv1[2][128], hv2[2][128];        // per column half: the row's largest and second largest logit
+  int32_t hc1[2][128];
   uint32_t tmem_base;
   int32_t abort_flag;
 };
 
-template <int HD>
-__device__ __forceinline__ void load_rows_sw128(uint8_t* dst, const uint16_t* src, bool valid, int row,
-                                                const void* fallback) {
-  // one 128-element (or 64-element) row: HD/8 chunks of 16 B into the SW128 layout
-#pragma unroll
-  for (int c16 = 0; c16 < HD / 8; ++c16) {
-    const int half = c16 >> 3, ch = c16 & 7;
-    cp_async_16(dst + half * (128 * 128) + sw128_offset(row, ch), valid ? src + c16 * 8 : nullptr, valid, fallback);
-  }
-}
-
+// Sampled logits l = q~ . k~ (fp32, tcgen05) for 128 sampled rows against every causal key tile of
+// 128 sampled keys, with one of two epilogues:
+//   ROWMAX  the four largest logits of each row and their keys (candidates for the exact maximum);
+//   SCORES  per (row, key block) the block maximum, P~ = exp(bm - M_r) with the float64 M_r, and its
+//           error bound; summed over the sampled rows of each query block into the score s_ij.
+// Warp 0 streams the K~ tiles with TMA, warp 1 issues the UMMAs into two TMEM accumulators, warps
+// 2-9 read the accumulators: warp w serves TMEM lanes 32 (w % 4) .. + 31 and columns [64 g, 64 g + 64)
+// with g = (w - 2) / 4.
 template <int HD, int KB, int MODE>
-__global__ void __launch_bounds__(128) kap_logits_kernel(KapArgs a) {
+__global__ void __launch_bounds__(kLogitsThreads, 1)
+    kap_logits_kernel(const __grid_constant__ CUtensorMap qs_map, const __grid_constant__ CUtensorMap ks_map,
+                      KapArgs a) {
   using S = KapTileSmem<HD>;
+  constexpr int DH = HD / 64;
+  constexpr int TILE = kKeyTile * HD * 2;
   extern __shared__ uint8_t smem_raw[];
   S& sm = *reinterpret_cast<S*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   int idx = blockIdx.x;
@@ -240,145 +293,152 @@ __global__ void __launch_bounds__(128) kap_logits_kernel(KapArgs a) {
   const ReqInfo ri = req_info(a, b);
   if (rt * kRowTile >= ri.R) return;
   const int kvh = h / (a.num_q_heads / a.num_kv_heads);
-  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const int r = rt * kRowTile + t;              // this thread's sampled row
-  const bool row_ok = r < ri.R;
-  const int64_t rec = a.row_off[b] + static_cast<int64_t>(h) * ri.R + r;
+  const int rp = (ri.R + kRowTile - 1) / kRowTile * kRowTile;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkt = rt + 1;                       // causal key tiles
-  const float scale = static_cast<float>(a.sm_scale);
+  const int64_t qrow0 = a.qs_off[b] + static_cast<int64_t>(h) * rp + static_cast<int64_t>(rt) * kRowTile;
+  const int64_t krow0 = a.ks_off[b] + static_cast<int64_t>(kvh) * rp;
+  volatile int* abort_flag = &sm.abort_flag;
 
-  if (t == 0) {
-    mbar_init(&sm.bar[0], 1);
-    mbar_init(&sm.bar[1], 1);
+  if (threadIdx.x == 0) {
+    mbar_init(&sm.q_full, 1);
+    for (int st = 0; st < kKeyStages; ++st) { mbar_init(&sm.k_full[st], 1); mbar_init(&sm.k_free[st], 1); }
+    for (int st = 0; st < 2; ++st) { mbar_init(&sm.acc_full[st], 1); mbar_init(&sm.acc_free[st], 8); }
+    mbar_init(&sm.cleanup, 1);
     sm.abort_flag = 0;
     fence_mbarrier_init();
   }
-  if (warp == 0) {
+  if (warp == 1) {
     tmem_alloc(&sm.tmem_base, 256);
     tmem_relinquish();
   }
-  // Q~ tile and key tile 0
-  load_rows_sw128<HD>(sm.q, row_ok ? query_ptr(a, ri, h, r) : nullptr, row_ok, t, a.q);
-  auto load_keys = [&](int kt, int buf) {
-    const int c = kt * kKeyTile + t;
-    const uint16_t* kp = key_ptr(a, ri, b, kvh, c);
-    load_rows_sw128<HD>(sm.k[buf], kp, kp != nullptr, t, a.q);
-    const unsigned bal = __ballot_sync(0xffffffffu, kp != nullptr);
-    if (lane == 0) sm.kvalid[buf][warp] = bal;
-    asm volatile("cp.async.commit_group;" ::: "memory");
-  };
-  load_keys(0, 0);
-  cp_async_wait_all();
-  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
-  constexpr uint32_t idesc = idesc_bf16_f32(128, kKeyTile, false, false);
-  auto issue = [&](int buf) {
-    if (t == 0) {
-#pragma unroll
-      for (int kk = 0; kk < HD / 16; ++kk) {
-        const uint64_t ad = smem_desc_sw128(smem_u32(&sm.q[(kk >> 2) * 128 * 128 + (kk & 3) * 32]), 16, 1024);
-        const uint64_t bd = smem_desc_sw128(smem_u32(&sm.k[buf][(kk >> 2) * 128 * 128 + (kk & 3) * 32]), 16, 1024);
-        umma_ss(tmem + buf * 128, ad, bd, idesc, kk > 0 ? 1u : 0u);
-      }
-      umma_commit(&sm.bar[buf]);
-    }
-  };
-  issue(0);
-  if (nkt > 1) load_keys(1, 1);
 
-  // per-row state
-  float topv[kTop];                             // kTop largest raw fp32 logits, descending
-  int topc[kTop];
+  if (warp == 0) {
+    // ------------------------------ TMA producer ------------------------------
+    int issued = 0;
+    if (lane == 0) {
+      tma_prefetch_desc(&qs_map);
+      tma_prefetch_desc(&ks_map);
+      mbar_arrive_expect_tx(&sm.q_full, kRowTile * HD * 2);
+      for (int dh = 0; dh < DH; ++dh)
+        tma_load_2d(&sm.q[dh * 128 * 128], &qs_map, &sm.q_full, dh * 64, static_cast<int>(qrow0));
+      for (int kt = 0; kt < nkt; ++kt) {
+        const int st = kt % kKeyStages;
+        if (kt >= kKeyStages && !wait_parity_bounded(&sm.k_free[st], ((kt / kKeyStages) - 1) & 1, abort_flag, a.status))
+          break;
+        mbar_arrive_expect_tx(&sm.k_full[st], TILE);
+        for (int dh = 0; dh < DH; ++dh)
+          tma_load_2d(&sm.k[st][dh * 128 * 128], &ks_map, &sm.k_full[st], dh * 64,
+                      static_cast<int>(krow0 + static_cast<int64_t>(kt) * kKeyTile));
+        ++issued;
+      }
+      if (*abort_flag) {
+        wait_parity_bounded(&sm.q_full, 0, nullptr, nullptr);
+        for (int st = 0; st < kKeyStages; ++st) {
+          const int n = (issued - st + kKeyStages - 1) / kKeyStages;
+          if (n > 0) wait_parity_bounded(&sm.k_full[st], (n - 1) & 1, nullptr, nullptr);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------ UMMA issuer ------------------------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128, kKeyTile, false, false);
+      bool ok = wait_parity_bounded(&sm.q_full, 0, abort_flag, a.status);
+      tc_fence_after();
+      for (int kt = 0; ok && kt < nkt; ++kt) {
+        const int st = kt % kKeyStages, ab = kt & 1;
+        if (!wait_parity_bounded(&sm.k_full[st], (kt / kKeyStages) & 1, abort_flag, a.status)) break;
+        if (kt >= 2 && !wait_parity_bounded(&sm.acc_free[ab], ((kt >> 1) - 1) & 1, abort_flag, a.status)) break;
+        tc_fence_after();
 #pragma unroll
-  for (int m = 0; m < kTop; ++m) { topv[m] = -INFINITY; topc[m] = -1; }
-  float M32 = -INFINITY, ebase = 0.0f;
-  int64_t sbase = 0;
-  int nqb = ri.nqb;
-  const float* kbn = a.kbnorm + (static_cast<size_t>(b) * a.num_kv_heads + kvh) * a.nqb_max;
-  if (MODE == kModeScores) {
-    if (row_ok) {
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint64_t ad = smem_desc_sw128(smem_u32(&sm.q[(kk >> 2) * 128 * 128 + (kk & 3) * 32]), 16, 1024);
+          const uint64_t bd = smem_desc_sw128(smem_u32(&sm.k[st][(kk >> 2) * 128 * 128 + (kk & 3) * 32]), 16, 1024);
+          umma_ss(tmem + ab * 128, ad, bd, idesc, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&sm.acc_full[ab]);
+        umma_commit(&sm.k_free[st]);
+      }
+      umma_commit(&sm.cleanup);
+      wait_parity_bounded(&sm.cleanup, 0, nullptr, nullptr);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------ epilogue (warps 2-9) ------------------------------
+    const int g = (warp - 2) >> 2;                // column half
+    const int t = (warp & 3) * 32 + lane;         // row in the tile == TMEM lane
+    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int r = rt * kRowTile + t;              // sampled row
+    const bool row_ok = r < ri.R;
+    const int64_t rec = a.row_off[b] + static_cast<int64_t>(h) * ri.R + r;
+    const float scale = static_cast<float>(a.sm_scale);
+    const uint32_t* kval = a.kvalid + (krow0 >> 5);
+    float r1 = -INFINITY, r2 = -INFINITY;     // largest and second largest raw logit of this half
+    int rc1 = -1;
+    float M32 = -INFINITY, ebase = 0.0f;
+    const int nqb = ri.nqb;
+    const int64_t sbase = a.sc_off[b] + static_cast<int64_t>(h) * nqb * nqb;
+    const float* kbn = a.kbnorm + (static_cast<size_t>(b) * a.num_kv_heads + kvh) * a.nqb_max;
+    if (MODE == kModeScores && row_ok) {
       M32 = static_cast<float>(a.M[rec]);
       ebase = kKappa * scale * a.qnorm[rec] * 1.001f;
     }
-    sbase = a.sc_off[b] + static_cast<int64_t>(h) * nqb * nqb;
-  }
-  const int qblk = r / KB;                      // query block of this row
-  bool ok = true;
-  for (int kt = 0; kt < nkt; ++kt) {
-    const int buf = kt & 1;
-    if (kt + 1 < nkt) {                         // key tile kt+1 has landed: start its UMMA
-      cp_async_wait_all();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncthreads();
+    const int qblk = r / KB;
+    for (int kt = 0; kt < nkt; ++kt) {
+      const int ab = kt & 1;
+      const bool okw = __all_sync(0xffffffffu,
+                                  wait_parity_bounded(&sm.acc_full[ab], (kt >> 1) & 1, abort_flag, a.status));
+      if (!okw) break;
       tc_fence_after();
-      issue(buf ^ 1);
-    }
-    // the whole CTA agrees on the outcome, so every thread leaves the loop together
-    ok = __syncthreads_and(wait_parity_bounded(&sm.bar[buf], (kt >> 1) & 1, &sm.abort_flag, a.status)) != 0;
-    if (!ok) break;
-    tc_fence_after();
-    uint32_t kvalid[kKeyTile / 32];
-#pragma unroll
-    for (int w = 0; w < kKeyTile / 32; ++w) kvalid[w] = sm.kvalid[buf][w];
-    __syncthreads();                            // buffer `buf` is free: UMMA kt is done, flags copied
-    if (kt + 2 < nkt) load_keys(kt + 2, buf);
-    // epilogue of key tile kt
-    const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16) + buf * 128;
-    const int last_col = r - kt * kKeyTile;     // causal: columns <= last_col
-#pragma unroll
-    for (int cc = 0; cc < kKeyTile / 32; ++cc) {
-      uint32_t rv[32];
-      tmem_ld32(taddr + cc * 32, rv);
+      uint32_t va[32], vb[32];
+      tmem_ld32(tmem + lane_addr + ab * 128 + g * 64, va);
+      tmem_ld32(tmem + lane_addr + ab * 128 + g * 64 + 32, vb);
       tmem_wait_ld();
-      const uint32_t vbits = kvalid[cc];
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.acc_free[ab]);
+      const int c0 = kt * kKeyTile + g * 64;      // key index of this thread's first column
+      const uint32_t bits0 = __ldg(kval + ((kt * kKeyTile + g * 64) >> 5));
+      const uint32_t bits1 = __ldg(kval + ((kt * kKeyTile + g * 64) >> 5) + 1);
+      const int last = r - c0;                    // causal: columns <= last
       if (MODE == kModeRowMax) {
+        // branch-free: second max = max(second, min(x, max)); argmax follows the first strict increase
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int col = cc * 32 + e;
-          if (!row_ok || col > last_col || !((vbits >> e) & 1u)) continue;
-          const float x = __uint_as_float(rv[e]);
-          if (x > topv[3]) {                    // insertion into the sorted top-4 (ties keep the first)
-            const int key = kt * kKeyTile + col;
-            if (x > topv[2]) {
-              topv[3] = topv[2]; topc[3] = topc[2];
-              if (x > topv[1]) {
-                topv[2] = topv[1]; topc[2] = topc[1];
-                if (x > topv[0]) {
-                  topv[1] = topv[0]; topc[1] = topc[0]; topv[0] = x; topc[0] = key;
-                } else {
-                  topv[1] = x; topc[1] = key;
-                }
-              } else {
-                topv[2] = x; topc[2] = key;
-              }
-            } else {
-              topv[3] = x; topc[3] = key;
-            }
-          }
+        for (int e = 0; e < 64; ++e) {
+          const uint32_t bits = e < 32 ? bits0 : bits1;
+          const bool vis = row_ok && e <= last && ((bits >> (e & 31)) & 1u);
+          const float x = vis ? __uint_as_float(e < 32 ? va[e] : vb[e - 32]) : -INFINITY;
+          r2 = fmaxf(r2, fminf(x, r1));
+          rc1 = (x > r1) ? c0 + e : rc1;
+          r1 = fmaxf(r1, x);
         }
       } else {
 #pragma unroll
-        for (int g = 0; g < 32 / KB; ++g) {
+        for (int gg = 0; gg < 64 / KB; ++gg) {
           float bm = -INFINITY;
 #pragma unroll
-          for (int e = g * KB; e < (g + 1) * KB; ++e) {
-            const int col = cc * 32 + e;
-            if (row_ok && col <= last_col && ((vbits >> e) & 1u)) bm = fmaxf(bm, __uint_as_float(rv[e]));
+          for (int e = gg * KB; e < (gg + 1) * KB; ++e) {
+            const uint32_t bits = e < 32 ? bits0 : bits1;
+            const float x = __uint_as_float(e < 32 ? va[e] : vb[e - 32]);
+            if (row_ok && e <= last && ((bits >> (e & 31)) & 1u)) bm = fmaxf(bm, x);
           }
-          const int j = kt * (kKeyTile / KB) + cc * (32 / KB) + g;
+          const int j = (c0 + gg * KB) / KB;
           float x = 0.0f, xe = 0.0f;
           if (bm != -INFINITY && M32 != -INFINITY) {
             const float u = fmaf(bm, scale, -M32);
             x = expf(u);
             // |u - exact| <= kappa * scale * ||q|| * (largest ||k|| of block j) plus the rounding of
-            // the scaled logit, of M_r and of the subtraction; expf adds at most 2 ulp; a value
-            // below exp(-80) is only bounded absolutely
+            // the scaled logit, of M_r and of the subtraction; expf adds at most 2 ulp; exp(du) - 1 <=
+            // 1.02 du for du <= 0.03; a value below exp(-80) is only bounded absolutely
             const float du = ebase * __ldg(kbn + j) + 1.2e-7f * (2.0f * fabsf(M32) + fabsf(u) + 1.0f);
-            xe = x * (expm1f(du) * 1.01f + 3.0e-7f) + ((u < -80.0f) ? 2.0e-35f : 0.0f);
+            const float rel = (du <= 0.03f) ? 1.02f * du : expm1f(du) * 1.01f;
+            xe = x * (rel + 3.0e-7f) + ((u < -80.0f) ? 2.0e-35f : 0.0f);
           }
 #pragma unroll
           for (int o = KB / 2; o > 0; o >>= 1) {
@@ -393,25 +453,34 @@ __global__ void __launch_bounds__(128) kap_logits_kernel(KapArgs a) {
         }
       }
     }
-    tc_fence_before();
-  }
-  if (MODE == kModeRowMax && row_ok) {
-#pragma unroll
-    for (int m = 0; m < kTop; ++m) {
-      a.topv[rec * kTop + m] = (topv[m] == -INFINITY) ? -INFINITY : topv[m] * scale;
-      a.topc[rec * kTop + m] = topc[m];
+    if (MODE == kModeRowMax) {
+      // merge the two column halves; half 0 writes the row's record
+      sm.hv1[g][t] = r1;
+      sm.hv2[g][t] = r2;
+      sm.hc1[g][t] = rc1;
+      named_bar_sync(1, 256);
+      if (g == 0 && row_ok) {
+        const float a1 = sm.hv1[0][t], b1 = sm.hv1[1][t];
+        const int ac = sm.hc1[0][t], bc = sm.hc1[1][t];
+        const float m1 = fmaxf(a1, b1);
+        const float m2 = fmaxf(fminf(a1, b1), fmaxf(sm.hv2[0][t], sm.hv2[1][t]));
+        const int mc = (a1 > b1 || (a1 == b1 && ac >= 0)) ? ac : bc;
+        a.v1[rec] = (m1 == -INFINITY) ? -INFINITY : m1 * scale;
+        a.v2[rec] = (m2 == -INFINITY) ? -INFINITY : m2 * scale;
+        a.c1[rec] = mc;
+      }
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 256);
   }
 }
 
 // ---------------------------------------------------------------------------
-// exact row maxima (float64) and HRM blocks of each sampled row; one warp per row
+// exact row maxima (float64) of each sampled row whose argmax fp32 certifies; one warp per row
 // ---------------------------------------------------------------------------
 template <int HD>
 __global__ void __launch_bounds__(256) kap_exact_kernel(KapArgs a) {
@@ -439,75 +508,137 @@ __global__ void __launch_bounds__(256) kap_exact_kernel(KapArgs a) {
   const float qn = sqrtf(s2) * (1.0f + 1.0f / 65536.0f);
   // bound on |fp32 logit - exact| for every key of the row (largest key norm of the request)
   const float e_r = kKappa * static_cast<float>(a.sm_scale) * qn * a.knorm[b * a.num_kv_heads + kvh] * 1.001f + 1e-30f;
-  const double scale = a.sm_scale;
-  float tv[kTop];
-  int tc[kTop];
-#pragma unroll
-  for (int m = 0; m < kTop; ++m) { tv[m] = a.topv[gw * kTop + m]; tc[m] = a.topc[gw * kTop + m]; }
+  const float v1 = a.v1[gw], v2 = a.v2[gw];
   if (lane == 0) { a.qnorm[gw] = qn; a.err[gw] = e_r; }
-  if (tv[0] == -INFINITY) {
+  if (v1 == -INFINITY) {
     if (lane == 0) { a.M[gw] = -INFINITY; a.rflags[gw] = 2; a.c1[gw] = -1; }
     return;
   }
   // a key can hold the exact maximum only if its fp32 logit is within 2 e_r of the largest one
-  const float window = tv[0] - 2.0f * e_r;
-  if (tv[1] < window) {
-    const double lx = warp_dot_f64<HD>(qr, key_ptr(a, ri, b, kvh, tc[0])) * scale;
-    if (lane == 0) { a.M[gw] = lx; a.rflags[gw] = 0; a.c1[gw] = tc[0]; }
+  if (v2 < v1 - 2.0f * e_r) {
+    const double lx = warp_dot_f64<HD>(qr, key_ptr(a, ri, b, kvh, a.c1[gw])) * a.sm_scale;
+    if (lane == 0) { a.M[gw] = lx; a.rflags[gw] = 0; }
     return;
   }
-  uint32_t* bits = a.hrm_bits + gw * a.words_per_row;
-  for (int w = lane; w < a.words_per_row; w += 32) bits[w] = 0u;
-  __syncwarp();
-  double best = -INFINITY;
-  int best_c = -1;
-  if (tv[kTop - 1] < window) {
-    // every candidate is among the kept top keys: evaluate them in float64
-    double ex[kTop];
+  // not certain from fp32: settled by kap_rescan_kernel
+  if (lane == 0) {
+    a.rflags[gw] = 1;
+    const unsigned long long slot = atomicAdd(reinterpret_cast<unsigned long long*>(&a.amb[0]), 1ull);
+    a.amb[1 + slot] = gw;
+  }
+}
+
+// Rows whose maximum fp32 cannot certify: one CTA per row (grid-stride over the queue).  Every
+// thread takes keys c = tid, tid + 256, ... of the row from the gathered arrays, screens them with an
+// fp32 dot (within 3 e_r of v1), re-evaluates the survivors in float64, and the CTA flags the blocks
+// of the keys that attain the exact maximum.
+template <int HD>
+__global__ void __launch_bounds__(256) kap_rescan_kernel(KapArgs a) {
+  constexpr int kCand = 256;
+  __shared__ float qf[HD];
+  __shared__ double cval[kCand];
+  __shared__ int ckey[kCand];
+  __shared__ int ncand;
+  __shared__ double red[8];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const long long n = a.amb[0];
+  for (long long qi = blockIdx.x; qi < n; qi += gridDim.x) {
+    const int64_t gw = a.amb[1 + qi];
+    int b = 0;
+    while (b + 1 < a.num_reqs && a.row_off[b + 1] <= gw) ++b;
+    const ReqInfo ri = req_info(a, b);
+    const int64_t local = gw - a.row_off[b];
+    const int h = static_cast<int>(local / ri.R);
+    const int r = static_cast<int>(local % ri.R);
+    const int kvh = h / (a.num_q_heads / a.num_kv_heads);
+    const int rp = (ri.R + kRowTile - 1) / kRowTile * kRowTile;
+    const uint16_t* qrow = a.qs + (a.qs_off[b] + static_cast<int64_t>(h) * rp + r) * HD;
+    const int64_t krow0 = a.ks_off[b] + static_cast<int64_t>(kvh) * rp;
+    for (int e = tid; e < HD; e += blockDim.x) qf[e] = bf16_to_f32(qrow[e]);
+    if (tid == 0) ncand = 0;
+    __syncthreads();
+    const float thr = a.v1[gw] - 3.0f * a.err[gw];
+    const float sc = static_cast<float>(a.sm_scale);
+    double best = -INFINITY;
+    bool overflow = false;
+    for (int c = tid; c <= r; c += blockDim.x) {
+      if (!((a.kvalid[(krow0 + c) >> 5] >> ((krow0 + c) & 31)) & 1u)) continue;
+      const uint16_t* kr = a.ks + (krow0 + c) * HD;
+      // four interleaved partial sums: rounding depth HD/4 + 2 stays within the fp32 bound e_r
+      float p4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 4
+      for (int e = 0; e < HD; e += 8) {
+        float kf[8];
+        load8_bf16(kr + e, kf);
 #pragma unroll
-    for (int m = 0; m < kTop; ++m) {
-      ex[m] = -INFINITY;
-      if (tv[m] >= window) ex[m] = warp_dot_f64<HD>(qr, key_ptr(a, ri, b, kvh, tc[m])) * scale;
-      if (ex[m] > best) { best = ex[m]; best_c = tc[m]; }
+        for (int i = 0; i < 8; ++i) p4[i & 3] = fmaf(qf[e + i], kf[i], p4[i & 3]);
+      }
+      const float acc = (p4[0] + p4[1]) + (p4[2] + p4[3]);
+      if (acc * sc < thr) continue;
+      double dacc = 0.0;
+      for (int e = 0; e < HD; e += 8) {
+        float kf[8];
+        load8_bf16(kr + e, kf);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dacc = fma(static_cast<double>(qf[e + i]), static_cast<double>(kf[i]), dacc);
+      }
+      const double lx = dacc * a.sm_scale;
+      best = fmax(best, lx);
+      const int slot = atomicAdd(&ncand, 1);
+      if (slot < kCand) { cval[slot] = lx; ckey[slot] = c; } else { overflow = true; }
     }
-    if (lane == 0) {
-#pragma unroll
-      for (int m = 0; m < kTop; ++m)
-        if (ex[m] == best) {
-          const int j = (tc[m] * a.stride) / a.block_size;
-          bits[j >> 5] |= 1u << (j & 31);
+    // CTA maximum of the float64 logits
+    for (int o = 16; o > 0; o >>= 1) best = fmax(best, __shfl_xor_sync(0xffffffffu, best, o));
+    if (lane == 0) red[warp] = best;
+    uint32_t* bits = a.hrm_bits + gw * a.words_per_row;
+    for (int w = tid; w < a.words_per_row; w += blockDim.x) bits[w] = 0u;
+    const int any_overflow = __syncthreads_or(overflow);
+    double M = red[0];
+    for (int w = 1; w < 8; ++w) M = fmax(M, red[w]);
+    const int nc = min(ncand, kCand);
+    if (!any_overflow) {
+      for (int x = tid; x < nc; x += blockDim.x)
+        if (cval[x] == M) {
+          const int j = (ckey[x] * a.stride) / a.block_size;
+          atomicOr(&bits[j >> 5], 1u << (j & 31));
         }
-    }
-  } else {
-    // more near-ties than kept: scan the row; fp32 screen, float64 for the survivors
-    const float thr = tv[0] - 3.0f * e_r;
-    for (int c = 0; c <= r; ++c) {
-      const uint16_t* kc = key_ptr(a, ri, b, kvh, c);
-      if (kc == nullptr) continue;
-      if (warp_dot_f32<HD>(qr, kc) * static_cast<float>(scale) < thr) continue;
-      const double lx = warp_dot_f64<HD>(qr, kc) * scale;
-      if (lx > best) { best = lx; best_c = c; }
-    }
-    for (int c = 0; c <= r; ++c) {
-      const uint16_t* kc = key_ptr(a, ri, b, kvh, c);
-      if (kc == nullptr) continue;
-      if (warp_dot_f32<HD>(qr, kc) * static_cast<float>(scale) < thr) continue;
-      if (warp_dot_f64<HD>(qr, kc) * scale == best && lane == 0) {
-        const int j = (c * a.stride) / a.block_size;
-        bits[j >> 5] |= 1u << (j & 31);
+    } else {
+      // more survivors than the candidate list holds: evaluate them again
+      for (int c = tid; c <= r; c += blockDim.x) {
+        if (!((a.kvalid[(krow0 + c) >> 5] >> ((krow0 + c) & 31)) & 1u)) continue;
+        const uint16_t* kr = a.ks + (krow0 + c) * HD;
+        float p4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        for (int e = 0; e < HD; e += 8) {
+          float kf[8];
+          load8_bf16(kr + e, kf);
+          for (int i = 0; i < 8; ++i) p4[i & 3] = fmaf(qf[e + i], kf[i], p4[i & 3]);
+        }
+        const float acc = (p4[0] + p4[1]) + (p4[2] + p4[3]);
+        if (acc * sc < thr) continue;
+        double dacc = 0.0;
+        for (int e = 0; e < HD; e += 8) {
+          float kf[8];
+          load8_bf16(kr + e, kf);
+          for (int i = 0; i < 8; ++i) dacc = fma(static_cast<double>(qf[e + i]), static_cast<double>(kf[i]), dacc);
+        }
+        if (dacc * a.sm_scale == M) {
+          const int j = (c * a.stride) / a.block_size;
+          atomicOr(&bits[j >> 5], 1u << (j & 31));
+        }
       }
     }
+    if (tid == 0) a.M[gw] = M;
+    __syncthreads();
   }
-  __syncwarp();
-  if (lane == 0) { a.M[gw] = best; a.rflags[gw] = 1; a.c1[gw] = best_c; }
 }
 
 // ---------------------------------------------------------------------------
 // per query block: flag-grouped sort, certification, float64 repair, mask row
 // ---------------------------------------------------------------------------
 // dynamic shared memory of kap_select for `cap` candidates (a power of two)
+constexpr int kRepChunk = 64;            // repaired positions per round of the float64 repair
 __host__ __device__ inline size_t select_smem_bytes(int cap) {
-  return static_cast<size_t>(cap) * (8 + 4 + 4 + 4 + 4 + 8 + 1) + 64;
+  return static_cast<size_t>(cap) * (8 + 4 + 4 + 4 + 4 + 8 + 1) + 64 + kRepChunk * 16 * sizeof(double) + 64;
 }
 
 __device__ __forceinline__ unsigned long long sort_key(bool hrm, float s, int j) {
@@ -517,7 +648,7 @@ __device__ __forceinline__ unsigned long long sort_key(bool hrm, float s, int j)
 }
 __device__ __forceinline__ int key_block(unsigned long long k) { return 0x7FFFFFFF - static_cast<int>(k & 0x7FFFFFFFull); }
 
-template <int HD>
+template <int HD, int KB>
 __global__ void __launch_bounds__(kSelectThreads) kap_select_kernel(KapArgs a, int cap) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   unsigned long long* key = reinterpret_cast<unsigned long long*>(smem_raw);  // [cap] sort keys
@@ -527,6 +658,8 @@ __global__ void __launch_bounds__(kSelectThreads) kap_select_kernel(KapArgs a, i
   float* suf = hi + cap;                                                       // [cap] suffix max of hi
   int32_t* rep_pos = reinterpret_cast<int32_t*>(suf + cap);                    // [cap] positions to repair
   uint8_t* hrm = reinterpret_cast<uint8_t*>(rep_pos + cap);                    // [cap] HRM flags
+  double* terms = reinterpret_cast<double*>(
+      (reinterpret_cast<uintptr_t>(hrm + cap) + 15) & ~uintptr_t(15));         // [kRepChunk * KB] row terms
   __shared__ int32_t n_rep_s, n_hrm_s;
 
   const int tid = threadIdx.x;
@@ -554,18 +687,15 @@ __global__ void __launch_bounds__(kSelectThreads) kap_select_kernel(KapArgs a, i
   // HRM flags of the candidates (exact, from the float64 row maxima)
   for (int j = tid; j < J; j += blockDim.x) hrm[j] = 0;
   __syncthreads();
-  if (tid < 32) {
-    for (int r = r0; r < r1; ++r) {
-      const int fl = a.rflags[rbase + r];
-      if (fl & 2) continue;
-      if (fl & 1) {
-        const uint32_t* bits = a.hrm_bits + (rbase + r) * a.words_per_row;
-        for (int j = tid; j < J; j += 32)
-          if ((bits[j >> 5] >> (j & 31)) & 1u) hrm[j] = 1;
-      } else if (tid == 0) {
-        hrm[(a.c1[rbase + r] * a.stride) / a.block_size] = 1;
-      }
-      __syncwarp();
+  if (tid < r1 - r0) {                       // one thread per sampled row of the query block
+    const int r = r0 + tid;
+    const int fl = a.rflags[rbase + r];
+    if (fl & 1) {
+      const uint32_t* bits = a.hrm_bits + (rbase + r) * a.words_per_row;
+      for (int j = 0; j < J; ++j)
+        if ((bits[j >> 5] >> (j & 31)) & 1u) hrm[j] = 1;
+    } else if (!(fl & 2)) {
+      hrm[(a.c1[rbase + r] * a.stride) / a.block_size] = 1;
     }
   }
   __syncthreads();
@@ -649,39 +779,81 @@ __global__ void __launch_bounds__(kSelectThreads) kap_select_kernel(KapArgs a, i
   __syncthreads();
   const int n_rep = n_rep_s;
   if (n_rep > 0) {
-    // exact scores, one warp per repaired block: s_ij = sum over rows r (ascending) of
-    // exp(bm[r,j] - M_r) with float64 logits
+    // exact scores s_ij = sum over rows r (ascending) of exp(bm[r,j] - M_r) with float64 logits.
+    // Warp per (position, row); lane group kgrp holds key j*KB + kgrp, its LPK lanes split d.
+    constexpr int LPK = 32 / KB;
+    constexpr int SL = HD / LPK;
     const int warps = blockDim.x / 32, w = tid >> 5, lane = tid & 31;
+    const int kgrp = lane / LPK, sub = lane % LPK;
+    const int nrows = r1 - r0;
+    const int rp = (ri.R + kRowTile - 1) / kRowTile * kRowTile;
+    const uint16_t* qbase = a.qs + (a.qs_off[b] + static_cast<int64_t>(h) * rp) * HD;
+    const int64_t krow0 = a.ks_off[b] + static_cast<int64_t>(kvh) * rp;
     const float sc = static_cast<float>(a.sm_scale);
-    for (int m = w; m < n_rep; m += warps) {
-      const int j = key_block(key[rep_pos[m]]);
-      double sum = 0.0;
-      for (int r = r0; r < r1; ++r) {
-        const int64_t rec = rbase + r;
-        const double Mr = a.M[rec];
-        if (Mr == -INFINITY) continue;
-        const uint16_t* qr = query_ptr(a, ri, h, r);
-        const float e_r = a.err[rec];
-        float mx = -INFINITY;
-        for (int c = 0; c < a.kb; ++c) {
-          const int kc = j * a.kb + c;
-          const uint16_t* kp = (kc <= r) ? key_ptr(a, ri, b, kvh, kc) : nullptr;
-          if (kp != nullptr) mx = fmaxf(mx, warp_dot_f32<HD>(qr, kp) * sc);
+    for (int base = 0; base < n_rep; base += kRepChunk) {
+      const int nm = min(kRepChunk, n_rep - base);
+      for (int item = w; item < nm * nrows; item += warps) {
+        const int m = base + item / nrows, r = r0 + item % nrows;
+        const int j = key_block(key[rep_pos[m]]);
+        const double Mr = a.M[rbase + r];
+        double term = 0.0;
+        if (Mr != -INFINITY) {
+          const int kc = j * KB + kgrp;
+          const bool vis = kc <= r && ((a.kvalid[(krow0 + kc) >> 5] >> ((krow0 + kc) & 31)) & 1u);
+          const uint16_t* qr = qbase + static_cast<int64_t>(r) * HD + sub * SL;
+          // keys past the row (or past the request) are not read: their lanes use the query row
+          const uint16_t* kr = vis ? a.ks + (krow0 + kc) * HD + sub * SL : qr;
+          // two interleaved partial sums: rounding depth SL/2 + 1 + log2(LPK) stays within e_r
+          float p0 = 0.0f, p1 = 0.0f;
+#pragma unroll 1
+          for (int e = 0; e < SL; e += 8) {
+            float qv[8], kv[8];
+            load8_bf16(qr + e, qv);
+            load8_bf16(kr + e, kv);
+#pragma unroll
+            for (int i = 0; i < 8; i += 2) {
+              p0 = fmaf(qv[i], kv[i], p0);
+              p1 = fmaf(qv[i + 1], kv[i + 1], p1);
+            }
+          }
+          float part = p0 + p1;
+#pragma unroll
+          for (int o = LPK / 2; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+          const float x = vis ? part * sc : -INFINITY;
+          float mx = x;
+#pragma unroll
+          for (int o = LPK; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+          if (mx != -INFINITY) {
+            const bool cand = vis && x >= mx - 2.0f * a.err[rbase + r];
+            double dp = 0.0;
+            if (cand) {
+#pragma unroll 1
+              for (int e = 0; e < SL; e += 8) {
+                float qv[8], kv[8];
+                load8_bf16(qr + e, qv);
+                load8_bf16(kr + e, kv);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) dp = fma(static_cast<double>(qv[i]), static_cast<double>(kv[i]), dp);
+              }
+            }
+#pragma unroll
+            for (int o = LPK / 2; o > 0; o >>= 1) dp += __shfl_xor_sync(0xffffffffu, dp, o);
+            double dv = cand ? dp * a.sm_scale : -INFINITY;
+#pragma unroll
+            for (int o = LPK; o < 32; o <<= 1) dv = fmax(dv, __shfl_xor_sync(0xffffffffu, dv, o));
+            term = exp(dv - Mr);
+          }
         }
-        if (mx == -INFINITY) continue;
-        double bm = -INFINITY;
-        for (int c = 0; c < a.kb; ++c) {
-          const int kc = j * a.kb + c;
-          const uint16_t* kp = (kc <= r) ? key_ptr(a, ri, b, kvh, kc) : nullptr;
-          if (kp == nullptr) continue;
-          if (warp_dot_f32<HD>(qr, kp) * sc < mx - 2.0f * e_r) continue;
-          bm = fmax(bm, warp_dot_f64<HD>(qr, kp) * a.sm_scale);
-        }
-        sum += exp(bm - Mr);
+        if (lane == 0) terms[item] = term;
       }
-      if (lane == 0) rep_val[m] = sum;
+      __syncthreads();
+      for (int m = tid; m < nm; m += blockDim.x) {
+        double sum = 0.0;
+        for (int rr = 0; rr < nrows; ++rr) sum += terms[m * nrows + rr];
+        rep_val[base + m] = sum;
+      }
+      __syncthreads();
     }
-    __syncthreads();
     // re-sort the repaired runs by (exact score desc, block asc); a run never crosses the
     // HRM / rest boundary
     if (tid == 0) {
@@ -723,7 +895,7 @@ T* carve(uint8_t*& p, size_t n) {
 }
 
 struct WsLayout {
-  size_t rows, scores, words;
+  size_t rows, scores, words, padded;  // padded: sampled rows of one head summed over requests, 128-padded
 };
 
 WsLayout ws_layout(int num_reqs, int num_q_heads, int block_size, int stride, int total_tokens, int max_seqlen) {
@@ -732,38 +904,49 @@ WsLayout ws_layout(int num_reqs, int num_q_heads, int block_size, int stride, in
   w.rows = static_cast<size_t>(num_q_heads) * (static_cast<size_t>(total_tokens) / stride + num_reqs);
   w.scores = static_cast<size_t>(num_q_heads) * nqb_max * (static_cast<size_t>(total_tokens) / block_size + num_reqs);
   w.words = (nqb_max + 31) / 32;
+  w.padded = static_cast<size_t>(total_tokens) / stride + static_cast<size_t>(num_reqs) * (kRowTile + 1);
   return w;
 }
 
 template <int HD, int KB>
-cudaError_t launch_kap_t(KapArgs a, cudaStream_t stream) {
-  const int threads = 128;
+cudaError_t launch_kap_t(KapArgs a, size_t qs_rows, size_t ks_rows, cudaStream_t stream) {
   kap_setup_kernel<<<1, 256, 0, stream>>>(a);
   {
-    dim3 g((a.max_seqlen / a.stride + 1 + 255) / 256, a.num_reqs * a.num_kv_heads);
-    kap_knorm_kernel<HD><<<g, 256, 0, stream>>>(a);
+    const int rpmax = (a.max_seqlen / a.stride + 1 + kRowTile - 1) / kRowTile * kRowTile;
+    dim3 g((rpmax + 255) / 256, a.num_reqs * (a.num_q_heads + a.num_kv_heads));
+    kap_gather_kernel<HD><<<g, 256, 0, stream>>>(a);
+  }
+  CUtensorMap qs_map, ks_map;
+  {
+    const cuuint64_t dims_q[2] = {static_cast<cuuint64_t>(HD), static_cast<cuuint64_t>(qs_rows)};
+    const cuuint64_t dims_k[2] = {static_cast<cuuint64_t>(HD), static_cast<cuuint64_t>(ks_rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(HD) * 2};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kRowTile)};
+    if (!encode_tiled_bf16(&qs_map, a.qs, 2, dims_q, strides, box)) return cudaErrorInvalidValue;
+    if (!encode_tiled_bf16(&ks_map, a.ks, 2, dims_k, strides, box)) return cudaErrorInvalidValue;
   }
   const size_t tsm = sizeof(KapTileSmem<HD>) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(kap_logits_kernel<HD, KB, kModeRowMax>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(tsm));
+  cudaError_t e = cudaFuncSetAttribute(kap_logits_kernel<HD, KB, kModeRowMax>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(tsm));
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(kap_logits_kernel<HD, KB, kModeScores>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(tsm));
   if (e != cudaSuccess) return e;
   const unsigned tiles = static_cast<unsigned>(a.num_reqs) * a.num_q_heads * a.nrow_tiles_max;
-  kap_logits_kernel<HD, KB, kModeRowMax><<<tiles, threads, tsm, stream>>>(a);
+  kap_logits_kernel<HD, KB, kModeRowMax><<<tiles, kLogitsThreads, tsm, stream>>>(qs_map, ks_map, a);
   {
     const size_t rows = static_cast<size_t>(a.num_q_heads) * (static_cast<size_t>(a.total_tokens) / a.stride + a.num_reqs);
     const unsigned blocks = static_cast<unsigned>((rows + 7) / 8);
     kap_exact_kernel<HD><<<blocks, 256, 0, stream>>>(a);
+    kap_rescan_kernel<HD><<<1024, 256, 0, stream>>>(a);
   }
-  kap_logits_kernel<HD, KB, kModeScores><<<tiles, threads, tsm, stream>>>(a);
+  kap_logits_kernel<HD, KB, kModeScores><<<tiles, kLogitsThreads, tsm, stream>>>(qs_map, ks_map, a);
   int cap = 32;
   while (cap < a.nqb_max) cap <<= 1;
   const size_t ssm = select_smem_bytes(cap);
-  e = cudaFuncSetAttribute(kap_select_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ssm));
+  e = cudaFuncSetAttribute(kap_select_kernel<HD, KB>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ssm));
   if (e != cudaSuccess) return e;
-  kap_select_kernel<HD><<<static_cast<unsigned>(a.num_reqs) * a.num_q_heads * a.nqb_max, kSelectThreads, ssm, stream>>>(a, cap);
+  kap_select_kernel<HD, KB><<<static_cast<unsigned>(a.num_reqs) * a.num_q_heads * a.nqb_max, kSelectThreads, ssm, stream>>>(a, cap);
   return cudaGetLastError();
 }
 
@@ -778,8 +961,9 @@ size_t kap_workspace_bytes(int num_reqs, int num_q_heads, int num_kv_heads, int 
   add(sizeof(int64_t) * (num_reqs + 1));
   add(sizeof(float) * num_reqs * num_kv_heads);
   add(sizeof(float) * static_cast<size_t>(num_reqs) * num_kv_heads * ((max_seqlen + block_size - 1) / block_size));
-  add(sizeof(float) * w.rows * kTop);
-  add(sizeof(int32_t) * w.rows * kTop);
+  add(sizeof(float) * w.rows);
+  add(sizeof(float) * w.rows);
+  add(sizeof(int64_t) * (w.rows + 1));
   add(sizeof(float) * w.rows);
   add(sizeof(int32_t) * w.rows);
   add(sizeof(double) * w.rows);
@@ -788,6 +972,11 @@ size_t kap_workspace_bytes(int num_reqs, int num_q_heads, int num_kv_heads, int 
   add(sizeof(uint32_t) * w.rows * w.words);
   add(sizeof(float) * w.scores);
   add(sizeof(float) * w.scores);
+  add(sizeof(int64_t) * (num_reqs + 1));
+  add(sizeof(int64_t) * (num_reqs + 1));
+  add(sizeof(uint16_t) * static_cast<size_t>(num_q_heads) * w.padded * 128);
+  add(sizeof(uint16_t) * static_cast<size_t>(num_kv_heads) * w.padded * 128);
+  add(sizeof(uint32_t) * (static_cast<size_t>(num_kv_heads) * w.padded / 32 + 1));
   return n + 256;
 }
 
@@ -845,8 +1034,9 @@ cudaError_t launch_kap(const KapLaunch& L, cudaStream_t stream) {
   a.sc_off = carve<int64_t>(p, L.num_reqs + 1);
   a.knorm = carve<float>(p, static_cast<size_t>(L.num_reqs) * L.num_kv_heads);
   a.kbnorm = carve<float>(p, static_cast<size_t>(L.num_reqs) * L.num_kv_heads * a.nqb_max);
-  a.topv = carve<float>(p, w.rows * kTop);
-  a.topc = carve<int32_t>(p, w.rows * kTop);
+  a.v1 = carve<float>(p, w.rows);
+  a.v2 = carve<float>(p, w.rows);
+  a.amb = carve<int64_t>(p, w.rows + 1);
   a.qnorm = carve<float>(p, w.rows);
   a.c1 = carve<int32_t>(p, w.rows);
   a.M = carve<double>(p, w.rows);
@@ -855,16 +1045,23 @@ cudaError_t launch_kap(const KapLaunch& L, cudaStream_t stream) {
   a.hrm_bits = carve<uint32_t>(p, w.rows * w.words);
   a.score = carve<float>(p, w.scores);
   a.score_err = carve<float>(p, w.scores);
+  a.qs_off = carve<int64_t>(p, L.num_reqs + 1);
+  a.ks_off = carve<int64_t>(p, L.num_reqs + 1);
+  a.qs = carve<uint16_t>(p, static_cast<size_t>(L.num_q_heads) * w.padded * 128);
+  a.ks = carve<uint16_t>(p, static_cast<size_t>(L.num_kv_heads) * w.padded * 128);
+  a.kvalid = carve<uint32_t>(p, static_cast<size_t>(L.num_kv_heads) * w.padded / 32 + 1);
   if (static_cast<size_t>(p - static_cast<uint8_t*>(L.workspace)) > L.workspace_bytes) return cudaErrorInvalidValue;
   const int kb = a.kb;
+  const size_t qs_rows = static_cast<size_t>(L.num_q_heads) * w.padded;
+  const size_t ks_rows = static_cast<size_t>(L.num_kv_heads) * w.padded;
   if (L.head_dim == 128) {
-    if (kb == 8) return launch_kap_t<128, 8>(a, stream);
-    if (kb == 4) return launch_kap_t<128, 4>(a, stream);
-    if (kb == 16) return launch_kap_t<128, 16>(a, stream);
+    if (kb == 8) return launch_kap_t<128, 8>(a, qs_rows, ks_rows, stream);
+    if (kb == 4) return launch_kap_t<128, 4>(a, qs_rows, ks_rows, stream);
+    if (kb == 16) return launch_kap_t<128, 16>(a, qs_rows, ks_rows, stream);
   } else if (L.head_dim == 64) {
-    if (kb == 8) return launch_kap_t<64, 8>(a, stream);
-    if (kb == 4) return launch_kap_t<64, 4>(a, stream);
-    if (kb == 16) return launch_kap_t<64, 16>(a, stream);
+    if (kb == 8) return launch_kap_t<64, 8>(a, qs_rows, ks_rows, stream);
+    if (kb == 4) return launch_kap_t<64, 4>(a, qs_rows, ks_rows, stream);
+    if (kb == 16) return launch_kap_t<64, 16>(a, qs_rows, ks_rows, stream);
   }
   return cudaErrorInvalidValue;
 }
