@@ -5,7 +5,7 @@
 // (block_size 64 is padded to 128 rows), its ordered list of key blocks (the
 // computation-order mask M_KAP), and the online-softmax state of its rows.
 //
-// Warp roles (352 threads):
+// Warp roles (384 threads):
 //   warps 0-7  softmax, two warpgroups.  Thread (g, t) with g = warp / 4 and t the TMEM lane
 //              (row) owns columns [g*b/2, (g+1)*b/2) of row t.  Per visit: read the row's half of
 //              S = Q K^T from TMEM, apply the causal / length / missing-page masks, exchange the
@@ -16,9 +16,12 @@
 //              occurrence), resolves each kept block to physical pages through the page table
 //              and TMA-gathers the K pages in mask order ("physical page jumping" and "any-order
 //              page visiting" of Sec. 4.3).
-//   warp 9     MMA: owns TMEM; issues tcgen05.mma for S = Q K^T (double-buffered S, two
-//              visits ahead of the softmax) and O += P V (P from TMEM, V from shared memory).
+//   warp 9     S issuer: owns TMEM; issues tcgen05.mma for S = Q K^T (double-buffered S, two
+//              visits ahead of the softmax).
 //   warp 10    V producer: TMA-gathers V pages only for blocks the vote computed.
+//   warp 11    O issuer: issues O += P V (P from TMEM, V from shared memory) per computed
+//              block.  Kept apart from the S issuer so that waiting for a V tile, which is
+//              only requested once the vote is in, never holds back Q K^T of later blocks.
 //
 // The running max m used by the skip rule is exact for the fp32 logits.  The reference
 // max m_ref used for the exponentials lags it by up to 2^8 (rescaling O in TMEM only
@@ -33,9 +36,9 @@
 namespace cosa {
 namespace {
 
-constexpr int kThreads = 352;
+constexpr int kThreads = 384;
 constexpr int kSoftmaxThreads = 256;
-constexpr int kWarpK = 8, kWarpMma = 9, kWarpV = 10;
+constexpr int kWarpK = 8, kWarpMma = 9, kWarpV = 10, kWarpPv = 11;
 constexpr int kMaxBlocksPerReq = 32768;  // dedupe bitmap capacity (blocks of one request)
 constexpr int kMaxPagesPerBlock = 8;
 constexpr float kRescaleLog2 = 8.0f;     // lazy-rescale threshold, log2 units
@@ -62,7 +65,7 @@ struct alignas(1024) OskSmem {
   uint64_t k_full[NK], k_free[NK];
   uint64_t v_full[NV], v_free[NV];
   uint64_t s_full[2], s_free[2];
-  uint64_t p_full[4];
+  uint64_t p_full[4];                         // per computed visit c: P written (slot c & 3)
   uint64_t o_done[2];
   uint64_t vreq_full[4];
   uint64_t cleanup;
@@ -72,8 +75,7 @@ struct alignas(1024) OskSmem {
   KInfo stash[2];                             // visit info kept by the softmax leader past s_free
   float pmax[2][128];                         // partial row maxima of the two column halves
   float lsum[2][128];                         // partial row sums, exchanged at the end
-  int32_t dec[4];
-  int32_t vote[2][8];
+  int32_t pv_cmd[4];                          // per computed visit c: 1 = issue P.V, 0 = end
   uint32_t tmem_base;
   int32_t abort_flag;
   uint32_t seen[kMaxBlocksPerReq / 32];
@@ -165,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 4; ++s) mbar_init(&sm.p_full[s], 8);
     for (int s = 0; s < 4; ++s) mbar_init(&sm.vreq_full[s], 1);
-    mbar_init(&sm.cleanup, 1);
+    mbar_init(&sm.cleanup, 2);       // one commit from each issuing warp
     sm.abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -279,26 +281,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == kWarpMma) {
-    // =========================== MMA issuer (lane 0) ===========================
-    // Event order per visit v: S(v+2) may start once the softmax has read S(v) (the buffer it
-    // reuses) and K(v+2) has landed; P.V for v follows the vote on v.  Waiting in that order
-    // with suspending waits keeps this warp off the issue slots the softmax warps need.
+    // =========================== S issuer (lane 0) ===========================
+    // S(v) = Q K_v^T once K(v) has landed and the softmax has read S(v - 2), the buffer it reuses.
     if (lane_id() == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, BLK, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, HD, false, true);
       bool ok = wait_parity_bounded(&sm.q_full, 0, abort_flag, a.status);
       tc_fence_after();
-      // S(vv) = Q K_vv^T; 1 issued, 0 end of the list (softmax told), -1 abort
-      auto issue_qk = [&](int vv) -> int {
+      for (int vv = 0; ok; ++vv) {
         const int slot = vv % NK, sb = vv & 1;
-        if (!wait_parity_bounded(&sm.k_full[slot], (vv / NK) & 1, abort_flag, a.status)) return -1;
-        if (vv >= 2 && !wait_parity_bounded(&sm.s_free[sb], ((vv >> 1) - 1) & 1, abort_flag, a.status)) return -1;
+        if (!wait_parity_bounded(&sm.k_full[slot], (vv / NK) & 1, abort_flag, a.status)) break;
+        if (vv >= 2 && !wait_parity_bounded(&sm.s_free[sb], ((vv >> 1) - 1) & 1, abort_flag, a.status)) break;
         const KInfo ki = sm.kinfo[slot];
         sm.sinfo[sb] = ki;
         mbar_arrive(&sm.s_full[sb]);
         if (ki.blk < 0) {
           mbar_arrive(&sm.s_full[sb]);
-          return 0;
+          break;
         }
         tc_fence_after();
 #pragma unroll
@@ -309,41 +307,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         umma_commit(&sm.s_full[sb]);
         umma_commit(&sm.k_free[slot]);
-        return 1;
-      };
-      int issued = 0;       // visits whose Q K^T has been issued
-      bool ended = false;   // end of the list reached (no more Q K^T)
-      while (ok && !ended && issued < 2) {
-        const int r = issue_qk(issued);
-        if (r < 0) ok = false;
-        else if (r == 0) ended = true;
-        else ++issued;
-      }
-      int c = 0;  // computed visits so far (P.V issued)
-      for (int v = 0; ok && v < issued; ++v) {
-        if (!ended) {
-          const int r = issue_qk(v + 2);
-          if (r < 0) { ok = false; break; }
-          if (r == 0) ended = true;
-          else ++issued;
-        }
-        if (!wait_parity_bounded(&sm.p_full[v & 3], (v >> 2) & 1, abort_flag, a.status)) { ok = false; break; }
-        if (sm.dec[v & 3]) {
-          const int slot = c % NV;
-          if (!wait_parity_bounded(&sm.v_full[slot], (c / NV) & 1, abort_flag, a.status)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t pcol = (c & 1) ? kTmemP1 : kTmemP0;
-#pragma unroll
-          for (int kk = 0; kk < BLK / 16; ++kk) {
-            const uint64_t bd = smem_desc_sw128(smem_u32(&sm.v[slot][kk * 16 * 128]), S::HALF, 1024);
-            umma_ts(tmem + kTmemO, tmem + pcol + kk * 8, bd, idesc_pv, (c > 0 || kk > 0) ? 1u : 0u);
-          }
-          umma_commit(&sm.v_free[slot]);
-          umma_commit(&sm.o_done[c & 1]);
-          ++c;
-        }
       }
       // every issued UMMA finishes before TMEM is released
+      umma_commit(&sm.cleanup);
+      wait_parity_bounded(&sm.cleanup, 0, nullptr, nullptr);
+    }
+    __syncwarp();
+  } else if (warp == kWarpPv) {
+    // =========================== O issuer (lane 0) ===========================
+    // O += P_c V_c for the c-th computed visit, once P_c is in TMEM and V_c has landed.
+    if (lane_id() == 0) {
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, HD, false, true);
+      for (int c = 0;; ++c) {
+        if (!wait_parity_bounded(&sm.p_full[c & 3], (c >> 2) & 1, abort_flag, a.status)) break;
+        if (!sm.pv_cmd[c & 3]) break;
+        const int slot = c % NV;
+        if (!wait_parity_bounded(&sm.v_full[slot], (c / NV) & 1, abort_flag, a.status)) break;
+        tc_fence_after();
+        const uint32_t pcol = (c & 1) ? kTmemP1 : kTmemP0;
+#pragma unroll
+        for (int kk = 0; kk < BLK / 16; ++kk) {
+          const uint64_t bd = smem_desc_sw128(smem_u32(&sm.v[slot][kk * 16 * 128]), S::HALF, 1024);
+          umma_ts(tmem + kTmemO, tmem + pcol + kk * 8, bd, idesc_pv, (c > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(&sm.v_free[slot]);
+        umma_commit(&sm.o_done[c & 1]);
+      }
       umma_commit(&sm.cleanup);
       wait_parity_bounded(&sm.cleanup, 0, nullptr, nullptr);
     }
@@ -402,7 +391,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int pos = i * BLK + t;          // token position of this row inside the request
     const bool row_valid = (t < BLK) && (pos < L);
     const bool use_skip = a.skip_delta > 0.0;
-    const float tau2 = use_skip ? static_cast<float>(log2(a.skip_delta / static_cast<double>(L))) : 0.0f;
+    // ln(Delta / L) in log2 units, in fp32 (the logits it is compared with are fp32)
+    const float tau2 = use_skip ? log2f(static_cast<float>(a.skip_delta)) - log2f(static_cast<float>(L)) : 0.0f;
     const float sl2 = a.scale_log2;
     const int pshift = __ffs(P) - 1;
     const bool leader = threadIdx.x == 0;
@@ -415,22 +405,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int v = 0;; ++v) {
       const int sb = v & 1;
       const uint32_t sbase = tmem + lane_addr + (sb ? kTmemS1 : kTmemS0) + col0;
-      // vote code of this warp: bit 0 some row wants the block computed, bit 1 abort, bit 2 end
-      int code = 0;
       int ki_blk = -1, ki_k = 0;
       uint32_t ki_pages = 0;
       float sv[SC];
+      float pm = -INFINITY;   // this half's row max of the block (raw logits)
       bool okw = !local_fail && wait_parity_bounded(&sm.s_full[sb], (v >> 1) & 1, abort_flag, a.status);
       okw = __all_sync(0xffffffffu, okw);
-      if (!okw) {
-        code = 2;
-      } else {
+      if (okw) {
         ki_blk = sm.sinfo[sb].blk;
         ki_pages = sm.sinfo[sb].pages;
         ki_k = sm.sinfo[sb].k;
-        if (ki_blk < 0) {
-          code = 4;
-        } else {
+        if (ki_blk >= 0) {
           if (leader) sm.stash[sb] = sm.sinfo[sb];   // sinfo is reused once S is released
           tc_fence_after();
 #pragma unroll
@@ -458,38 +443,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int q = 0; q < 8; ++q) m8[q] = sv[q];
 #pragma unroll
           for (int e = 8; e < SC; ++e) m8[e & 7] = fmaxf(m8[e & 7], sv[e]);
-          sm.pmax[g][t] = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+          pm = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
         }
       }
-      named_bar_sync(1, kSoftmaxThreads);   // partial maxima of both halves are in
+      // end of the list or a wait that ran out: every softmax warp learns it at the same barrier
+      if (named_bar_red_or(1, kSoftmaxThreads, !okw || ki_blk < 0)) {
+        if (named_bar_red_or(2, kSoftmaxThreads, !okw)) ok = false;
+        break;
+      }
+      // skip vote (Eq. (5)).  A row wants the block iff m_loc - max(m_run, m_loc) >= tau2; that
+      // test is monotone in m_loc, so it holds for the row iff it holds for one of the two
+      // column halves' partial maxima, and the block is computed iff some half of some row wants it.
+      const float p_loc = (pm == -INFINITY) ? -INFINITY : pm * sl2;
+      bool want = true;
+      if (use_skip) want = row_valid && (p_loc != -INFINITY) && (p_loc - fmaxf(m_run, p_loc) >= tau2);
+      const bool compute = named_bar_red_or(2, kSoftmaxThreads, want);
+      // a skipped block leaves every row's running max unchanged (m_loc < m_run + tau2 <= m_run)
       float m_new = m_run;
-      if (code == 0) {
+      if (compute) {
+        sm.pmax[g][t] = pm;
+        named_bar_sync(3, kSoftmaxThreads);
         const float mx = fmaxf(sm.pmax[0][t], sm.pmax[1][t]);
         const float m_loc = (mx == -INFINITY) ? -INFINITY : mx * sl2;
         m_new = fmaxf(m_run, m_loc);
-        bool want = true;
-        if (use_skip) want = row_valid && (m_loc != -INFINITY) && (m_loc - m_new >= tau2);
-        code = (__ballot_sync(0xffffffffu, want) != 0u) ? 1 : 0;
       }
-      if (lane == 0) sm.vote[sb][warp] = code;
-      named_bar_sync(2, kSoftmaxThreads);   // every warp's vote is in
-      int all = 0;
-#pragma unroll
-      for (int w = 0; w < 8; ++w) all |= sm.vote[sb][w];
-      if (all & 2) { ok = false; break; }
-      if (all & 4) break;
-      const bool compute = (all & 1) != 0;
       m_run = m_new;
       if (leader && flags_row) flags_row[ki_k] = compute ? kVisitComputed : kVisitSkipped;
-      if (!compute) {
-        if (leader) sm.dec[v & 3] = 0;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.p_full[v & 3]);
-        continue;
-      }
+      if (!compute) continue;
       if (leader) {
-        sm.dec[v & 3] = 1;
+        sm.pv_cmd[c & 3] = 1;
         sm.vreq[c & 3] = sm.stash[sb];
         mbar_arrive(&sm.vreq_full[c & 3]);
       }
@@ -543,13 +525,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.p_full[v & 3]);
+      if (lane == 0) mbar_arrive(&sm.p_full[c & 3]);
       ++c;
     }
+    // end markers for the V producer and the O issuer
     if (leader) {
       sm.vreq[c & 3].blk = -1;
       mbar_arrive(&sm.vreq_full[c & 3]);
+      sm.pv_cmd[c & 3] = 0;
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.p_full[c & 3]);
     // ---------------- epilogue: O / l -> bf16 -> global ----------------
     if (ok && c > 0) ok = wait_parity_bounded(&sm.o_done[(c - 1) & 1], ((c - 1) >> 1) & 1, abort_flag, a.status);
     tc_fence_after();
