@@ -70,9 +70,8 @@ struct alignas(1024) OskSmem {
   uint64_t vreq_full[4];
   uint64_t cleanup;
   KInfo kinfo[NK];
-  KInfo sinfo[2];
+  KInfo sinfo[4];                             // visit info of visit v (slot v & 3), written with S(v)
   KInfo vreq[4];
-  KInfo stash[2];                             // visit info kept by the softmax leader past s_free
   float pmax[2][128];                         // partial row maxima of the two column halves
   float lsum[2][128];                         // partial row sums, exchanged at the end
   int32_t pv_cmd[4];                          // per computed visit c: 1 = issue P.V, 0 = end
@@ -292,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_parity_bounded(&sm.k_full[slot], (vv / NK) & 1, abort_flag, a.status)) break;
         if (vv >= 2 && !wait_parity_bounded(&sm.s_free[sb], ((vv >> 1) - 1) & 1, abort_flag, a.status)) break;
         const KInfo ki = sm.kinfo[slot];
-        sm.sinfo[sb] = ki;
+        sm.sinfo[vv & 3] = ki;
         mbar_arrive(&sm.s_full[sb]);
         if (ki.blk < 0) {
           mbar_arrive(&sm.s_full[sb]);
@@ -412,11 +411,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool okw = !local_fail && wait_parity_bounded(&sm.s_full[sb], (v >> 1) & 1, abort_flag, a.status);
       okw = __all_sync(0xffffffffu, okw);
       if (okw) {
-        ki_blk = sm.sinfo[sb].blk;
-        ki_pages = sm.sinfo[sb].pages;
-        ki_k = sm.sinfo[sb].k;
+        // slot v & 3 is rewritten with S(v + 4), which waits for S(v + 2) to be released
+        ki_blk = sm.sinfo[v & 3].blk;
+        ki_pages = sm.sinfo[v & 3].pages;
+        ki_k = sm.sinfo[v & 3].k;
         if (ki_blk >= 0) {
-          if (leader) sm.stash[sb] = sm.sinfo[sb];   // sinfo is reused once S is released
           tc_fence_after();
 #pragma unroll
           for (int cc = 0; cc < SC / 32; ++cc) {
@@ -438,12 +437,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < SC; ++e)
               if (col0 + e > lim || !((ki_pages >> ((col0 + e) >> pshift)) & 1u)) sv[e] = -INFINITY;
           }
+          static_assert(SC % 16 == 0, "16-column groups");
           float m8[8];
 #pragma unroll
-          for (int q = 0; q < 8; ++q) m8[q] = sv[q];
+          for (int q = 0; q < 8; ++q) m8[q] = fmaxf(sv[2 * q], sv[2 * q + 1]);
 #pragma unroll
-          for (int e = 8; e < SC; ++e) m8[e & 7] = fmaxf(m8[e & 7], sv[e]);
-          pm = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+          for (int e = 16; e < SC; e += 16) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) m8[q] = fmax3f(m8[q], sv[e + 2 * q], sv[e + 2 * q + 1]);
+          }
+          pm = fmax3f(fmax3f(m8[0], m8[1], m8[2]), fmax3f(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
         }
       }
       // end of the list or a wait that ran out: every softmax warp learns it at the same barrier
@@ -472,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!compute) continue;
       if (leader) {
         sm.pv_cmd[c & 3] = 1;
-        sm.vreq[c & 3] = sm.stash[sb];
+        sm.vreq[c & 3] = sm.sinfo[v & 3];
         mbar_arrive(&sm.vreq_full[c & 3]);
       }
       // lazy rescale of O and l when the max rises by more than 2^8
@@ -491,9 +494,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       float rs4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
       for (int e = 0; e < SC / 2; ++e) {
-        const float p0 = ex2_approx(fmaf(sv[2 * e], sl2, -base));
-        const float p1 = ex2_approx(fmaf(sv[2 * e + 1], sl2, -base));
-        rs4[e & 3] += p0 + p1;
+        float x0, x1;
+        fma2_bc(x0, x1, sv[2 * e], sv[2 * e + 1], sl2, -base);
+        const float p0 = ex2_approx(x0);
+        const float p1 = ex2_approx(x1);
+        add2_acc(rs4[(e & 1) * 2], rs4[(e & 1) * 2 + 1], p0, p1);
         pk[e] = pack_bf16x2(p0, p1);
       }
       l_part += (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
