@@ -49,6 +49,7 @@ struct KInfo {
   int32_t blk;     // block id, -1 = end of the list
   uint32_t pages;  // bit u set: page u of the block exists
   int32_t k;       // index of the entry in the mask row
+  int32_t kvh;     // kv head of the work item
   int32_t phys[kMaxPagesPerBlock];
 };
 
@@ -61,7 +62,7 @@ struct alignas(1024) OskSmem {
   uint8_t q[128 * HD * 2];                    // [HD/64][128 rows][128 B], SW128
   uint8_t k[NK][TILE];                        // [HD/64][BLK rows][128 B], SW128
   uint8_t v[NV][TILE];
-  uint64_t q_full;
+  uint64_t q_full, q_free;
   uint64_t k_full[NK], k_free[NK];
   uint64_t v_full[NV], v_free[NV];
   uint64_t s_full[2], s_free[2];
@@ -74,7 +75,7 @@ struct alignas(1024) OskSmem {
   KInfo vreq[4];
   float pmax[2][128];                         // partial row maxima of the two column halves
   float lsum[2][128];                         // partial row sums, exchanged at the end
-  int32_t pv_cmd[4];                          // per computed visit c: 1 = issue P.V, 0 = end
+  int32_t pv_cmd[4];                          // per computed visit c: 2 = first of its item, 1 = accumulate, 0 = end
   uint32_t tmem_base;
   int32_t abort_flag;
   uint32_t seen[kMaxBlocksPerReq / 32];
@@ -90,6 +91,7 @@ struct OskArgs {
   int32_t* status;
   int num_reqs, num_q_heads, num_kv_heads, total_tokens, max_seqlen, nqb_max;
   int page_size, num_pages, max_pages_per_req, mask_pitch;
+  int num_items;                      // kv heads * query blocks * requests * query heads per kv head
   float scale_log2;
   double skip_delta;
 };
@@ -111,6 +113,31 @@ __device__ __forceinline__ void tmem_st_n(uint32_t taddr, const uint32_t (&r)[N]
   }
 }
 
+// Work item `idx` of the grid-stride order: kv-head major (a head's K/V stay in L2 while its
+// query heads are processed), heaviest query blocks first.
+struct Item {
+  int b, h, kvh, i, tok0, L, nblk;
+  int state;  // 0 run, 1 absent query block (shorter request), 2 bad cu_seqlens
+};
+
+__device__ __forceinline__ Item decode_item(const OskArgs& a, int idx, int blk) {
+  Item it;
+  const int G = a.num_q_heads / a.num_kv_heads;
+  const int hg = idx % G;
+  idx /= G;
+  it.b = idx % a.num_reqs;
+  idx /= a.num_reqs;
+  it.i = a.nqb_max - 1 - (idx % a.nqb_max);
+  it.kvh = idx / a.nqb_max;
+  it.h = it.kvh * G + hg;
+  it.tok0 = a.cu_seqlens[it.b];
+  it.L = a.cu_seqlens[it.b + 1] - it.tok0;
+  it.nblk = (it.L + blk - 1) / blk;
+  if (it.L < 0 || it.L > a.max_seqlen || it.tok0 < 0 || it.tok0 + it.L > a.total_tokens) it.state = 2;
+  else it.state = (it.i >= it.nblk) ? 1 : 0;
+  return it;
+}
+
 template <int BLK, int HD>
 __global__ void __launch_bounds__(kThreads, 1)
     osk_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
@@ -120,43 +147,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int DH = HD / 64;       // 64-wide d chunks
   constexpr int SC = BLK / 2;       // S columns per softmax thread
   constexpr int OC = HD / 2;        // O columns per softmax thread
+  static_assert(NV * S::TILE >= 128 * HD * 2, "the V slots stage one output tile");
   extern __shared__ uint8_t smem_raw[];
   S& sm = *reinterpret_cast<S*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-
-  // ---------------- work item: kv-head major, heaviest query blocks first ----------------
-  const int G = a.num_q_heads / a.num_kv_heads;
-  int idx = blockIdx.x;
-  const int hg = idx % G;
-  idx /= G;
-  const int b = idx % a.num_reqs;
-  idx /= a.num_reqs;
-  const int i = a.nqb_max - 1 - (idx % a.nqb_max);
-  const int kvh = idx / a.nqb_max;
-  const int h = kvh * G + hg;
-  const int tok0 = a.cu_seqlens[b];
-  const int L = a.cu_seqlens[b + 1] - tok0;
-  if (L < 0 || L > a.max_seqlen || tok0 < 0 || tok0 + L > a.total_tokens) {
-    if (threadIdx.x == 0) report_status(a.status, kStatusBadInput);
-    return;
-  }
-  const int nblk = (L + BLK - 1) / BLK;
-  if (i >= nblk) return;  // absent query block of a shorter request
 
   const int warp = threadIdx.x >> 5;
   const int P = a.page_size;
   const int pages_per_blk = BLK / P;
   const uint32_t all_pages = (1u << pages_per_blk) - 1u;
-  const int req_pages = (L + P - 1) / P;
-  const size_t row_base = ((static_cast<size_t>(b) * a.num_q_heads + h) * a.nqb_max + i);
-  const int32_t* mask_row = a.mask + row_base * a.mask_pitch;
-  uint8_t* flags_row = a.visit_flags ? a.visit_flags + row_base * a.mask_pitch : nullptr;
-  int n_entries = a.mask_len[row_base];
-  n_entries = n_entries < 0 ? 0 : (n_entries > a.mask_pitch ? a.mask_pitch : n_entries);
   volatile int* abort_flag = &sm.abort_flag;
 
-  // ---------------- set-up ----------------
+  // ---------------- set-up (once per CTA) ----------------
   if (threadIdx.x == 0) {
     mbar_init(&sm.q_full, 1);
+    mbar_init(&sm.q_free, 1);
     for (int s = 0; s < NK; ++s) { mbar_init(&sm.k_full[s], 1); mbar_init(&sm.k_free[s], 1); }
     for (int s = 0; s < NV; ++s) { mbar_init(&sm.v_full[s], 1); mbar_init(&sm.v_free[s], 1); }
     for (int s = 0; s < 2; ++s) {
@@ -175,17 +179,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   // padding rows 64..127 of a 64-row query block must hold finite values (their S rows are
-  // discarded, but the UMMA reads them)
+  // discarded, but the UMMA reads them); Q loads never write them
   if (BLK < 128) {
     for (int e = threadIdx.x; e < DH * 64 * 8; e += kThreads) {
       const int dh = e / (64 * 8), rem = e % (64 * 8);
       reinterpret_cast<uint4*>(&sm.q[dh * 128 * 128 + 64 * 128])[rem] = make_uint4(0, 0, 0, 0);
     }
-  }
-  if (warp == kWarpK) {
-    for (int w = lane_id(); w < (nblk + 31) / 32; w += 32) sm.seen[w] = 0u;
-    if (flags_row)
-      for (int k = n_entries + lane_id(); k < a.mask_pitch; k += 32) flags_row[k] = kVisitIgnored;
   }
   fence_proxy_async_smem();
   tc_fence_before();
@@ -193,6 +192,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
 
+  // Every role walks the same items (blockIdx.x, + gridDim.x, ...) and skips the same absent
+  // or malformed ones.  Ring positions and barrier phases run on across items: v counts visits
+  // (one extra per item for its end marker), c counts computed visits, n counts items.
   if (warp == kWarpK) {
     // =========================== K producer ===========================
     const uint32_t lane = lane_id();
@@ -200,80 +202,105 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&qmap);
       tma_prefetch_desc(&kmap);
       tma_prefetch_desc(&vmap);
-      mbar_arrive_expect_tx(&sm.q_full, BLK * HD * 2);
-      for (int dh = 0; dh < DH; ++dh) tma_load_3d(&sm.q[dh * 128 * 128], &qmap, &sm.q_full, dh * 64, h, tok0 + i * BLK);
     }
-    const int32_t* pt_row = a.page_table + static_cast<size_t>(b) * a.max_pages_per_req;
-    int v = 0;  // visits issued
+    int v = 0, n = 0;
     bool ok = true;
-    for (int k0 = 0; k0 < n_entries && ok; k0 += 32) {
-      const int k = k0 + static_cast<int>(lane);
-      const int j = (k < n_entries) ? mask_row[k] : -1;
-      const bool valid = (k < n_entries) && j >= 0 && j <= i && j < nblk;
-      const unsigned peers = __match_any_sync(0xffffffffu, valid ? j : -1 - static_cast<int>(lane));
-      const bool first = valid && (static_cast<int>(lane) == __ffs(peers) - 1);
-      const bool dup = first && ((sm.seen[j >> 5] >> (j & 31)) & 1u);
-      const bool keep = first && !dup;
+    for (int idx = blockIdx.x; idx < a.num_items && ok; idx += gridDim.x) {
+      const Item it = decode_item(a, idx, BLK);
+      if (it.state == 2 && lane == 0) report_status(a.status, kStatusBadInput);
+      if (it.state != 0) continue;
+      const int i = it.i, nblk = it.nblk, kvh = it.kvh;
+      const int req_pages = (it.L + P - 1) / P;
+      const size_t row_base = ((static_cast<size_t>(it.b) * a.num_q_heads + it.h) * a.nqb_max + i);
+      const int32_t* mask_row = a.mask + row_base * a.mask_pitch;
+      uint8_t* flags_row = a.visit_flags ? a.visit_flags + row_base * a.mask_pitch : nullptr;
+      int n_entries = a.mask_len[row_base];
+      n_entries = n_entries < 0 ? 0 : (n_entries > a.mask_pitch ? a.mask_pitch : n_entries);
+      for (int w = lane; w < (nblk + 31) / 32; w += 32) sm.seen[w] = 0u;
+      if (flags_row)
+        for (int k = n_entries + lane; k < a.mask_pitch; k += 32) flags_row[k] = kVisitIgnored;
       __syncwarp();
-      if (keep) atomicOr(&sm.seen[j >> 5], 1u << (j & 31));
-      if (flags_row && k < n_entries && !keep) flags_row[k] = kVisitIgnored;
-      // physical pages of this lane's block
-      int phys[kMaxPagesPerBlock];
-      uint32_t pages = 0;
+      // Q of this item, once every Q K^T product of the previous item has completed
+      if (n > 0) ok = warp_wait(&sm.q_free, (n - 1) & 1, abort_flag, a.status);
+      if (!ok) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&sm.q_full, BLK * HD * 2);
+        for (int dh = 0; dh < DH; ++dh)
+          tma_load_3d(&sm.q[dh * 128 * 128], &qmap, &sm.q_full, dh * 64, it.h, it.tok0 + i * BLK);
+      }
+      ++n;
+      const int32_t* pt_row = a.page_table + static_cast<size_t>(it.b) * a.max_pages_per_req;
+      for (int k0 = 0; k0 < n_entries && ok; k0 += 32) {
+        const int k = k0 + static_cast<int>(lane);
+        const int j = (k < n_entries) ? mask_row[k] : -1;
+        const bool valid = (k < n_entries) && j >= 0 && j <= i && j < nblk;
+        const unsigned peers = __match_any_sync(0xffffffffu, valid ? j : -1 - static_cast<int>(lane));
+        const bool first = valid && (static_cast<int>(lane) == __ffs(peers) - 1);
+        const bool dup = first && ((sm.seen[j >> 5] >> (j & 31)) & 1u);
+        const bool keep = first && !dup;
+        __syncwarp();
+        if (keep) atomicOr(&sm.seen[j >> 5], 1u << (j & 31));
+        if (flags_row && k < n_entries && !keep) flags_row[k] = kVisitIgnored;
+        // physical pages of this lane's block
+        int phys[kMaxPagesPerBlock];
+        uint32_t pages = 0;
 #pragma unroll
-      for (int u = 0; u < kMaxPagesPerBlock; ++u) {
-        phys[u] = -1;
-        if (keep && u < pages_per_blk) {
-          const int lp = j * pages_per_blk + u;
-          const int pp = (lp < req_pages) ? pt_row[lp] : -1;
-          if (pp >= 0 && pp < a.num_pages) { phys[u] = pp; pages |= 1u << u; }
+        for (int u = 0; u < kMaxPagesPerBlock; ++u) {
+          phys[u] = -1;
+          if (keep && u < pages_per_blk) {
+            const int lp = j * pages_per_blk + u;
+            const int pp = (lp < req_pages) ? pt_row[lp] : -1;
+            if (pp >= 0 && pp < a.num_pages) { phys[u] = pp; pages |= 1u << u; }
+          }
+        }
+        __syncwarp();
+        unsigned todo = __ballot_sync(0xffffffffu, keep);
+        while (todo && ok) {
+          const int src = __ffs(todo) - 1;
+          todo &= todo - 1;
+          const int jj = __shfl_sync(0xffffffffu, j, src);
+          const uint32_t pg = __shfl_sync(0xffffffffu, pages, src);
+          int ph[kMaxPagesPerBlock];
+#pragma unroll
+          for (int u = 0; u < kMaxPagesPerBlock; ++u) ph[u] = __shfl_sync(0xffffffffu, phys[u], src);
+          const int slot = v % NK;
+          if (v >= NK) ok = warp_wait(&sm.k_free[slot], ((v / NK) - 1) & 1, abort_flag, a.status);
+          if (!ok) break;
+          if (lane == 0) {
+            KInfo& ki = sm.kinfo[slot];
+            ki.blk = jj;
+            ki.pages = pg;
+            ki.k = k0 + src;
+            ki.kvh = kvh;
+#pragma unroll
+            for (int u = 0; u < kMaxPagesPerBlock; ++u) ki.phys[u] = ph[u];
+            const uint32_t bytes = static_cast<uint32_t>(__popc(pg)) * DH * P * 128u;
+            mbar_arrive_expect_tx(&sm.k_full[slot], bytes);
+            for (int u = 0; u < pages_per_blk; ++u) {
+              if (!((pg >> u) & 1u)) continue;
+              for (int dh = 0; dh < DH; ++dh)
+                tma_load_4d(&sm.k[slot][dh * S::HALF + u * P * 128], &kmap, &sm.k_full[slot], dh * 64, kvh, 0, ph[u]);
+            }
+          }
+          __syncwarp();
+          ++v;
         }
       }
-      __syncwarp();
-      unsigned todo = __ballot_sync(0xffffffffu, keep);
-      while (todo && ok) {
-        const int src = __ffs(todo) - 1;
-        todo &= todo - 1;
-        const int jj = __shfl_sync(0xffffffffu, j, src);
-        const uint32_t pg = __shfl_sync(0xffffffffu, pages, src);
-        int ph[kMaxPagesPerBlock];
-#pragma unroll
-        for (int u = 0; u < kMaxPagesPerBlock; ++u) ph[u] = __shfl_sync(0xffffffffu, phys[u], src);
+      // end marker of the item
+      if (ok) {
         const int slot = v % NK;
         if (v >= NK) ok = warp_wait(&sm.k_free[slot], ((v / NK) - 1) & 1, abort_flag, a.status);
-        if (!ok) break;
-        if (lane == 0) {
-          KInfo& ki = sm.kinfo[slot];
-          ki.blk = jj;
-          ki.pages = pg;
-          ki.k = k0 + src;
-#pragma unroll
-          for (int u = 0; u < kMaxPagesPerBlock; ++u) ki.phys[u] = ph[u];
-          const uint32_t bytes = static_cast<uint32_t>(__popc(pg)) * DH * P * 128u;
-          mbar_arrive_expect_tx(&sm.k_full[slot], bytes);
-          for (int u = 0; u < pages_per_blk; ++u) {
-            if (!((pg >> u) & 1u)) continue;
-            for (int dh = 0; dh < DH; ++dh)
-              tma_load_4d(&sm.k[slot][dh * S::HALF + u * P * 128], &kmap, &sm.k_full[slot], dh * 64, kvh, 0, ph[u]);
-          }
+        if (ok && lane == 0) {
+          sm.kinfo[slot].blk = -1;
+          mbar_arrive(&sm.k_full[slot]);
         }
         __syncwarp();
         ++v;
       }
     }
-    // end marker
-    if (ok) {
-      const int slot = v % NK;
-      if (v >= NK) ok = warp_wait(&sm.k_free[slot], ((v / NK) - 1) & 1, abort_flag, a.status);
-      if (ok && lane == 0) {
-        sm.kinfo[slot].blk = -1;
-        mbar_arrive(&sm.k_full[slot]);
-      }
-    }
-    __syncwarp();
     // on abort, let every issued copy land before the CTA exits
     if (*abort_flag && lane == 0) {
-      wait_parity_bounded(&sm.q_full, 0, nullptr, nullptr);
+      if (n > 0) wait_parity_bounded(&sm.q_full, (n - 1) & 1, nullptr, nullptr);
       for (int s = 0; s < NK; ++s) {
         const int issued = (v - s + NK - 1) / NK;  // loads issued into slot s
         if (issued > 0) wait_parity_bounded(&sm.k_full[s], (issued - 1) & 1, nullptr, nullptr);
@@ -284,28 +311,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     // S(v) = Q K_v^T once K(v) has landed and the softmax has read S(v - 2), the buffer it reuses.
     if (lane_id() == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, BLK, false, false);
-      bool ok = wait_parity_bounded(&sm.q_full, 0, abort_flag, a.status);
-      tc_fence_after();
-      for (int vv = 0; ok; ++vv) {
-        const int slot = vv % NK, sb = vv & 1;
-        if (!wait_parity_bounded(&sm.k_full[slot], (vv / NK) & 1, abort_flag, a.status)) break;
-        if (vv >= 2 && !wait_parity_bounded(&sm.s_free[sb], ((vv >> 1) - 1) & 1, abort_flag, a.status)) break;
-        const KInfo ki = sm.kinfo[slot];
-        sm.sinfo[vv & 3] = ki;
-        mbar_arrive(&sm.s_full[sb]);
-        if (ki.blk < 0) {
-          mbar_arrive(&sm.s_full[sb]);
-          break;
-        }
+      int vv = 0, n = 0;
+      bool ok = true;
+      for (int idx = blockIdx.x; idx < a.num_items && ok; idx += gridDim.x) {
+        const Item it = decode_item(a, idx, BLK);
+        if (it.state != 0) continue;
+        ok = wait_parity_bounded(&sm.q_full, n & 1, abort_flag, a.status);
+        ++n;
         tc_fence_after();
+        while (ok) {
+          const int slot = vv % NK, sb = vv & 1;
+          if (!wait_parity_bounded(&sm.k_full[slot], (vv / NK) & 1, abort_flag, a.status)) { ok = false; break; }
+          if (vv >= 2 && !wait_parity_bounded(&sm.s_free[sb], ((vv >> 1) - 1) & 1, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          const KInfo ki = sm.kinfo[slot];
+          sm.sinfo[vv & 3] = ki;
+          mbar_arrive(&sm.s_full[sb]);
+          if (ki.blk < 0) {
+            // end of the item: no product; the K slot and the S buffer pass on unused
+            mbar_arrive(&sm.s_full[sb]);
+            mbar_arrive(&sm.k_free[slot]);
+            ++vv;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint64_t ad = smem_desc_sw128(smem_u32(&sm.q[(kk >> 2) * 128 * 128 + (kk & 3) * 32]), 16, 1024);
-          const uint64_t bd = smem_desc_sw128(smem_u32(&sm.k[slot][(kk >> 2) * S::HALF + (kk & 3) * 32]), 16, 1024);
-          umma_ss(tmem + (sb ? kTmemS1 : kTmemS0), ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < HD / 16; ++kk) {
+            const uint64_t ad = smem_desc_sw128(smem_u32(&sm.q[(kk >> 2) * 128 * 128 + (kk & 3) * 32]), 16, 1024);
+            const uint64_t bd = smem_desc_sw128(smem_u32(&sm.k[slot][(kk >> 2) * S::HALF + (kk & 3) * 32]), 16, 1024);
+            umma_ss(tmem + (sb ? kTmemS1 : kTmemS0), ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(&sm.s_full[sb]);
+          umma_commit(&sm.k_free[slot]);
+          ++vv;
         }
-        umma_commit(&sm.s_full[sb]);
-        umma_commit(&sm.k_free[slot]);
+        // Q may be replaced once this item's products have completed
+        if (ok) umma_commit(&sm.q_free);
       }
       // every issued UMMA finishes before TMEM is released
       umma_commit(&sm.cleanup);
@@ -314,12 +357,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == kWarpPv) {
     // =========================== O issuer (lane 0) ===========================
-    // O += P_c V_c for the c-th computed visit, once P_c is in TMEM and V_c has landed.
+    // O += P_c V_c for the c-th computed visit, once P_c is in TMEM and V_c has landed;
+    // the first computed visit of an item overwrites O.
     if (lane_id() == 0) {
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, HD, false, true);
       for (int c = 0;; ++c) {
         if (!wait_parity_bounded(&sm.p_full[c & 3], (c >> 2) & 1, abort_flag, a.status)) break;
-        if (!sm.pv_cmd[c & 3]) break;
+        const int cmd = sm.pv_cmd[c & 3];
+        if (!cmd) break;
         const int slot = c % NV;
         if (!wait_parity_bounded(&sm.v_full[slot], (c / NV) & 1, abort_flag, a.status)) break;
         tc_fence_after();
@@ -327,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < BLK / 16; ++kk) {
           const uint64_t bd = smem_desc_sw128(smem_u32(&sm.v[slot][kk * 16 * 128]), S::HALF, 1024);
-          umma_ts(tmem + kTmemO, tmem + pcol + kk * 8, bd, idesc_pv, (c > 0 || kk > 0) ? 1u : 0u);
+          umma_ts(tmem + kTmemO, tmem + pcol + kk * 8, bd, idesc_pv, (cmd == 1 || kk > 0) ? 1u : 0u);
         }
         umma_commit(&sm.v_free[slot]);
         umma_commit(&sm.o_done[c & 1]);
@@ -368,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int u = 0; u < pages_per_blk; ++u) {
           if (!((r.pages >> u) & 1u)) continue;
           for (int dh = 0; dh < DH; ++dh)
-            tma_load_4d(&sm.v[slot][dh * S::HALF + u * P * 128], &vmap, &sm.v_full[slot], dh * 64, kvh, 0, r.phys[u]);
+            tma_load_4d(&sm.v[slot][dh * S::HALF + u * P * 128], &vmap, &sm.v_full[slot], dh * 64, r.kvh, 0, r.phys[u]);
         }
       }
       __syncwarp();
@@ -387,151 +432,221 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane = lane_id();
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int col0 = g * SC;              // first S column of this thread
-    const int pos = i * BLK + t;          // token position of this row inside the request
-    const bool row_valid = (t < BLK) && (pos < L);
     const bool use_skip = a.skip_delta > 0.0;
-    // ln(Delta / L) in log2 units, in fp32 (the logits it is compared with are fp32)
-    const float tau2 = use_skip ? log2f(static_cast<float>(a.skip_delta)) - log2f(static_cast<float>(L)) : 0.0f;
     const float sl2 = a.scale_log2;
     const int pshift = __ffs(P) - 1;
     const bool leader = threadIdx.x == 0;
-    float m_run = -INFINITY;   // running max (log2 units), Algorithm A line 13
-    float m_ref = -INFINITY;   // max the exponentials are taken against
-    float l_part = 0.0f;       // this half's share of the row sum l
-    int c = 0;                 // computed visits
+    int v = 0;                 // visits, all items
+    int c = 0;                 // computed visits, all items
     bool ok = true;
     bool local_fail = false;   // a wait of this warp ran out after the last vote
-    for (int v = 0;; ++v) {
-      const int sb = v & 1;
-      const uint32_t sbase = tmem + lane_addr + (sb ? kTmemS1 : kTmemS0) + col0;
-      int ki_blk = -1, ki_k = 0;
-      uint32_t ki_pages = 0;
-      float sv[SC];
-      float pm = -INFINITY;   // this half's row max of the block (raw logits)
-      bool okw = !local_fail && wait_parity_bounded(&sm.s_full[sb], (v >> 1) & 1, abort_flag, a.status);
-      okw = __all_sync(0xffffffffu, okw);
-      if (okw) {
-        // slot v & 3 is rewritten with S(v + 4), which waits for S(v + 2) to be released
-        ki_blk = sm.sinfo[v & 3].blk;
-        ki_pages = sm.sinfo[v & 3].pages;
-        ki_k = sm.sinfo[v & 3].k;
-        if (ki_blk >= 0) {
-          tc_fence_after();
+    for (int idx = blockIdx.x; idx < a.num_items && ok; idx += gridDim.x) {
+      const Item it = decode_item(a, idx, BLK);
+      if (it.state != 0) continue;
+      const int i = it.i, L = it.L;
+      const int pos = i * BLK + t;          // token position of this row inside the request
+      const bool row_valid = (t < BLK) && (pos < L);
+      // ln(Delta / L) in log2 units, in fp32 (the logits it is compared with are fp32)
+      const float tau2 = use_skip ? log2f(static_cast<float>(a.skip_delta)) - log2f(static_cast<float>(L)) : 0.0f;
+      const size_t row_base = ((static_cast<size_t>(it.b) * a.num_q_heads + it.h) * a.nqb_max + i);
+      uint8_t* flags_row = a.visit_flags ? a.visit_flags + row_base * a.mask_pitch : nullptr;
+      float m_run = -INFINITY;   // running max (log2 units), Algorithm A line 13
+      float m_ref = -INFINITY;   // max the exponentials are taken against
+      float l_part = 0.0f;       // this half's share of the row sum l
+      int c_item = 0;            // computed visits of this item
+      for (;; ++v) {
+        const int sb = v & 1;
+        const uint32_t sbase = tmem + lane_addr + (sb ? kTmemS1 : kTmemS0) + col0;
+        int ki_blk = -1, ki_k = 0;
+        uint32_t ki_pages = 0;
+        float sv[SC];
+        float pm = -INFINITY;   // this half's row max of the block (raw logits)
+        bool okw = !local_fail && wait_parity_bounded(&sm.s_full[sb], (v >> 1) & 1, abort_flag, a.status);
+        okw = __all_sync(0xffffffffu, okw);
+        if (okw) {
+          // slot v & 3 is rewritten with S(v + 4), which waits for S(v + 2) to be released
+          ki_blk = sm.sinfo[v & 3].blk;
+          ki_pages = sm.sinfo[v & 3].pages;
+          ki_k = sm.sinfo[v & 3].k;
+          if (ki_blk >= 0) {
+            tc_fence_after();
 #pragma unroll
-          for (int cc = 0; cc < SC / 32; ++cc) {
-            uint32_t r[32];
-            tmem_ld32(sbase + cc * 32, r);
+            for (int cc = 0; cc < SC / 32; ++cc) {
+              uint32_t r[32];
+              tmem_ld32(sbase + cc * 32, r);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) sv[cc * 32 + e] = __uint_as_float(r[e]);
+              for (int e = 0; e < 32; ++e) sv[cc * 32 + e] = __uint_as_float(r[e]);
+            }
+            tmem_wait_ld();
+            tc_fence_before();
           }
-          tmem_wait_ld();
-          tc_fence_before();
+          // the buffer is released for every visit, the end marker's included
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm.s_free[sb]);
-          // masks: causal on the diagonal block, length on the last block, missing pages
-          const int key0 = ki_blk * BLK;
-          const bool need_mask = (ki_blk == i) || (key0 + BLK > L) || (ki_pages != all_pages) || !row_valid;
-          if (need_mask) {
-            const int lim = row_valid ? min(pos, L - 1) - key0 : -1;  // last visible column
+          if (ki_blk >= 0) {
+            // masks: causal on the diagonal block, length on the last block, missing pages
+            const int key0 = ki_blk * BLK;
+            const bool need_mask = (ki_blk == i) || (key0 + BLK > L) || (ki_pages != all_pages) || !row_valid;
+            if (need_mask) {
+              const int lim = row_valid ? min(pos, L - 1) - key0 : -1;  // last visible column
 #pragma unroll
-            for (int e = 0; e < SC; ++e)
-              if (col0 + e > lim || !((ki_pages >> ((col0 + e) >> pshift)) & 1u)) sv[e] = -INFINITY;
+              for (int e = 0; e < SC; ++e)
+                if (col0 + e > lim || !((ki_pages >> ((col0 + e) >> pshift)) & 1u)) sv[e] = -INFINITY;
+            }
+            static_assert(SC % 16 == 0, "16-column groups");
+            float m8[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) m8[q] = fmaxf(sv[2 * q], sv[2 * q + 1]);
+#pragma unroll
+            for (int e = 16; e < SC; e += 16) {
+#pragma unroll
+              for (int q = 0; q < 8; ++q) m8[q] = fmax3f(m8[q], sv[e + 2 * q], sv[e + 2 * q + 1]);
+            }
+            pm = fmax3f(fmax3f(m8[0], m8[1], m8[2]), fmax3f(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
           }
-          static_assert(SC % 16 == 0, "16-column groups");
-          float m8[8];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) m8[q] = fmaxf(sv[2 * q], sv[2 * q + 1]);
-#pragma unroll
-          for (int e = 16; e < SC; e += 16) {
-#pragma unroll
-            for (int q = 0; q < 8; ++q) m8[q] = fmax3f(m8[q], sv[e + 2 * q], sv[e + 2 * q + 1]);
-          }
-          pm = fmax3f(fmax3f(m8[0], m8[1], m8[2]), fmax3f(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
         }
-      }
-      // end of the list or a wait that ran out: every softmax warp learns it at the same barrier
-      if (named_bar_red_or(1, kSoftmaxThreads, !okw || ki_blk < 0)) {
-        if (named_bar_red_or(2, kSoftmaxThreads, !okw)) ok = false;
-        break;
-      }
-      // skip vote (Eq. (5)).  A row wants the block iff m_loc - max(m_run, m_loc) >= tau2; that
-      // test is monotone in m_loc, so it holds for the row iff it holds for one of the two
-      // column halves' partial maxima, and the block is computed iff some half of some row wants it.
-      const float p_loc = (pm == -INFINITY) ? -INFINITY : pm * sl2;
-      bool want = true;
-      if (use_skip) want = row_valid && (p_loc != -INFINITY) && (p_loc - fmaxf(m_run, p_loc) >= tau2);
-      const bool compute = named_bar_red_or(2, kSoftmaxThreads, want);
-      // a skipped block leaves every row's running max unchanged (m_loc < m_run + tau2 <= m_run)
-      float m_new = m_run;
-      if (compute) {
-        sm.pmax[g][t] = pm;
-        named_bar_sync(3, kSoftmaxThreads);
-        const float mx = fmaxf(sm.pmax[0][t], sm.pmax[1][t]);
-        const float m_loc = (mx == -INFINITY) ? -INFINITY : mx * sl2;
-        m_new = fmaxf(m_run, m_loc);
-      }
-      m_run = m_new;
-      if (leader && flags_row) flags_row[ki_k] = compute ? kVisitComputed : kVisitSkipped;
-      if (!compute) continue;
-      if (leader) {
-        sm.pv_cmd[c & 3] = 1;
-        sm.vreq[c & 3] = sm.sinfo[v & 3];
-        mbar_arrive(&sm.vreq_full[c & 3]);
-      }
-      // lazy rescale of O and l when the max rises by more than 2^8
-      const bool first_mass = (m_ref == -INFINITY) && (m_new != -INFINITY);
-      const bool rescale = (m_ref != -INFINITY) && (m_new > m_ref + kRescaleLog2);
-      float alpha = 1.0f;
-      if (first_mass) m_ref = m_new;
-      if (rescale) {
-        alpha = ex2_approx(m_ref - m_new);
-        m_ref = m_new;
-        l_part *= alpha;
-      }
-      // P = exp2(S * scale * log2(e) - m_ref) as bf16 pairs; masked entries are -inf -> 0
-      const float base = (m_ref == -INFINITY) ? 0.0f : m_ref;
-      uint32_t pk[SC / 2];
-      float rs4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        // end of the item or a wait that ran out: every softmax warp learns it at the same barrier
+        if (named_bar_red_or(1, kSoftmaxThreads, !okw || ki_blk < 0)) {
+          if (named_bar_red_or(2, kSoftmaxThreads, !okw)) ok = false;
+          ++v;
+          break;
+        }
+        // skip vote (Eq. (5)).  A row wants the block iff m_loc - max(m_run, m_loc) >= tau2; that
+        // test is monotone in m_loc, so it holds for the row iff it holds for one of the two
+        // column halves' partial maxima, and the block is computed iff some half of some row wants it.
+        const float p_loc = (pm == -INFINITY) ? -INFINITY : pm * sl2;
+        bool want = true;
+        if (use_skip) want = row_valid && (p_loc != -INFINITY) && (p_loc - fmaxf(m_run, p_loc) >= tau2);
+        const bool compute = named_bar_red_or(2, kSoftmaxThreads, want);
+        // a skipped block leaves every row's running max unchanged (m_loc < m_run + tau2 <= m_run)
+        float m_new = m_run;
+        if (compute) {
+          sm.pmax[g][t] = pm;
+          named_bar_sync(3, kSoftmaxThreads);
+          const float mx = fmaxf(sm.pmax[0][t], sm.pmax[1][t]);
+          const float m_loc = (mx == -INFINITY) ? -INFINITY : mx * sl2;
+          m_new = fmaxf(m_run, m_loc);
+        }
+        m_run = m_new;
+        if (leader && flags_row) flags_row[ki_k] = compute ? kVisitComputed : kVisitSkipped;
+        if (!compute) continue;
+        if (leader) {
+          sm.pv_cmd[c & 3] = (c_item == 0) ? 2 : 1;
+          sm.vreq[c & 3] = sm.sinfo[v & 3];
+          mbar_arrive(&sm.vreq_full[c & 3]);
+        }
+        // lazy rescale of O and l when the max rises by more than 2^8
+        const bool first_mass = (m_ref == -INFINITY) && (m_new != -INFINITY);
+        const bool rescale = (m_ref != -INFINITY) && (m_new > m_ref + kRescaleLog2);
+        float alpha = 1.0f;
+        if (first_mass) m_ref = m_new;
+        if (rescale) {
+          alpha = ex2_approx(m_ref - m_new);
+          m_ref = m_new;
+          l_part *= alpha;
+        }
+        // P = exp2(S * scale * log2(e) - m_ref) as bf16 pairs; masked entries are -inf -> 0
+        const float base = (m_ref == -INFINITY) ? 0.0f : m_ref;
+        uint32_t pk[SC / 2];
+        float rs4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-      for (int e = 0; e < SC / 2; ++e) {
-        float x0, x1;
-        fma2_bc(x0, x1, sv[2 * e], sv[2 * e + 1], sl2, -base);
-        const float p0 = ex2_approx(x0);
-        const float p1 = ex2_approx(x1);
-        add2_acc(rs4[(e & 1) * 2], rs4[(e & 1) * 2 + 1], p0, p1);
-        pk[e] = pack_bf16x2(p0, p1);
-      }
-      l_part += (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
-      // the P buffer written now was read by the P.V two computed visits ago
-      if (c >= 2) {
-        bool okp = wait_parity_bounded(&sm.o_done[c & 1], ((c - 2) >> 1) & 1, abort_flag, a.status);
-        if (!__all_sync(0xffffffffu, okp)) { local_fail = true; continue; }
-      }
-      tc_fence_after();
-      tmem_st_n<SC / 2>(tmem + lane_addr + ((c & 1) ? kTmemP1 : kTmemP0) + g * (SC / 2), pk);
-      tmem_wait_st();
-      // O (this half's columns) is scaled once every earlier P.V has landed; P.V of this visit
-      // is issued only after p_full, so it accumulates onto the scaled O
-      if (__any_sync(0xffffffffu, rescale) && c > 0) {
-        bool okr = wait_parity_bounded(&sm.o_done[(c - 1) & 1], ((c - 1) >> 1) & 1, abort_flag, a.status);
-        if (!__all_sync(0xffffffffu, okr)) { local_fail = true; continue; }
+        for (int e = 0; e < SC / 2; ++e) {
+          float x0, x1;
+          fma2_bc(x0, x1, sv[2 * e], sv[2 * e + 1], sl2, -base);
+          const float p0 = ex2_approx(x0);
+          const float p1 = ex2_approx(x1);
+          add2_acc(rs4[(e & 1) * 2], rs4[(e & 1) * 2 + 1], p0, p1);
+          pk[e] = pack_bf16x2(p0, p1);
+        }
+        l_part += (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
+        // the P buffer written now was read by the P.V two computed visits ago
+        if (c >= 2) {
+          bool okp = wait_parity_bounded(&sm.o_done[c & 1], ((c - 2) >> 1) & 1, abort_flag, a.status);
+          if (!__all_sync(0xffffffffu, okp)) { local_fail = true; continue; }
+        }
         tc_fence_after();
-        const uint32_t ob = tmem + lane_addr + kTmemO + g * OC;
+        tmem_st_n<SC / 2>(tmem + lane_addr + ((c & 1) ? kTmemP1 : kTmemP0) + g * (SC / 2), pk);
+        tmem_wait_st();
+        // O (this half's columns) is scaled once every earlier P.V of the item has landed; P.V of
+        // this visit is issued only after p_full, so it accumulates onto the scaled O
+        if (__any_sync(0xffffffffu, rescale) && c_item > 0) {
+          bool okr = wait_parity_bounded(&sm.o_done[(c - 1) & 1], ((c - 1) >> 1) & 1, abort_flag, a.status);
+          if (!__all_sync(0xffffffffu, okr)) { local_fail = true; continue; }
+          tc_fence_after();
+          const uint32_t ob = tmem + lane_addr + kTmemO + g * OC;
 #pragma unroll 1
-        for (int cc = 0; cc < OC / 16; ++cc) {
-          uint32_t r[16];
-          tmem_ld16(ob + cc * 16, r);
-          tmem_wait_ld();
+          for (int cc = 0; cc < OC / 16; ++cc) {
+            uint32_t r[16];
+            tmem_ld16(ob + cc * 16, r);
+            tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-          tmem_st16(ob + cc * 16, r);
-          tmem_wait_st();
+            for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+            tmem_st16(ob + cc * 16, r);
+            tmem_wait_st();
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.p_full[c & 3]);
+        ++c;
+        ++c_item;
+      }
+      if (!ok) break;
+      // ---------------- epilogue: O / l -> bf16 -> global ----------------
+      if (c_item > 0) ok = wait_parity_bounded(&sm.o_done[(c - 1) & 1], ((c - 1) >> 1) & 1, abort_flag, a.status);
+      ok = named_bar_red_or(1, kSoftmaxThreads, !ok) ? false : ok;
+      if (!ok) break;
+      tc_fence_after();
+      sm.lsum[g][t] = l_part;
+      named_bar_sync(3, kSoftmaxThreads);
+      const float l_sum = sm.lsum[0][t] + sm.lsum[1][t];
+      const float inv_l = (l_sum > 0.0f) ? 1.0f / l_sum : 0.0f;
+      // the V slots are idle here: this item's P.V products are done, the next item's V loads
+      // follow its first vote
+      uint8_t* stage = &sm.v[0][0];
+      constexpr int CH = HD / 8;  // 16-byte chunks per output row
+      {
+        const uint32_t ob = tmem + lane_addr + kTmemO + g * OC;
+#pragma unroll
+        for (int cc = 0; cc < OC / 32; ++cc) {
+          uint32_t r[32];
+          if (c_item > 0) {
+            tmem_ld32(ob + cc * 32, r);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = 0u;
+          }
+          // 32 fp32 -> 16 packed bf16 pairs -> four 16-byte chunks, XOR-swizzled by row
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(r[q4 * 8 + 0]) * inv_l, __uint_as_float(r[q4 * 8 + 1]) * inv_l);
+            w.y = pack_bf16x2(__uint_as_float(r[q4 * 8 + 2]) * inv_l, __uint_as_float(r[q4 * 8 + 3]) * inv_l);
+            w.z = pack_bf16x2(__uint_as_float(r[q4 * 8 + 4]) * inv_l, __uint_as_float(r[q4 * 8 + 5]) * inv_l);
+            w.w = pack_bf16x2(__uint_as_float(r[q4 * 8 + 6]) * inv_l, __uint_as_float(r[q4 * 8 + 7]) * inv_l);
+            const int chunk = (g * OC) / 8 + cc * 4 + q4;   // 16-byte chunk of the row
+            const int phys_chunk = chunk ^ (t & (CH - 1));
+            *reinterpret_cast<uint4*>(stage + t * (HD * 2) + phys_chunk * 16) = w;
+          }
         }
       }
       tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.p_full[c & 3]);
-      ++c;
+      named_bar_sync(3, kSoftmaxThreads);
+      {
+        const int rows = min(BLK, L - i * BLK);
+        uint8_t* out = reinterpret_cast<uint8_t*>(a.out);
+        const int tid = g * 128 + t;
+        for (int e = tid; e < rows * CH; e += kSoftmaxThreads) {
+          const int r = e / CH, chunk = e % CH;
+          const uint4 w = *reinterpret_cast<const uint4*>(stage + r * (HD * 2) + ((chunk ^ (r & (CH - 1))) * 16));
+          const size_t tok = static_cast<size_t>(it.tok0) + static_cast<size_t>(i) * BLK + r;
+          *reinterpret_cast<uint4*>(out + ((tok * a.num_q_heads + it.h) * HD) * 2 + chunk * 16) = w;
+        }
+      }
+      // the staging reads finish before a later TMA load may refill the V slots
+      fence_proxy_async_smem();
+      named_bar_sync(3, kSoftmaxThreads);
     }
     // end markers for the V producer and the O issuer
     if (leader) {
@@ -541,53 +656,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.p_full[c & 3]);
-    // ---------------- epilogue: O / l -> bf16 -> global ----------------
-    if (ok && c > 0) ok = wait_parity_bounded(&sm.o_done[(c - 1) & 1], ((c - 1) >> 1) & 1, abort_flag, a.status);
-    tc_fence_after();
-    sm.lsum[g][t] = l_part;
-    named_bar_sync(1, kSoftmaxThreads);
-    const float l_sum = sm.lsum[0][t] + sm.lsum[1][t];
-    const float inv_l = (l_sum > 0.0f) ? 1.0f / l_sum : 0.0f;
-    uint8_t* stage = &sm.q[0];  // every UMMA reading Q has completed
-    constexpr int CH = HD / 8;  // 16-byte chunks per output row
-    {
-      const uint32_t ob = tmem + lane_addr + kTmemO + g * OC;
-#pragma unroll
-      for (int cc = 0; cc < OC / 32; ++cc) {
-        uint32_t r[32];
-        if (c > 0) {
-          tmem_ld32(ob + cc * 32, r);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) r[e] = 0u;
-        }
-        // 32 fp32 -> 16 packed bf16 pairs -> four 16-byte chunks, XOR-swizzled by row
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          uint4 w;
-          w.x = pack_bf16x2(__uint_as_float(r[q4 * 8 + 0]) * inv_l, __uint_as_float(r[q4 * 8 + 1]) * inv_l);
-          w.y = pack_bf16x2(__uint_as_float(r[q4 * 8 + 2]) * inv_l, __uint_as_float(r[q4 * 8 + 3]) * inv_l);
-          w.z = pack_bf16x2(__uint_as_float(r[q4 * 8 + 4]) * inv_l, __uint_as_float(r[q4 * 8 + 5]) * inv_l);
-          w.w = pack_bf16x2(__uint_as_float(r[q4 * 8 + 6]) * inv_l, __uint_as_float(r[q4 * 8 + 7]) * inv_l);
-          const int chunk = (g * OC) / 8 + cc * 4 + q4;   // 16-byte chunk of the row
-          const int phys_chunk = chunk ^ (t & (CH - 1));
-          *reinterpret_cast<uint4*>(stage + t * (HD * 2) + phys_chunk * 16) = w;
-        }
-      }
-    }
-    named_bar_sync(2, kSoftmaxThreads);
-    {
-      const int rows = min(BLK, L - i * BLK);
-      uint8_t* out = reinterpret_cast<uint8_t*>(a.out);
-      const int tid = g * 128 + t;
-      for (int e = tid; e < rows * CH; e += kSoftmaxThreads) {
-        const int r = e / CH, chunk = e % CH;
-        const uint4 w = *reinterpret_cast<const uint4*>(stage + r * (HD * 2) + ((chunk ^ (r & (CH - 1))) * 16));
-        const size_t tok = static_cast<size_t>(tok0) + static_cast<size_t>(i) * BLK + r;
-        *reinterpret_cast<uint4*>(out + ((tok * a.num_q_heads + h) * HD) * 2 + chunk * 16) = w;
-      }
-    }
   }
 
   tc_fence_before();
@@ -627,7 +695,16 @@ cudaError_t launch_osk_t(const OskLaunch& L, cudaStream_t stream) {
   const long long items =
       static_cast<long long>(L.num_kv_heads) * a.nqb_max * L.num_reqs * (L.num_q_heads / L.num_kv_heads);
   if (items <= 0) return cudaSuccess;
-  osk_kernel<BLK, HD><<<static_cast<unsigned>(items), kThreads, smem, stream>>>(L.qmap, L.kmap, L.vmap, a);
+  if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
+  a.num_items = static_cast<int>(items);
+  // persistent: one CTA per SM walks the items with a grid stride
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = static_cast<unsigned>(items < sms ? items : sms);
+  osk_kernel<BLK, HD><<<grid, kThreads, smem, stream>>>(L.qmap, L.kmap, L.vmap, a);
   return cudaGetLastError();
 }
 
