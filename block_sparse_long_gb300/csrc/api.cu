@@ -178,19 +178,25 @@ int cosa_sparse_prefill(const cosa_params* p, const void* q, const int32_t* cu_s
   if (p->total_tokens == 0) return COSA_OK;
   OskLaunch L{};
   const cuuint64_t d = static_cast<cuuint64_t>(p->head_dim);
+  // {d mod 64, row, d / 64, head} views: see OskLaunch
+  const cuuint64_t dh = d / 64;
   {
-    const cuuint64_t dims[3] = {d, static_cast<cuuint64_t>(p->num_q_heads), static_cast<cuuint64_t>(p->total_tokens)};
-    const cuuint64_t strides[2] = {d * 2, d * 2 * p->num_q_heads};
-    const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(p->block_size)};
-    if (!encode_tiled(&L.qmap, q, 3, dims, strides, box)) return COSA_ERR_CUDA;
+    const cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(p->total_tokens), dh, static_cast<cuuint64_t>(p->num_q_heads)};
+    const cuuint64_t strides[3] = {d * 2 * p->num_q_heads, 128, d * 2};
+    const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(p->block_size), 1, 1};
+    if (!encode_tiled(&L.qmap, q, 4, dims, strides, box)) return COSA_ERR_CUDA;
   }
   {
-    const cuuint64_t dims[4] = {d, static_cast<cuuint64_t>(p->num_kv_heads), static_cast<cuuint64_t>(p->page_size),
-                                static_cast<cuuint64_t>(p->num_pages)};
-    const cuuint64_t strides[3] = {d * 2, d * 2 * p->num_kv_heads, d * 2 * p->num_kv_heads * p->page_size};
-    const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(p->page_size), 1};
-    if (!encode_tiled(&L.kmap, k_cache, 4, dims, strides, box)) return COSA_ERR_CUDA;
-    if (!encode_tiled(&L.vmap, v_cache, 4, dims, strides, box)) return COSA_ERR_CUDA;
+    const int64_t rows = static_cast<int64_t>(p->num_pages) * p->page_size;
+    if (rows > INT32_MAX) return COSA_ERR_UNSUPPORTED;   // TMA coordinates are 32-bit
+    const cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(rows), dh, static_cast<cuuint64_t>(p->num_kv_heads)};
+    const cuuint64_t strides[3] = {d * 2 * p->num_kv_heads, 128, d * 2};
+    const cuuint32_t box_blk[4] = {64, static_cast<cuuint32_t>(p->block_size), static_cast<cuuint32_t>(dh), 1};
+    const cuuint32_t box_pg[4] = {64, static_cast<cuuint32_t>(p->page_size), 1, 1};
+    if (!encode_tiled(&L.kmap_blk, k_cache, 4, dims, strides, box_blk)) return COSA_ERR_CUDA;
+    if (!encode_tiled(&L.kmap_pg, k_cache, 4, dims, strides, box_pg)) return COSA_ERR_CUDA;
+    if (!encode_tiled(&L.vmap_blk, v_cache, 4, dims, strides, box_blk)) return COSA_ERR_CUDA;
+    if (!encode_tiled(&L.vmap_pg, v_cache, 4, dims, strides, box_pg)) return COSA_ERR_CUDA;
   }
   L.cu_seqlens = cu_seqlens;
   L.page_table = page_table;

@@ -20,10 +20,15 @@ bool encode_tiled_bf16(CUtensorMap* map, const void* base, int rank, const cuuin
 // ---------------------------------------------------------------------------
 // OSK
 // ---------------------------------------------------------------------------
+// The TMA maps view a [rows, heads, d] bf16 tensor as {d mod 64, row, d / 64, head} (row stride
+// heads * d * 2 bytes, then 128 bytes, then d * 2 bytes), so that one box lands in shared memory as
+// [d / 64][rows][128 B], the 128-byte-swizzled K-major layout the tensor cores read.
 struct OskLaunch {
-  CUtensorMap qmap;  // q   bf16 [T, Hq, d]: dims {d, Hq, T}, box {64, 1, block_size}, SW128
-  CUtensorMap kmap;  // K   bf16 [pages, P, Hkv, d]: dims {d, Hkv, P, pages}, box {64, 1, P, 1}, SW128
-  CUtensorMap vmap;  // V   same as K
+  CUtensorMap qmap;      // q [T, Hq, d]: box {64, block_size, 1, 1} (one 64-wide d chunk of a query block)
+  CUtensorMap kmap_blk;  // K [pages * P, Hkv, d]: box {64, block_size, d / 64, 1} (a block on consecutive pages)
+  CUtensorMap kmap_pg;   // K: box {64, P, 1, 1} (one d chunk of one page)
+  CUtensorMap vmap_blk;  // V, as kmap_blk
+  CUtensorMap vmap_pg;   // V, as kmap_pg
   const int32_t* cu_seqlens;
   const int32_t* page_table;
   const int32_t* mask;

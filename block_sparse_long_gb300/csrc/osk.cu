@@ -70,8 +70,7 @@ struct alignas(1024) OskSmem {
   uint64_t o_done[2];
   uint64_t vreq_full[4];
   uint64_t cleanup;
-  KInfo kinfo[NK];
-  KInfo sinfo[4];                             // visit info of visit v (slot v & 3), written with S(v)
+  KInfo info[8];                              // visit info of visit v (slot v & 7), written with K(v)
   KInfo vreq[4];
   float pmax[2][128];                         // partial row maxima of the two column halves
   float lsum[2][128];                         // partial row sums, exchanged at the end
@@ -97,6 +96,17 @@ struct OskArgs {
 };
 
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
+
+// every page of the block exists and they occupy consecutive physical pages
+template <typename Arr>
+__device__ __forceinline__ bool pages_consecutive(uint32_t pages, uint32_t all_pages, const Arr& phys, int n) {
+  if (pages != all_pages) return false;
+  bool ok = true;
+#pragma unroll
+  for (int u = 1; u < kMaxPagesPerBlock; ++u)
+    if (u < n) ok = ok && (phys[u] == phys[0] + u);
+  return ok;
+}
 
 // Bounded wait taken by every lane of a warp; the warp agrees on the outcome.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status) {
@@ -140,8 +150,9 @@ __device__ __forceinline__ Item decode_item(const OskArgs& a, int idx, int blk) 
 
 template <int BLK, int HD>
 __global__ void __launch_bounds__(kThreads, 1)
-    osk_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-               const __grid_constant__ CUtensorMap vmap, const OskArgs a) {
+    osk_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap_blk,
+               const __grid_constant__ CUtensorMap kmap_pg, const __grid_constant__ CUtensorMap vmap_blk,
+               const __grid_constant__ CUtensorMap vmap_pg, const OskArgs a) {
   using S = OskSmem<BLK, HD>;
   constexpr int NK = S::NK, NV = S::NV;
   constexpr int DH = HD / 64;       // 64-wide d chunks
@@ -200,8 +211,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane = lane_id();
     if (lane == 0) {
       tma_prefetch_desc(&qmap);
-      tma_prefetch_desc(&kmap);
-      tma_prefetch_desc(&vmap);
+      tma_prefetch_desc(&kmap_blk);
+      tma_prefetch_desc(&kmap_pg);
+      tma_prefetch_desc(&vmap_blk);
+      tma_prefetch_desc(&vmap_pg);
     }
     int v = 0, n = 0;
     bool ok = true;
@@ -226,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         mbar_arrive_expect_tx(&sm.q_full, BLK * HD * 2);
         for (int dh = 0; dh < DH; ++dh)
-          tma_load_3d(&sm.q[dh * 128 * 128], &qmap, &sm.q_full, dh * 64, it.h, it.tok0 + i * BLK);
+          tma_load_4d(&sm.q[dh * 128 * 128], &qmap, &sm.q_full, 0, it.tok0 + i * BLK, dh, it.h);
       }
       ++n;
       const int32_t* pt_row = a.page_table + static_cast<size_t>(it.b) * a.max_pages_per_req;
@@ -267,19 +280,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (v >= NK) ok = warp_wait(&sm.k_free[slot], ((v / NK) - 1) & 1, abort_flag, a.status);
           if (!ok) break;
           if (lane == 0) {
-            KInfo& ki = sm.kinfo[slot];
+            KInfo& ki = sm.info[v & 7];
             ki.blk = jj;
             ki.pages = pg;
             ki.k = k0 + src;
             ki.kvh = kvh;
 #pragma unroll
             for (int u = 0; u < kMaxPagesPerBlock; ++u) ki.phys[u] = ph[u];
-            const uint32_t bytes = static_cast<uint32_t>(__popc(pg)) * DH * P * 128u;
-            mbar_arrive_expect_tx(&sm.k_full[slot], bytes);
-            for (int u = 0; u < pages_per_blk; ++u) {
-              if (!((pg >> u) & 1u)) continue;
-              for (int dh = 0; dh < DH; ++dh)
-                tma_load_4d(&sm.k[slot][dh * S::HALF + u * P * 128], &kmap, &sm.k_full[slot], dh * 64, kvh, 0, ph[u]);
+            if (pages_consecutive(pg, all_pages, ph, pages_per_blk)) {
+              // the block's pages follow each other in the cache: one copy of the whole tile
+              mbar_arrive_expect_tx(&sm.k_full[slot], BLK * HD * 2);
+              tma_load_4d(&sm.k[slot][0], &kmap_blk, &sm.k_full[slot], 0, ph[0] * P, 0, kvh);
+            } else {
+              const uint32_t bytes = static_cast<uint32_t>(__popc(pg)) * DH * P * 128u;
+              mbar_arrive_expect_tx(&sm.k_full[slot], bytes);
+              for (int u = 0; u < pages_per_blk; ++u) {
+                if (!((pg >> u) & 1u)) continue;
+                for (int dh = 0; dh < DH; ++dh)
+                  tma_load_4d(&sm.k[slot][dh * S::HALF + u * P * 128], &kmap_pg, &sm.k_full[slot], 0, ph[u] * P, dh, kvh);
+              }
             }
           }
           __syncwarp();
@@ -291,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int slot = v % NK;
         if (v >= NK) ok = warp_wait(&sm.k_free[slot], ((v / NK) - 1) & 1, abort_flag, a.status);
         if (ok && lane == 0) {
-          sm.kinfo[slot].blk = -1;
+          sm.info[v & 7].blk = -1;
           mbar_arrive(&sm.k_full[slot]);
         }
         __syncwarp();
@@ -311,6 +330,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // S(v) = Q K_v^T once K(v) has landed and the softmax has read S(v - 2), the buffer it reuses.
     if (lane_id() == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, BLK, false, false);
+      // descriptors differ from these bases only in the start-address field (address >> 4)
+      const uint64_t qdesc = smem_desc_sw128(smem_u32(&sm.q[0]), 16, 1024);
+      const uint64_t kdesc = smem_desc_sw128(smem_u32(&sm.k[0][0]), 16, 1024);
       int vv = 0, n = 0;
       bool ok = true;
       for (int idx = blockIdx.x; idx < a.num_items && ok; idx += gridDim.x) {
@@ -326,10 +348,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          const KInfo ki = sm.kinfo[slot];
-          sm.sinfo[vv & 3] = ki;
+          // info[vv & 7] is rewritten with K(vv + 8), long after the softmax has read it
+          const int blk = sm.info[vv & 7].blk;
           mbar_arrive(&sm.s_full[sb]);
-          if (ki.blk < 0) {
+          if (blk < 0) {
             // end of the item: no product; the K slot and the S buffer pass on unused
             mbar_arrive(&sm.s_full[sb]);
             mbar_arrive(&sm.k_free[slot]);
@@ -337,10 +359,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
+          const uint64_t kslot = kdesc + static_cast<uint64_t>(slot * (S::TILE >> 4));
 #pragma unroll
           for (int kk = 0; kk < HD / 16; ++kk) {
-            const uint64_t ad = smem_desc_sw128(smem_u32(&sm.q[(kk >> 2) * 128 * 128 + (kk & 3) * 32]), 16, 1024);
-            const uint64_t bd = smem_desc_sw128(smem_u32(&sm.k[slot][(kk >> 2) * S::HALF + (kk & 3) * 32]), 16, 1024);
+            const uint64_t ad = qdesc + static_cast<uint64_t>(((kk >> 2) * 128 * 128 + (kk & 3) * 32) >> 4);
+            const uint64_t bd = kslot + static_cast<uint64_t>(((kk >> 2) * S::HALF + (kk & 3) * 32) >> 4);
             umma_ss(tmem + (sb ? kTmemS1 : kTmemS0), ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
           }
           umma_commit(&sm.s_full[sb]);
@@ -361,6 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the first computed visit of an item overwrites O.
     if (lane_id() == 0) {
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, HD, false, true);
+      const uint64_t vdesc = smem_desc_sw128(smem_u32(&sm.v[0][0]), S::HALF, 1024);
       for (int c = 0;; ++c) {
         if (!wait_parity_bounded(&sm.p_full[c & 3], (c >> 2) & 1, abort_flag, a.status)) break;
         const int cmd = sm.pv_cmd[c & 3];
@@ -369,9 +393,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_parity_bounded(&sm.v_full[slot], (c / NV) & 1, abort_flag, a.status)) break;
         tc_fence_after();
         const uint32_t pcol = (c & 1) ? kTmemP1 : kTmemP0;
+        const uint64_t vslot = vdesc + static_cast<uint64_t>(slot * (S::TILE >> 4));
 #pragma unroll
         for (int kk = 0; kk < BLK / 16; ++kk) {
-          const uint64_t bd = smem_desc_sw128(smem_u32(&sm.v[slot][kk * 16 * 128]), S::HALF, 1024);
+          const uint64_t bd = vslot + static_cast<uint64_t>((kk * 16 * 128) >> 4);
           umma_ts(tmem + kTmemO, tmem + pcol + kk * 8, bd, idesc_pv, (cmd == 1 || kk > 0) ? 1u : 0u);
         }
         umma_commit(&sm.v_free[slot]);
@@ -408,12 +433,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       }
       if (lane == 0) {
-        const uint32_t bytes = static_cast<uint32_t>(__popc(r.pages)) * DH * P * 128u;
-        mbar_arrive_expect_tx(&sm.v_full[slot], bytes);
-        for (int u = 0; u < pages_per_blk; ++u) {
-          if (!((r.pages >> u) & 1u)) continue;
-          for (int dh = 0; dh < DH; ++dh)
-            tma_load_4d(&sm.v[slot][dh * S::HALF + u * P * 128], &vmap, &sm.v_full[slot], dh * 64, r.kvh, 0, r.phys[u]);
+        if (pages_consecutive(r.pages, all_pages, r.phys, pages_per_blk)) {
+          mbar_arrive_expect_tx(&sm.v_full[slot], BLK * HD * 2);
+          tma_load_4d(&sm.v[slot][0], &vmap_blk, &sm.v_full[slot], 0, r.phys[0] * P, 0, r.kvh);
+        } else {
+          const uint32_t bytes = static_cast<uint32_t>(__popc(r.pages)) * DH * P * 128u;
+          mbar_arrive_expect_tx(&sm.v_full[slot], bytes);
+          for (int u = 0; u < pages_per_blk; ++u) {
+            if (!((r.pages >> u) & 1u)) continue;
+            for (int dh = 0; dh < DH; ++dh)
+              tma_load_4d(&sm.v[slot][dh * S::HALF + u * P * 128], &vmap_pg, &sm.v_full[slot], 0, r.phys[u] * P, dh, r.kvh);
+          }
         }
       }
       __syncwarp();
@@ -464,10 +494,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool okw = !local_fail && wait_parity_bounded(&sm.s_full[sb], (v >> 1) & 1, abort_flag, a.status);
         okw = __all_sync(0xffffffffu, okw);
         if (okw) {
-          // slot v & 3 is rewritten with S(v + 4), which waits for S(v + 2) to be released
-          ki_blk = sm.sinfo[v & 3].blk;
-          ki_pages = sm.sinfo[v & 3].pages;
-          ki_k = sm.sinfo[v & 3].k;
+          // slot v & 7 is rewritten with K(v + 8), which waits for S(v + 3) to be released
+          ki_blk = sm.info[v & 7].blk;
+          ki_pages = sm.info[v & 7].pages;
+          ki_k = sm.info[v & 7].k;
           if (ki_blk >= 0) {
             tc_fence_after();
 #pragma unroll
@@ -532,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!compute) continue;
         if (leader) {
           sm.pv_cmd[c & 3] = (c_item == 0) ? 2 : 1;
-          sm.vreq[c & 3] = sm.sinfo[v & 3];
+          sm.vreq[c & 3] = sm.info[v & 7];
           mbar_arrive(&sm.vreq_full[c & 3]);
         }
         // lazy rescale of O and l when the max rises by more than 2^8
@@ -704,7 +734,7 @@ cudaError_t launch_osk_t(const OskLaunch& L, cudaStream_t stream) {
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(items < sms ? items : sms);
-  osk_kernel<BLK, HD><<<grid, kThreads, smem, stream>>>(L.qmap, L.kmap, L.vmap, a);
+  osk_kernel<BLK, HD><<<grid, kThreads, smem, stream>>>(L.qmap, L.kmap_blk, L.kmap_pg, L.vmap_blk, L.vmap_pg, a);
   return cudaGetLastError();
 }
 
