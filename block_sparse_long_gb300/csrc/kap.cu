@@ -648,6 +648,83 @@ __device__ __forceinline__ unsigned long long sort_key(bool hrm, float s, int j)
 }
 __device__ __forceinline__ int key_block(unsigned long long k) { return 0x7FFFFFFF - static_cast<int>(k & 0x7FFFFFFFull); }
 
+// ---- bitonic sort (descending) of kSelectThreads * E keys held E per thread, thread t holding
+// positions t*E .. t*E+E-1: partners closer than E are swapped in registers, closer than 32*E
+// through warp shuffles, the rest through shared memory.
+template <int JJ, int E>
+__device__ __forceinline__ void sort_stage_reg(unsigned long long (&v)[E], int k, int tid) {
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    if ((e & JJ) == 0) {
+      const int x = tid * E + e;
+      const bool desc = (x & k) == 0;
+      const unsigned long long lo = v[e], hi = v[e | JJ];
+      const bool sw = desc ? (lo < hi) : (lo > hi);
+      v[e] = sw ? hi : lo;
+      v[e | JJ] = sw ? lo : hi;
+    }
+  }
+}
+
+template <int E>
+__device__ void sort_keys_desc(unsigned long long (&v)[E], unsigned long long* buf, int N) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  for (int k = 2; k <= N; k <<= 1) {
+    for (int jj = k >> 1; jj > 0; jj >>= 1) {
+      if (jj < E) {
+        if (jj == 1) sort_stage_reg<1, E>(v, k, tid);
+        else if constexpr (E > 2) {
+          if (jj == 2) sort_stage_reg<2, E>(v, k, tid);
+          else if constexpr (E > 4) {
+            if (jj == 4) sort_stage_reg<4, E>(v, k, tid);
+            else if constexpr (E > 8) {
+              if (jj == 8) sort_stage_reg<8, E>(v, k, tid);
+            }
+          }
+        }
+      } else if (jj < 32 * E) {
+        const int ld = jj / E;
+        const bool lower = (lane & ld) == 0;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const unsigned long long o = __shfl_xor_sync(0xffffffffu, v[e], ld);
+          const bool desc = ((tid * E + e) & k) == 0;
+          const bool take_max = (lower == desc);
+          v[e] = take_max ? (v[e] > o ? v[e] : o) : (v[e] < o ? v[e] : o);
+        }
+      } else {
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < E; ++e) buf[tid * E + e] = v[e];
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int x = tid * E + e, y = x ^ jj;
+          const unsigned long long o = buf[y];
+          const bool take_max = (x < y) == ((x & k) == 0);
+          v[e] = take_max ? (v[e] > o ? v[e] : o) : (v[e] < o ? v[e] : o);
+        }
+      }
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int e = 0; e < E; ++e) buf[tid * E + e] = v[e];
+  __syncthreads();
+}
+
+// keys[j] for j < J (0 past J) sorted descending into key[0..N)
+template <int E>
+__device__ void sort_block_keys(unsigned long long* key, const uint8_t* hrm, const float* score, int J, int N) {
+  unsigned long long v[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int j = threadIdx.x * E + e;
+    v[e] = (j < J) ? sort_key(hrm[j] != 0, fmaxf(score[j], 0.0f), j) : 0ull;
+  }
+  sort_keys_desc<E>(v, key, N);
+}
+
 template <int HD, int KB>
 __global__ void __launch_bounds__(kSelectThreads) kap_select_kernel(KapArgs a, int cap) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -660,7 +737,7 @@ __global__ void __launch_bounds__(kSelectThreads) kap_select_kernel(KapArgs a, i
   uint8_t* hrm = reinterpret_cast<uint8_t*>(rep_pos + cap);                    // [cap] HRM flags
   double* terms = reinterpret_cast<double*>(
       (reinterpret_cast<uintptr_t>(hrm + cap) + 15) & ~uintptr_t(15));         // [kRepChunk * KB] row terms
-  __shared__ int32_t n_rep_s, n_hrm_s;
+  __shared__ int32_t n_rep_s, n_hrm_s, cstar_s[2], warp_cnt_s[kSelectThreads / 32];
 
   const int tid = threadIdx.x;
   int idx = blockIdx.x;
@@ -699,32 +776,32 @@ __global__ void __launch_bounds__(kSelectThreads) kap_select_kernel(KapArgs a, i
     }
   }
   __syncthreads();
-  // sort keys (bitonic, descending) over the next power of two
+  // sort keys (bitonic, descending) over N = max(next power of two, threads) positions
   int n2 = 1;
   while (n2 < J) n2 <<= 1;
-  for (int j = tid; j < n2; j += blockDim.x)
-    key[j] = (j < J) ? sort_key(hrm[j] != 0, fmaxf(a.score[sbase + j], 0.0f), j) : 0ull;
-  __syncthreads();
-  for (int k = 2; k <= n2; k <<= 1) {
-    for (int jj = k >> 1; jj > 0; jj >>= 1) {
-      for (int x = tid; x < n2; x += blockDim.x) {
-        const int y = x ^ jj;
-        if (y > x) {
-          const unsigned long long kx = key[x], ky = key[y];
-          const bool desc = (x & k) == 0;
-          if (desc ? (kx < ky) : (kx > ky)) { key[x] = ky; key[y] = kx; }
-        }
-      }
-      __syncthreads();
+  const int N = n2 < kSelectThreads ? kSelectThreads : n2;
+  if (tid == 0) {
+    n_hrm_s = 0;
+    cstar_s[0] = cstar_s[1] = 0x7fffffff;
+  }
+  {
+    int cnt = 0;
+    for (int j = tid; j < J; j += blockDim.x) cnt += hrm[j] != 0;
+    __syncthreads();
+    if (cnt) atomicAdd(&n_hrm_s, cnt);
+  }
+  {
+    const float* sc = a.score + sbase;
+    switch (N / kSelectThreads) {
+      case 1: sort_block_keys<1>(key, hrm, sc, J, N); break;
+      case 2: sort_block_keys<2>(key, hrm, sc, J, N); break;
+      case 4: sort_block_keys<4>(key, hrm, sc, J, N); break;
+      case 8: sort_block_keys<8>(key, hrm, sc, J, N); break;
+      default: sort_block_keys<16>(key, hrm, sc, J, N); break;
     }
   }
+  const int nh = n_hrm_s;   // HRM keys sort first
   // score intervals per sorted position
-  if (tid == 0) {
-    n_rep_s = 0;
-    int nh = 0;
-    while (nh < J && (key[nh] >> 63)) ++nh;
-    n_hrm_s = nh;
-  }
   for (int p = tid; p < n2; p += blockDim.x) {
     if (p < J) {
       const int j = key_block(key[p]);
@@ -738,43 +815,83 @@ __global__ void __launch_bounds__(kSelectThreads) kap_select_kernel(KapArgs a, i
     }
   }
   __syncthreads();
-  const int nh = n_hrm_s;
-  // suffix maximum of hi inside each group (Hillis-Steele, log2(n2) rounds)
+  // within each group (HRM positions [0, nh), the rest [nh, J)): suffix maximum of hi and prefix
+  // minimum of lo (Hillis-Steele, log2(n2) rounds); lo is overwritten by its prefix minimum
   for (int p = tid; p < n2; p += blockDim.x) suf[p] = hi[p];
   __syncthreads();
   for (int off = 1; off < n2; off <<= 1) {
-    float tmp[16];
+    float ts[16], tp[16];
     int cnt = 0;
     for (int p = tid; p < n2; p += blockDim.x, ++cnt) {
-      const int q = p + off;
-      const bool same = q < n2 && ((p < nh) == (q < nh));
-      tmp[cnt & 15] = same ? fmaxf(suf[p], suf[q]) : suf[p];
+      const int q = p + off, r = p - off;
+      const bool sq = q < n2 && ((p < nh) == (q < nh));
+      const bool sr = r >= 0 && ((p < nh) == (r < nh));
+      ts[cnt & 15] = sq ? fmaxf(suf[p], suf[q]) : suf[p];
+      tp[cnt & 15] = sr ? fminf(lo[p], lo[r]) : lo[p];
     }
     __syncthreads();
     cnt = 0;
-    for (int p = tid; p < n2; p += blockDim.x, ++cnt) suf[p] = tmp[cnt & 15];
+    for (int p = tid; p < n2; p += blockDim.x, ++cnt) {
+      suf[p] = ts[cnt & 15];
+      lo[p] = tp[cnt & 15];
+    }
     __syncthreads();
   }
-  // clusters of positions whose relative order, or side of the budget cut, the bounds cannot
-  // certify: [p, q] grows while some later element of the group may exceed its lowest member
-  if (tid == 0) {
-    int nr = 0;
-    for (int g = 0; g < 2; ++g) {
-      const int g0 = g == 0 ? 0 : nh, g1 = g == 0 ? nh : J;
-      int p = g0;
-      while (p < g1 && p < K) {
-        float cmin = lo[p];
-        int q = p;
-        while (q + 1 < g1 && suf[q + 1] >= cmin) {
-          ++q;
-          cmin = fminf(cmin, lo[q]);
-        }
-        if (q > p)
-          for (int x = p; x <= q; ++x) rep_pos[nr++] = x;
-        p = q + 1;
+  // Clusters of positions whose relative order, or side of the budget cut, the bounds cannot
+  // certify.  The cut after position q is certain iff every element up to q (in its group)
+  // stays above every later one: min lo[g0..q] > max hi[q+1..g1).  (Cuts certified for the
+  // elements of q's own run suffice: an earlier certain cut already puts all elements before
+  // it above everything after it.)  Runs of two or more positions between certain cuts are
+  // repaired when they start before K.  hrm[] is reused for the cut flags.
+  uint8_t* cutf = hrm;
+  for (int p = tid; p < J; p += blockDim.x) {
+    const int g1 = p < nh ? nh : J;
+    cutf[p] = (p == g1 - 1) || (lo[p] > suf[p + 1]);
+  }
+  __syncthreads();
+  for (int p = tid; p < J; p += blockDim.x) {
+    const int g = p < nh ? 0 : 1;
+    const int g1 = g ? J : nh;
+    const int kg = min(K, g1);
+    if (p >= kg - 1 && cutf[p]) atomicMin(&cstar_s[g], p);
+  }
+  __syncthreads();
+  {
+    // each thread marks positions tid*E .. tid*E+E-1 in order; a block scan places them
+    const int E = N / kSelectThreads;
+    int cnt = 0;
+    uint32_t bits = 0;
+    for (int e = 0; e < E; ++e) {
+      const int x = tid * E + e;
+      if (x >= J) break;
+      const int g = x < nh ? 0 : 1;
+      const int g0 = g ? nh : 0, g1 = g ? J : nh;
+      const int kg = min(K, g1);
+      bool mk = false;
+      if (kg > g0) {
+        const bool multi = !cutf[x] || (x > g0 && !cutf[x - 1]);
+        mk = multi && (x < kg || x <= cstar_s[g]);
       }
+      if (mk) { bits |= 1u << e; ++cnt; }
     }
-    n_rep_s = nr;
+    const int lane = tid & 31, w = tid >> 5;
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_cnt_s[w] = incl;
+    __syncthreads();
+    int base = 0, total = 0;
+    for (int q = 0; q < kSelectThreads / 32; ++q) {
+      if (q < w) base += warp_cnt_s[q];
+      total += warp_cnt_s[q];
+    }
+    int pos = base + incl - cnt;
+    for (int e = 0; e < E; ++e)
+      if ((bits >> e) & 1u) rep_pos[pos++] = tid * E + e;
+    if (tid == 0) n_rep_s = total;
   }
   __syncthreads();
   const int n_rep = n_rep_s;
@@ -824,28 +941,40 @@ __global__ void __launch_bounds__(kSelectThreads) kap_select_kernel(KapArgs a, i
 #pragma unroll
           for (int o = LPK; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
           if (mx != -INFINITY) {
+            // candidates: keys whose fp32 logit is within 2 e_r of the row's block maximum; each
+            // candidate's float64 logit is taken by the whole warp (four elements per lane)
             const bool cand = vis && x >= mx - 2.0f * a.err[rbase + r];
-            double dp = 0.0;
-            if (cand) {
-#pragma unroll 1
-              for (int e = 0; e < SL; e += 8) {
-                float qv[8], kv[8];
-                load8_bf16(qr + e, qv);
-                load8_bf16(kr + e, kv);
+            uint32_t cmask = __ballot_sync(0xffffffffu, cand && sub == 0);
+            double dv = -INFINITY;
+            const uint16_t* qrow = qbase + static_cast<int64_t>(r) * HD;
+            while (cmask) {
+              const int g = (__ffs(cmask) - 1) / LPK;   // key group of the candidate
+              cmask &= cmask - 1;
+              const uint16_t* krow = a.ks + (krow0 + j * KB + g) * HD;
+              double dp = 0.0;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) dp = fma(static_cast<double>(qv[i]), static_cast<double>(kv[i]), dp);
+              for (int e = lane * (HD / 32); e < (lane + 1) * (HD / 32); e += 2) {
+                const uint32_t qw = *reinterpret_cast<const uint32_t*>(qrow + e);
+                const uint32_t kw = *reinterpret_cast<const uint32_t*>(krow + e);
+                dp = fma(static_cast<double>(__uint_as_float(qw << 16)), static_cast<double>(__uint_as_float(kw << 16)), dp);
+                dp = fma(static_cast<double>(__uint_as_float(qw & 0xffff0000u)),
+                         static_cast<double>(__uint_as_float(kw & 0xffff0000u)), dp);
               }
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) dp += __shfl_xor_sync(0xffffffffu, dp, o);
+              dv = fmax(dv, dp * a.sm_scale);
             }
-#pragma unroll
-            for (int o = LPK / 2; o > 0; o >>= 1) dp += __shfl_xor_sync(0xffffffffu, dp, o);
-            double dv = cand ? dp * a.sm_scale : -INFINITY;
-#pragma unroll
-            for (int o = LPK; o < 32; o <<= 1) dv = fmax(dv, __shfl_xor_sync(0xffffffffu, dv, o));
-            term = exp(dv - Mr);
+            term = dv - Mr;   // exponent; exp is taken below, one item per thread
+          } else {
+            term = -INFINITY;
           }
+        } else {
+          term = -INFINITY;
         }
         if (lane == 0) terms[item] = term;
       }
+      __syncthreads();
+      for (int item = tid; item < nm * nrows; item += blockDim.x) terms[item] = exp(terms[item]);
       __syncthreads();
       for (int m = tid; m < nm; m += blockDim.x) {
         double sum = 0.0;
@@ -941,7 +1070,7 @@ cudaError_t launch_kap_t(KapArgs a, size_t qs_rows, size_t ks_rows, cudaStream_t
     kap_rescan_kernel<HD><<<1024, 256, 0, stream>>>(a);
   }
   kap_logits_kernel<HD, KB, kModeScores><<<tiles, kLogitsThreads, tsm, stream>>>(qs_map, ks_map, a);
-  int cap = 32;
+  int cap = kSelectThreads;   // the sort works on at least one key per thread
   while (cap < a.nqb_max) cap <<= 1;
   const size_t ssm = select_smem_bytes(cap);
   e = cudaFuncSetAttribute(kap_select_kernel<HD, KB>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ssm));
