@@ -407,7 +407,37 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
       const uint32_t bits0 = __ldg(kval + ((kt * kKeyTile + g * 64) >> 5));
       const uint32_t bits1 = __ldg(kval + ((kt * kKeyTile + g * 64) >> 5) + 1);
       const int last = r - c0;                    // causal: columns <= last
-      if (MODE == kModeRowMax) {
+      // every column of this thread's half is visible: below the diagonal tile, all keys valid
+      const bool interior = row_ok && kt < rt && (bits0 & bits1) == 0xffffffffu;
+      if (MODE == kModeRowMax && interior) {
+        // tile maximum by a three-input max tree; the first index and the tile's second largest
+        // value are only needed when the running maximum rises (a few tiles per row)
+        float m8[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) m8[q] = fmaxf(__uint_as_float(va[2 * q]), __uint_as_float(va[2 * q + 1]));
+#pragma unroll
+        for (int q = 0; q < 8; ++q) m8[q] = fmax3f(m8[q], __uint_as_float(va[16 + 2 * q]), __uint_as_float(va[17 + 2 * q]));
+#pragma unroll
+        for (int q = 0; q < 8; ++q) m8[q] = fmax3f(m8[q], __uint_as_float(vb[2 * q]), __uint_as_float(vb[2 * q + 1]));
+#pragma unroll
+        for (int q = 0; q < 8; ++q) m8[q] = fmax3f(m8[q], __uint_as_float(vb[16 + 2 * q]), __uint_as_float(vb[17 + 2 * q]));
+        const float t1 = fmax3f(fmax3f(m8[0], m8[1], m8[2]), fmax3f(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+        if (t1 > r1) {
+          int e1 = 0;
+#pragma unroll
+          for (int e = 63; e >= 0; --e)
+            if (__uint_as_float(e < 32 ? va[e] : vb[e - 32]) == t1) e1 = e;
+          float t2 = -INFINITY;
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            if (e != e1) t2 = fmaxf(t2, __uint_as_float(e < 32 ? va[e] : vb[e - 32]));
+          r2 = fmaxf(r1, t2);
+          r1 = t1;
+          rc1 = c0 + e1;
+        } else {
+          r2 = fmaxf(r2, t1);
+        }
+      } else if (MODE == kModeRowMax) {
         // branch-free: second max = max(second, min(x, max)); argmax follows the first strict increase
 #pragma unroll
         for (int e = 0; e < 64; ++e) {
@@ -422,11 +452,16 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
 #pragma unroll
         for (int gg = 0; gg < 64 / KB; ++gg) {
           float bm = -INFINITY;
+          if (interior) {
 #pragma unroll
-          for (int e = gg * KB; e < (gg + 1) * KB; ++e) {
-            const uint32_t bits = e < 32 ? bits0 : bits1;
-            const float x = __uint_as_float(e < 32 ? va[e] : vb[e - 32]);
-            if (row_ok && e <= last && ((bits >> (e & 31)) & 1u)) bm = fmaxf(bm, x);
+            for (int e = gg * KB; e < (gg + 1) * KB; ++e) bm = fmaxf(bm, __uint_as_float(e < 32 ? va[e] : vb[e - 32]));
+          } else {
+#pragma unroll
+            for (int e = gg * KB; e < (gg + 1) * KB; ++e) {
+              const uint32_t bits = e < 32 ? bits0 : bits1;
+              const float x = __uint_as_float(e < 32 ? va[e] : vb[e - 32]);
+              if (row_ok && e <= last && ((bits >> (e & 31)) & 1u)) bm = fmaxf(bm, x);
+            }
           }
           const int j = (c0 + gg * KB) / KB;
           float x = 0.0f, xe = 0.0f;
