@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(256) kap_gather_kernel(KapArgs a) {
 // ---------------------------------------------------------------------------
 enum { kModeRowMax = 0, kModeScores = 1 };
 
-constexpr int kKeyStages = 4;           // K~ tiles in flight
+constexpr int kKeyStages = 2;           // K~ tiles in flight (two CTAs fit per SM)
 constexpr int kLogitsThreads = 320;      // warp 0 TMA, warp 1 UMMA, warps 2-9 epilogue
 
 template <int HD>
@@ -277,7 +277,7 @@ struct alignas(1024) KapTileSmem {
 // 2-9 read the accumulators: warp w serves TMEM lanes 32 (w % 4) .. + 31 and columns [64 g, 64 g + 64)
 // with g = (w - 2) / 4.
 template <int HD, int KB, int MODE>
-__global__ void __launch_bounds__(kLogitsThreads, 1)
+__global__ void __launch_bounds__(kLogitsThreads, 2)
     kap_logits_kernel(const __grid_constant__ CUtensorMap qs_map, const __grid_constant__ CUtensorMap ks_map,
                       KapArgs a) {
   using S = KapTileSmem<HD>;
@@ -449,6 +449,13 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
           r1 = fmaxf(r1, x);
         }
       } else {
+        // key-block norms of this half's blocks, loaded up front (blocks past the request read 0)
+        float kbv[64 / KB];
+#pragma unroll
+        for (int gg = 0; gg < 64 / KB; ++gg) {
+          const int j = (c0 + gg * KB) / KB;
+          kbv[gg] = (j < nqb) ? __ldg(kbn + j) : 0.0f;
+        }
 #pragma unroll
         for (int gg = 0; gg < 64 / KB; ++gg) {
           float bm = -INFINITY;
@@ -471,7 +478,7 @@ __global__ void __launch_bounds__(kLogitsThreads, 1)
             // |u - exact| <= kappa * scale * ||q|| * (largest ||k|| of block j) plus the rounding of
             // the scaled logit, of M_r and of the subtraction; expf adds at most 2 ulp; exp(du) - 1 <=
             // 1.02 du for du <= 0.03; a value below exp(-80) is only bounded absolutely
-            const float du = ebase * __ldg(kbn + j) + 1.2e-7f * (2.0f * fabsf(M32) + fabsf(u) + 1.0f);
+            const float du = ebase * kbv[gg] + 1.2e-7f * (2.0f * fabsf(M32) + fabsf(u) + 1.0f);
             const float rel = (du <= 0.03f) ? 1.02f * du : expm1f(du) * 1.01f;
             xe = x * (rel + 3.0e-7f) + ((u < -80.0f) ? 2.0e-35f : 0.0f);
           }
