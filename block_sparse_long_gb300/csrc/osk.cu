@@ -38,7 +38,7 @@ namespace {
 
 constexpr int kThreads = 384;
 constexpr int kSoftmaxThreads = 256;
-constexpr int kWarpK = 8, kWarpMma = 9, kWarpV = 10, kWarpPv = 11;
+constexpr int kWarpK = 8, kWarpMma = 9, kWarpV = 10, kWarpS2 = 11;
 constexpr int kMaxBlocksPerReq = 32768;  // dedupe bitmap capacity (blocks of one request)
 constexpr int kMaxPagesPerBlock = 8;
 constexpr float kRescaleLog2 = 8.0f;     // lazy-rescale threshold, log2 units
@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---------------- set-up (once per CTA) ----------------
   if (threadIdx.x == 0) {
     mbar_init(&sm.q_full, 1);
-    mbar_init(&sm.q_free, 1);
+    mbar_init(&sm.q_free, 2);        // one commit from each S issuer
     for (int s = 0; s < NK; ++s) { mbar_init(&sm.k_full[s], 1); mbar_init(&sm.k_free[s], 1); }
     for (int s = 0; s < NV; ++s) { mbar_init(&sm.v_full[s], 1); mbar_init(&sm.v_free[s], 1); }
     for (int s = 0; s < 2; ++s) {
@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 4; ++s) mbar_init(&sm.p_full[s], 8);
     for (int s = 0; s < 4; ++s) mbar_init(&sm.vreq_full[s], 1);
-    mbar_init(&sm.cleanup, 2);       // one commit from each issuing warp
+    mbar_init(&sm.cleanup, 3);       // one commit from each issuing warp
     sm.abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -305,8 +305,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++v;
         }
       }
-      // end marker of the item
-      if (ok) {
+      // two end markers, one in each S issuer's half of the visit sequence
+      for (int e2 = 0; e2 < 2 && ok; ++e2) {
         const int slot = v % NK;
         if (v >= NK) ok = warp_wait(&sm.k_free[slot], ((v / NK) - 1) & 1, abort_flag, a.status);
         if (ok && lane == 0) {
@@ -325,15 +325,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (issued > 0) wait_parity_bounded(&sm.k_full[s], (issued - 1) & 1, nullptr, nullptr);
       }
     }
-  } else if (warp == kWarpMma) {
-    // =========================== S issuer (lane 0) ===========================
-    // S(v) = Q K_v^T once K(v) has landed and the softmax has read S(v - 2), the buffer it reuses.
+  } else if (warp == kWarpMma || warp == kWarpS2) {
+    // =========================== S issuers (lane 0 of two warps) ===========================
+    // Issuer X takes the visits v with v % 2 == X and owns S buffer X: S(v) = Q K_v^T once K(v)
+    // has landed and the softmax has read S(v - 2).  Two issuing threads keep two products in
+    // flight (one thread issues a product's dependent steps one after another).
     if (lane_id() == 0) {
+      const int X = (warp == kWarpMma) ? 0 : 1;
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, BLK, false, false);
       // descriptors differ from these bases only in the start-address field (address >> 4)
       const uint64_t qdesc = smem_desc_sw128(smem_u32(&sm.q[0]), 16, 1024);
       const uint64_t kdesc = smem_desc_sw128(smem_u32(&sm.k[0][0]), 16, 1024);
-      int vv = 0, n = 0;
+      int vv = X, n = 0;
       bool ok = true;
       for (int idx = blockIdx.x; idx < a.num_items && ok; idx += gridDim.x) {
         const Item it = decode_item(a, idx, BLK);
@@ -342,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++n;
         tc_fence_after();
         while (ok) {
-          const int slot = vv % NK, sb = vv & 1;
+          const int slot = vv % NK, sb = X;
           if (!wait_parity_bounded(&sm.k_full[slot], (vv / NK) & 1, abort_flag, a.status)) { ok = false; break; }
           if (vv >= 2 && !wait_parity_bounded(&sm.s_free[sb], ((vv >> 1) - 1) & 1, abort_flag, a.status)) {
             ok = false;
@@ -355,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // end of the item: no product; the K slot and the S buffer pass on unused
             mbar_arrive(&sm.s_full[sb]);
             mbar_arrive(&sm.k_free[slot]);
-            ++vv;
+            vv += 2;
             break;
           }
           tc_fence_after();
@@ -368,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           umma_commit(&sm.s_full[sb]);
           umma_commit(&sm.k_free[slot]);
-          ++vv;
+          vv += 2;
         }
         // Q may be replaced once this item's products have completed
         if (ok) umma_commit(&sm.q_free);
@@ -378,37 +381,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait_parity_bounded(&sm.cleanup, 0, nullptr, nullptr);
     }
     __syncwarp();
-  } else if (warp == kWarpPv) {
-    // =========================== O issuer (lane 0) ===========================
-    // O += P_c V_c for the c-th computed visit, once P_c is in TMEM and V_c has landed;
-    // the first computed visit of an item overwrites O.
-    if (lane_id() == 0) {
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, HD, false, true);
-      const uint64_t vdesc = smem_desc_sw128(smem_u32(&sm.v[0][0]), S::HALF, 1024);
-      for (int c = 0;; ++c) {
-        if (!wait_parity_bounded(&sm.p_full[c & 3], (c >> 2) & 1, abort_flag, a.status)) break;
-        const int cmd = sm.pv_cmd[c & 3];
-        if (!cmd) break;
-        const int slot = c % NV;
-        if (!wait_parity_bounded(&sm.v_full[slot], (c / NV) & 1, abort_flag, a.status)) break;
-        tc_fence_after();
-        const uint32_t pcol = (c & 1) ? kTmemP1 : kTmemP0;
-        const uint64_t vslot = vdesc + static_cast<uint64_t>(slot * (S::TILE >> 4));
-#pragma unroll
-        for (int kk = 0; kk < BLK / 16; ++kk) {
-          const uint64_t bd = vslot + static_cast<uint64_t>((kk * 16 * 128) >> 4);
-          umma_ts(tmem + kTmemO, tmem + pcol + kk * 8, bd, idesc_pv, (cmd == 1 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(&sm.v_free[slot]);
-        umma_commit(&sm.o_done[c & 1]);
-      }
-      umma_commit(&sm.cleanup);
-      wait_parity_bounded(&sm.cleanup, 0, nullptr, nullptr);
-    }
-    __syncwarp();
   } else if (warp == kWarpV) {
-    // =========================== V producer ===========================
+    // =========================== V loads and O issue ===========================
+    // For the c-th computed visit: load V_c as soon as the vote requests it, then O += P_c V_c once
+    // P_c is in TMEM and V_c has landed (the first computed visit of an item overwrites O).  The
+    // softmax requests V_{c+1} only after it has handed over P_c, so taking the two steps in this
+    // order never waits on a later request.
     const uint32_t lane = lane_id();
+    constexpr uint32_t idesc_pv = idesc_bf16_f32(128, HD, false, true);
+    const uint64_t vdesc = smem_desc_sw128(smem_u32(&sm.v[0][0]), S::HALF, 1024);
     int c = 0;
     bool ok = true;
     while (ok) {
@@ -447,14 +428,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       __syncwarp();
+      if (!warp_wait(&sm.p_full[c & 3], (c >> 2) & 1, abort_flag, a.status)) { ok = false; break; }
+      const int cmd = sm.pv_cmd[c & 3];
+      if (!warp_wait(&sm.v_full[slot], (c / NV) & 1, abort_flag, a.status)) { ok = false; break; }
+      if (lane == 0) {
+        tc_fence_after();
+        const uint32_t pcol = (c & 1) ? kTmemP1 : kTmemP0;
+        const uint64_t vslot = vdesc + static_cast<uint64_t>(slot * (S::TILE >> 4));
+#pragma unroll
+        for (int kk = 0; kk < BLK / 16; ++kk) {
+          const uint64_t bd = vslot + static_cast<uint64_t>((kk * 16 * 128) >> 4);
+          umma_ts(tmem + kTmemO, tmem + pcol + kk * 8, bd, idesc_pv, (cmd == 1 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(&sm.v_free[slot]);
+        umma_commit(&sm.o_done[c & 1]);
+      }
+      __syncwarp();
       ++c;
     }
-    if (*abort_flag && lane == 0) {
-      for (int s = 0; s < NV; ++s) {
-        const int issued = (c - s + NV - 1) / NV;
-        if (issued > 0) wait_parity_bounded(&sm.v_full[s], (issued - 1) & 1, nullptr, nullptr);
+    if (lane == 0) {
+      umma_commit(&sm.cleanup);
+      wait_parity_bounded(&sm.cleanup, 0, nullptr, nullptr);
+      if (*abort_flag) {
+        for (int s2 = 0; s2 < NV; ++s2) {
+          const int issued = (c - s2 + NV - 1) / NV;
+          if (issued > 0) wait_parity_bounded(&sm.v_full[s2], (issued - 1) & 1, nullptr, nullptr);
+        }
       }
     }
+    __syncwarp();
   } else {
     // =========================== softmax warpgroups (warps 0-7) ===========================
     const int g = warp >> 2;              // column half
@@ -538,7 +540,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         // end of the item or a wait that ran out: every softmax warp learns it at the same barrier
         if (named_bar_red_or(1, kSoftmaxThreads, !okw || ki_blk < 0)) {
           if (named_bar_red_or(2, kSoftmaxThreads, !okw)) ok = false;
-          ++v;
+          if (ok) {
+            // the item's second end marker (the other S issuer's): release that buffer too
+            const int v1 = v + 1;
+            bool ok2 = wait_parity_bounded(&sm.s_full[v1 & 1], (v1 >> 1) & 1, abort_flag, a.status);
+            ok2 = __all_sync(0xffffffffu, ok2);
+            if (ok2) {
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&sm.s_free[v1 & 1]);
+            } else {
+              ok = false;
+            }
+          }
+          v += 2;
           break;
         }
         // skip vote (Eq. (5)).  A row wants the block iff m_loc - max(m_run, m_loc) >= tau2; that
