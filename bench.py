@@ -268,11 +268,11 @@ def run_cosa(args, spec, workload_name, delta):
     cpu = None
     if rank == 0 and world >= 1 and not args.no_cpu_baseline:
         cores = os.cpu_count() or 1
-        groups = sample_groups(spec, n_groups=cores, per_group=10, delta=delta)
+        groups = sample_groups(spec, n_groups=cores, per_group=40, delta=delta)
         f, wall, cpu_s = cpu_oracle_run(w, groups, cores)
         cpu = {"value": f / wall / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"{sum(len(g[2]) for g in groups)} (head, query block) items of the {workload_name} "
-                         f"workload ({len(groups)} heads x up to 10 blocks, KAP + OSK each), {wall:.1f} s wall, "
+                         f"workload ({len(groups)} heads x up to 40 blocks, KAP + OSK each), {wall:.1f} s wall, "
                          f"{cpu_s:.1f} s CPU"}
 
     import torch
@@ -433,7 +433,7 @@ def run_cosa(args, spec, workload_name, delta):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", type=int, default=4, help="workload number (1-5); 4 = 128K GQA")
     ap.add_argument("--impl", choices=["cosa", "reference"], default="cosa")
