@@ -93,6 +93,9 @@ def cosa_status_string(code: int) -> str:
     return library().cosa_status_string(int(code)).decode()
 
 
+COSA_FLAG_TEST_STALL = 1   # test hook of cosa_sparse_prefill: every in-kernel wait runs out
+
+
 def make_params(*, num_reqs, num_q_heads, num_kv_heads, head_dim, block_size, page_size, stride=None,
                 total_tokens, max_seqlen, num_pages, max_pages_per_req, mask_pitch, budget_ppm=1_000_000,
                 sm_scale=None, skip_delta=-1.0, flags=0) -> CosaParams:

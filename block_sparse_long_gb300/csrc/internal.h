@@ -39,6 +39,7 @@ struct OskLaunch {
   int num_reqs, num_q_heads, num_kv_heads, head_dim, block_size, page_size;
   int total_tokens, max_seqlen, num_pages, max_pages_per_req, mask_pitch;
   double sm_scale, skip_delta;
+  int flags;             // COSA_FLAG_*
 };
 
 size_t osk_smem_bytes(int block_size, int head_dim);

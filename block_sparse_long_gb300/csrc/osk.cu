@@ -30,6 +30,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "cosa.h"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -91,6 +92,7 @@ struct OskArgs {
   int num_reqs, num_q_heads, num_kv_heads, total_tokens, max_seqlen, nqb_max;
   int page_size, num_pages, max_pages_per_req, mask_pitch;
   int num_items;                      // kv heads * query blocks * requests * query heads per kv head
+  int stall;                          // test hook: the K producer issues nothing (every wait runs out)
   float scale_log2;
   double skip_delta;
 };
@@ -217,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&vmap_pg);
     }
     int v = 0, n = 0;
-    bool ok = true;
+    bool ok = !a.stall;
     for (int idx = blockIdx.x; idx < a.num_items && ok; idx += gridDim.x) {
       const Item it = decode_item(a, idx, BLK);
       if (it.state == 2 && lane == 0) report_status(a.status, kStatusBadInput);
@@ -732,6 +734,7 @@ cudaError_t launch_osk_t(const OskLaunch& L, cudaStream_t stream) {
   a.mask_pitch = L.mask_pitch;
   a.scale_log2 = static_cast<float>(L.sm_scale * 1.4426950408889634);
   a.skip_delta = L.skip_delta;
+  a.stall = (L.flags & COSA_FLAG_TEST_STALL) ? 1 : 0;
   const size_t smem = sizeof(OskSmem<BLK, HD>) + 1024;
   cudaError_t e = cudaFuncSetAttribute(osk_kernel<BLK, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));

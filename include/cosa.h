@@ -72,6 +72,10 @@ extern "C" {
 
 /* cosa_params.flags */
 #define COSA_FLAG_NONE 0
+/* Test hook for the bounded waits (cosa_sparse_prefill only): the producer of K and Q tiles issues
+   nothing, so every wait inside the kernel runs out after its 2 s budget, the kernel stops cleanly and
+   *device_status becomes COSA_ERR_DEVICE_TIMEOUT; out is then undefined.  The CUDA context stays usable. */
+#define COSA_FLAG_TEST_STALL 1
 
 /* values written to visit_flags (one per mask entry) */
 #define COSA_VISIT_COMPUTED 0 /* softmax and P.V accumulated (pattern 3 of the paper's Fig. 4) */

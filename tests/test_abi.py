@@ -85,6 +85,8 @@ def test_host_validation(lib):
     assert osk(_params(lib, head_dim=80)) == lib.COSA_ERR_UNSUPPORTED
     assert osk(_params(lib, sm_scale=0.0)) == lib.COSA_ERR_INVALID_ARG
     assert osk(_params(lib), q=None) == lib.COSA_ERR_INVALID_ARG
+    assert osk(_params(lib, flags=1 << 5)) == lib.COSA_ERR_INVALID_ARG      # unknown flag bit
+    assert kap(_params(lib, flags=1 << 5)) == lib.COSA_ERR_INVALID_ARG
     assert osk(_params(lib, total_tokens=0)) == lib.COSA_OK                 # nothing to do
 
 
