@@ -430,6 +430,70 @@ def run_cosa(args, spec, workload_name, delta):
     return 0
 
 
+def run_sweep(args):
+    """Dense endpoint vs CoSA over context lengths (one JSON line per length, not the bench line).
+
+    For each length N the 128K workload's structure is generated at N tokens; CoSA runs KAP + OSK at
+    B1 = 10 % with Delta = 15000 N / 131072 (the same ln(Delta / N) as the calibrated 128K workload);
+    the dense endpoint runs the same OSK over every causal block in ascending order with skipping off
+    (B1 = 100 %, Delta = -1), i.e. exact causal attention on the same kernel."""
+    import torch
+    from block_sparse_long_gb300 import cosa as C
+    dev = torch.device("cuda", 0)
+
+    def bf(x):
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    def timed(fn, reps):
+        fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    for n_tok in (4096, 8192, 16384, 32768, 65536, 131072):
+        spec = synth.spec_for(4, lengths=(n_tok,), name=f"c4_structure_{n_tok // 1024}k")
+        delta = 15000.0 * n_tok / 131072
+        w = synth.make_workload(spec)
+        q, k, v = bf(w.q), bf(w.k_cache), bf(w.v_cache)
+        pt = torch.from_numpy(w.page_table).to(dev)
+        cu = torch.from_numpy(w.cu_seqlens).to(dev)
+        nqb = -(-n_tok // spec.block_size)
+        pitch = C.stage1_pitch(spec.budget_ppm, spec.max_seqlen, spec.block_size)
+        p = C.params_for(q, k, pt, cu, block_size=spec.block_size, max_seqlen=spec.max_seqlen, stride=spec.stride,
+                         budget_ppm=spec.budget_ppm, mask_pitch=pitch, skip_delta=delta)
+        mask = torch.empty((1, spec.num_q_heads, nqb, pitch), dtype=torch.int32, device=dev)
+        mask_len = torch.empty((1, spec.num_q_heads, nqb), dtype=torch.int32, device=dev)
+        ws = torch.empty(C.cosa_proxy_workspace_size(p), dtype=torch.uint8, device=dev)
+        out = torch.empty_like(q)
+        kap_ms = timed(lambda: C.cosa_proxy_select(p, q, cu, k, pt, mask=mask, mask_len=mask_len, workspace=ws), 10)
+        osk_ms = timed(lambda: C.cosa_sparse_prefill(p, q, cu, k, v, pt, mask, mask_len, out=out), 10)
+        # dense endpoint: every causal block, ascending, skipping off
+        ar = torch.arange(nqb, dtype=torch.int32, device=dev)
+        dmask = torch.where(ar[None, :] <= ar[:, None], ar[None, :], torch.full_like(ar[None, :], -1))
+        dmask = dmask.expand(spec.num_q_heads, nqb, nqb).reshape(1, spec.num_q_heads, nqb, nqb).contiguous()
+        dlen = (ar + 1).expand(spec.num_q_heads, nqb).reshape(1, spec.num_q_heads, nqb).contiguous()
+        pd = C.params_for(q, k, pt, cu, block_size=spec.block_size, max_seqlen=spec.max_seqlen, stride=spec.stride,
+                          budget_ppm=1_000_000, mask_pitch=nqb, skip_delta=-1.0)
+        dense_ms = timed(lambda: C.cosa_sparse_prefill(pd, q, cu, k, v, pt, dmask, dlen, out=out), 5)
+        causal_pairs = spec.num_q_heads * nqb * (nqb + 1) // 2
+        dense_tflops = 4.0 * spec.block_size * spec.block_size * spec.head_dim * causal_pairs / (dense_ms * 1e-3) / 1e12
+        print(json.dumps({"sweep": "cosa_vs_dense_endpoint", "tokens": n_tok, "workload": spec.name,
+                          "skip_delta": delta, "stage1_budget": spec.budget_ppm / 1e6,
+                          "cosa_ms": kap_ms + osk_ms, "kap_ms": kap_ms, "osk_ms": osk_ms, "dense_ms": dense_ms,
+                          "dense_tflops": dense_tflops, "speedup_vs_dense": dense_ms / (kap_ms + osk_ms)}),
+              flush=True)
+        del q, k, v, mask, ws, out, dmask
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -438,7 +502,11 @@ def main():
     ap.add_argument("--workload", type=int, default=4, help="workload number (1-5); 4 = 128K GQA")
     ap.add_argument("--impl", choices=["cosa", "reference"], default="cosa")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time CoSA against the dense endpoint of the same kernel from 4K to 128K tokens")
     args = ap.parse_args()
+    if args.sweep:
+        return run_sweep(args)
     spec = synth.spec_for(args.workload)
     delta = delta_for(args.workload) if args.workload != 1 else 2000.0
     name = spec.name
