@@ -680,7 +680,7 @@ __global__ void __launch_bounds__(256) kap_rescan_kernel(KapArgs a) {
 // dynamic shared memory of kap_select for `cap` candidates (a power of two)
 constexpr int kRepChunk = 64;            // repaired positions per round of the float64 repair
 __host__ __device__ inline size_t select_smem_bytes(int cap) {
-  return static_cast<size_t>(cap) * (8 + 4 + 4 + 4 + 4 + 8 + 1) + 64 + kRepChunk * 16 * sizeof(double) + 64;
+  return static_cast<size_t>(cap) * (8 + 4 + 4 + 4 + 4 + 8 + 1 + 1) + 64 + kRepChunk * 16 * sizeof(double) + 64;
 }
 
 __device__ __forceinline__ unsigned long long sort_key(bool hrm, float s, int j) {
@@ -767,8 +767,105 @@ __device__ void sort_block_keys(unsigned long long* key, const uint8_t* hrm, con
   sort_keys_desc<E>(v, key, N);
 }
 
+constexpr int kTopFast = 128;             // budgets up to this many blocks take the top-K path
+
+// Shared state of the top-K selection.
+struct TopkShared {
+  uint32_t hist[256];
+  int digit, above, count;
+  int hi_out[2];                          // float bits of the largest upper bound of the unselected
+                                          // keys of each group ([0] rest, [1] HRM); scores are >= 0
+  int warp_cnt[kSelectThreads / 32];
+};
+
+// The K largest of the J keys (distinct) into key[0..K), sorted descending, key[K..256) = 0; the largest
+// upper bound (score + error) of the unselected keys of each group into sh.hi_out.  Radix select on
+// 8-bit digits from the top finds the K-th key; the winners are compacted and sorted.
+template <int E>
+__device__ void select_top_keys(unsigned long long* key, const uint8_t* hrm, const float* score,
+                                const float* serr, int J, int K, TopkShared& sh) {
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  unsigned long long v[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int j = tid * E + e;
+    v[e] = (j < J) ? sort_key(hrm[j] != 0, fmaxf(score[j], 0.0f), j) : 0ull;
+  }
+  unsigned long long prefix = 0ull, pmask = 0ull;
+  int krem = K;   // rank (from the top, 1-based) of the K-th key among the keys matching the prefix
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    __syncthreads();
+    for (int d = tid; d < 256; d += blockDim.x) sh.hist[d] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+      if (tid * E + e < J && (v[e] & pmask) == prefix) atomicAdd(&sh.hist[(v[e] >> shift) & 255u], 1u);
+    __syncthreads();
+    if (w == 0) {
+      // lane l holds digits 255 - 8l .. 248 - 8l (highest first)
+      int cq[8], sum = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) { cq[q] = static_cast<int>(sh.hist[255 - 8 * lane - q]); sum += cq[q]; }
+      int incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      int run = incl - sum;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (run < krem && run + cq[q] >= krem) { sh.digit = 255 - 8 * lane - q; sh.above = run; sh.count = cq[q]; }
+        run += cq[q];
+      }
+    }
+    __syncthreads();
+    const int d = sh.digit;
+    krem -= sh.above;
+    prefix |= static_cast<unsigned long long>(d) << shift;
+    pmask |= 0xFFull << shift;
+    if (sh.count == krem) break;   // every key with this prefix is among the K
+  }
+  // a key is selected iff its masked top bits are at least the prefix: exactly K keys
+  int cnt = 0;
+#pragma unroll
+  for (int e = 0; e < E; ++e) cnt += (tid * E + e < J && (v[e] & pmask) >= prefix) ? 1 : 0;
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) sh.warp_cnt[w] = incl;
+  if (tid < 2) sh.hi_out[tid] = __float_as_int(-INFINITY);
+  key[tid] = 0ull;   // kSelectThreads slots
+  __syncthreads();
+  int pos = incl - cnt;
+  for (int q = 0; q < w; ++q) pos += sh.warp_cnt[q];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int j = tid * E + e;
+    if (j >= J) continue;
+    if ((v[e] & pmask) >= prefix) {
+      key[pos++] = v[e];
+    } else {
+      const float hv = fmaxf(score[j], 0.0f) + serr[j];
+      atomicMax(&sh.hi_out[hrm[j] != 0 ? 1 : 0], __float_as_int(hv));
+    }
+  }
+  __syncthreads();
+  unsigned long long s1[1] = {key[tid]};
+  sort_keys_desc<1>(s1, key, kSelectThreads);
+}
+
+template <int E>
+__device__ void select_top_dispatch(unsigned long long* key, const uint8_t* hrm, const float* score,
+                                    const float* serr, int J, int K, TopkShared& sh) {
+  select_top_keys<E>(key, hrm, score, serr, J, K, sh);
+}
+
 template <int HD, int KB>
-__global__ void __launch_bounds__(kSelectThreads) kap_select_kernel(KapArgs a, int cap) {
+__global__ void __launch_bounds__(kSelectThreads, 3) kap_select_kernel(KapArgs a, int cap) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   unsigned long long* key = reinterpret_cast<unsigned long long*>(smem_raw);  // [cap] sort keys
   double* rep_val = reinterpret_cast<double*>(key + cap);                      // [cap] exact scores
@@ -778,8 +875,10 @@ __global__ void __launch_bounds__(kSelectThreads) kap_select_kernel(KapArgs a, i
   int32_t* rep_pos = reinterpret_cast<int32_t*>(suf + cap);                    // [cap] positions to repair
   uint8_t* hrm = reinterpret_cast<uint8_t*>(rep_pos + cap);                    // [cap] HRM flags
   double* terms = reinterpret_cast<double*>(
-      (reinterpret_cast<uintptr_t>(hrm + cap) + 15) & ~uintptr_t(15));         // [kRepChunk * KB] row terms
-  __shared__ int32_t n_rep_s, n_hrm_s, cstar_s[2], warp_cnt_s[kSelectThreads / 32];
+      (reinterpret_cast<uintptr_t>(hrm + 2 * cap) + 15) & ~uintptr_t(15));     // [kRepChunk * KB] row terms
+  uint8_t* cutf = hrm + cap;                                                   // [cap] certain-cut flags
+  __shared__ int32_t n_rep_s, n_hrm_s, cstar_s[2], warp_cnt_s[kSelectThreads / 32], sentinel_marked_s;
+  __shared__ TopkShared topk;
 
   const int tid = threadIdx.x;
   int idx = blockIdx.x;
@@ -818,122 +917,161 @@ __global__ void __launch_bounds__(kSelectThreads) kap_select_kernel(KapArgs a, i
     }
   }
   __syncthreads();
-  // sort keys (bitonic, descending) over N = max(next power of two, threads) positions
-  int n2 = 1;
-  while (n2 < J) n2 <<= 1;
-  const int N = n2 < kSelectThreads ? kSelectThreads : n2;
-  if (tid == 0) {
-    n_hrm_s = 0;
-    cstar_s[0] = cstar_s[1] = 0x7fffffff;
-  }
+  if (tid == 0) n_hrm_s = 0;
   {
     int cnt = 0;
     for (int j = tid; j < J; j += blockDim.x) cnt += hrm[j] != 0;
     __syncthreads();
     if (cnt) atomicAdd(&n_hrm_s, cnt);
   }
-  {
-    const float* sc = a.score + sbase;
-    switch (N / kSelectThreads) {
-      case 1: sort_block_keys<1>(key, hrm, sc, J, N); break;
-      case 2: sort_block_keys<2>(key, hrm, sc, J, N); break;
-      case 4: sort_block_keys<4>(key, hrm, sc, J, N); break;
-      case 8: sort_block_keys<8>(key, hrm, sc, J, N); break;
-      default: sort_block_keys<16>(key, hrm, sc, J, N); break;
-    }
-  }
-  const int nh = n_hrm_s;   // HRM keys sort first
-  // score intervals per sorted position
-  for (int p = tid; p < n2; p += blockDim.x) {
-    if (p < J) {
-      const int j = key_block(key[p]);
-      const float s = fmaxf(a.score[sbase + j], 0.0f);
-      const float e = a.score_err[sbase + j];
-      lo[p] = s - e;
-      hi[p] = s + e;
-    } else {
-      lo[p] = -INFINITY;
-      hi[p] = -INFINITY;
-    }
-  }
   __syncthreads();
-  // within each group (HRM positions [0, nh), the rest [nh, J)): suffix maximum of hi and prefix
-  // minimum of lo (Hillis-Steele, log2(n2) rounds); lo is overwritten by its prefix minimum
-  for (int p = tid; p < n2; p += blockDim.x) suf[p] = hi[p];
-  __syncthreads();
-  for (int off = 1; off < n2; off <<= 1) {
-    float ts[16], tp[16];
-    int cnt = 0;
-    for (int p = tid; p < n2; p += blockDim.x, ++cnt) {
-      const int q = p + off, r = p - off;
-      const bool sq = q < n2 && ((p < nh) == (q < nh));
-      const bool sr = r >= 0 && ((p < nh) == (r < nh));
-      ts[cnt & 15] = sq ? fmaxf(suf[p], suf[q]) : suf[p];
-      tp[cnt & 15] = sr ? fminf(lo[p], lo[r]) : lo[p];
-    }
-    __syncthreads();
-    cnt = 0;
-    for (int p = tid; p < n2; p += blockDim.x, ++cnt) {
-      suf[p] = ts[cnt & 15];
-      lo[p] = tp[cnt & 15];
-    }
-    __syncthreads();
-  }
-  // Clusters of positions whose relative order, or side of the budget cut, the bounds cannot
-  // certify.  The cut after position q is certain iff every element up to q (in its group)
-  // stays above every later one: min lo[g0..q] > max hi[q+1..g1).  (Cuts certified for the
-  // elements of q's own run suffice: an earlier certain cut already puts all elements before
-  // it above everything after it.)  Runs of two or more positions between certain cuts are
-  // repaired when they start before K.  hrm[] is reused for the cut flags.
-  uint8_t* cutf = hrm;
-  for (int p = tid; p < J; p += blockDim.x) {
-    const int g1 = p < nh ? nh : J;
-    cutf[p] = (p == g1 - 1) || (lo[p] > suf[p + 1]);
-  }
-  __syncthreads();
-  for (int p = tid; p < J; p += blockDim.x) {
-    const int g = p < nh ? 0 : 1;
-    const int g1 = g ? J : nh;
-    const int kg = min(K, g1);
-    if (p >= kg - 1 && cutf[p]) atomicMin(&cstar_s[g], p);
-  }
-  __syncthreads();
-  {
-    // each thread marks positions tid*E .. tid*E+E-1 in order; a block scan places them
-    const int E = N / kSelectThreads;
-    int cnt = 0;
-    uint32_t bits = 0;
-    for (int e = 0; e < E; ++e) {
-      const int x = tid * E + e;
-      if (x >= J) break;
-      const int g = x < nh ? 0 : 1;
-      const int g0 = g ? nh : 0, g1 = g ? J : nh;
-      const int kg = min(K, g1);
-      bool mk = false;
-      if (kg > g0) {
-        const bool multi = !cutf[x] || (x > g0 && !cutf[x - 1]);
-        mk = multi && (x < kg || x <= cstar_s[g]);
+  const int nh_all = n_hrm_s;   // HRM keys sort first
+  const float* sc = a.score + sbase;
+  const float* se = a.score_err + sbase;
+  // Ordered list the certification runs on: either all J keys sorted (full path), or the K selected
+  // keys sorted plus one sentinel at position K that stands for every unselected key of its group
+  // (its upper bound is theirs, largest; it is never a candidate).  If the budget cut cannot be
+  // certified against the sentinel, the full path runs instead.
+  int Jl = J, nh = nh_all, n2 = 1, Nl = kSelectThreads;
+  bool sentinel = false;
+  float sentinel_hi = -INFINITY;
+  for (int attempt = (K <= kTopFast && K < J) ? 0 : 1; attempt < 2; ++attempt) {
+    int N2 = 1;
+    while (N2 < J) N2 <<= 1;
+    const int N = N2 < kSelectThreads ? kSelectThreads : N2;
+    if (attempt == 0) {
+      switch (N / kSelectThreads) {
+        case 1: select_top_dispatch<1>(key, hrm, sc, se, J, K, topk); break;
+        case 2: select_top_dispatch<2>(key, hrm, sc, se, J, K, topk); break;
+        case 4: select_top_dispatch<4>(key, hrm, sc, se, J, K, topk); break;
+        case 8: select_top_dispatch<8>(key, hrm, sc, se, J, K, topk); break;
+        default: select_top_dispatch<16>(key, hrm, sc, se, J, K, topk); break;
       }
-      if (mk) { bits |= 1u << e; ++cnt; }
+      sentinel = true;
+      Jl = K + 1;
+      nh = (nh_all > K) ? K + 1 : nh_all;   // the sentinel joins the HRM group iff HRM keys were left out
+      sentinel_hi = __int_as_float(topk.hi_out[(nh_all > K) ? 1 : 0]);
+      Nl = kSelectThreads;
+    } else {
+      switch (N / kSelectThreads) {
+        case 1: sort_block_keys<1>(key, hrm, sc, J, N); break;
+        case 2: sort_block_keys<2>(key, hrm, sc, J, N); break;
+        case 4: sort_block_keys<4>(key, hrm, sc, J, N); break;
+        case 8: sort_block_keys<8>(key, hrm, sc, J, N); break;
+        default: sort_block_keys<16>(key, hrm, sc, J, N); break;
+      }
+      sentinel = false;
+      Jl = J;
+      nh = nh_all;
+      Nl = N;
     }
-    const int lane = tid & 31, w = tid >> 5;
-    int incl = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
+    n2 = 1;
+    while (n2 < Jl) n2 <<= 1;
+    if (tid == 0) {
+      cstar_s[0] = cstar_s[1] = 0x7fffffff;
+      sentinel_marked_s = 0;
     }
-    if (lane == 31) warp_cnt_s[w] = incl;
+    // score intervals per listed position
+    for (int p = tid; p < n2; p += blockDim.x) {
+      if (sentinel && p == K) {
+        lo[p] = -INFINITY;
+        hi[p] = sentinel_hi;
+      } else if (p < Jl) {
+        const int j = key_block(key[p]);
+        const float s = fmaxf(sc[j], 0.0f);
+        const float e = se[j];
+        lo[p] = s - e;
+        hi[p] = s + e;
+      } else {
+        lo[p] = -INFINITY;
+        hi[p] = -INFINITY;
+      }
+    }
     __syncthreads();
-    int base = 0, total = 0;
-    for (int q = 0; q < kSelectThreads / 32; ++q) {
-      if (q < w) base += warp_cnt_s[q];
-      total += warp_cnt_s[q];
+    // within each group (HRM positions [0, nh), the rest [nh, Jl)): suffix maximum of hi and prefix
+    // minimum of lo (Hillis-Steele, log2(n2) rounds); lo is overwritten by its prefix minimum
+    for (int p = tid; p < n2; p += blockDim.x) suf[p] = hi[p];
+    __syncthreads();
+    for (int off = 1; off < n2; off <<= 1) {
+      float ts[16], tp[16];
+      int cnt = 0;
+      for (int p = tid; p < n2; p += blockDim.x, ++cnt) {
+        const int q = p + off, r = p - off;
+        const bool sq = q < n2 && ((p < nh) == (q < nh));
+        const bool sr = r >= 0 && ((p < nh) == (r < nh));
+        ts[cnt & 15] = sq ? fmaxf(suf[p], suf[q]) : suf[p];
+        tp[cnt & 15] = sr ? fminf(lo[p], lo[r]) : lo[p];
+      }
+      __syncthreads();
+      cnt = 0;
+      for (int p = tid; p < n2; p += blockDim.x, ++cnt) {
+        suf[p] = ts[cnt & 15];
+        lo[p] = tp[cnt & 15];
+      }
+      __syncthreads();
     }
-    int pos = base + incl - cnt;
-    for (int e = 0; e < E; ++e)
-      if ((bits >> e) & 1u) rep_pos[pos++] = tid * E + e;
-    if (tid == 0) n_rep_s = total;
+    // Clusters of positions whose relative order, or side of the budget cut, the bounds cannot
+    // certify.  The cut after position q is certain iff every element up to q (in its group)
+    // stays above every later one: min lo[g0..q] > max hi[q+1..g1).  (Cuts certified for the
+    // elements of q's own run suffice: an earlier certain cut already puts all elements before
+    // it above everything after it.)  Runs of two or more positions between certain cuts are
+    // repaired when they start before K.
+    for (int p = tid; p < Jl; p += blockDim.x) {
+      const int g1 = p < nh ? nh : Jl;
+      cutf[p] = (p == g1 - 1) || (lo[p] > suf[p + 1]);
+    }
+    __syncthreads();
+    for (int p = tid; p < Jl; p += blockDim.x) {
+      const int g = p < nh ? 0 : 1;
+      const int g1 = g ? Jl : nh;
+      const int kg = min(K, g1);
+      if (p >= kg - 1 && cutf[p]) atomicMin(&cstar_s[g], p);
+    }
+    __syncthreads();
+    {
+      // each thread marks positions tid*E .. tid*E+E-1 in order; a block scan places them
+      const int E = Nl / kSelectThreads;
+      int cnt = 0;
+      uint32_t bits = 0;
+      for (int e = 0; e < E; ++e) {
+        const int x = tid * E + e;
+        if (x >= Jl) break;
+        const int g = x < nh ? 0 : 1;
+        const int g0 = g ? nh : 0, g1 = g ? Jl : nh;
+        const int kg = min(K, g1);
+        bool mk = false;
+        if (kg > g0) {
+          const bool multi = !cutf[x] || (x > g0 && !cutf[x - 1]);
+          mk = multi && (x < kg || x <= cstar_s[g]);
+        }
+        if (mk) {
+          bits |= 1u << e;
+          ++cnt;
+          if (sentinel && x == K) sentinel_marked_s = 1;
+        }
+      }
+      const int lane = tid & 31, w = tid >> 5;
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (lane == 31) warp_cnt_s[w] = incl;
+      __syncthreads();
+      int base = 0, total = 0;
+      for (int q = 0; q < kSelectThreads / 32; ++q) {
+        if (q < w) base += warp_cnt_s[q];
+        total += warp_cnt_s[q];
+      }
+      int pos = base + incl - cnt;
+      for (int e = 0; e < E; ++e)
+        if ((bits >> e) & 1u) rep_pos[pos++] = tid * E + e;
+      if (tid == 0) n_rep_s = total;
+    }
+    __syncthreads();
+    if (!sentinel_marked_s) break;   // certified (or the full path): done
+    __syncthreads();
   }
   __syncthreads();
   const int n_rep = n_rep_s;
