@@ -151,13 +151,16 @@ __device__ __forceinline__ float warp_dot_f32(const uint16_t* x, const uint16_t*
 }
 
 template <int HD>
+// Products of two bf16 values are exact in fp32 (8-bit significands), so each float64 step below,
+// acc + (double)(x * y), rounds exactly like fma((double)x, (double)y, acc) with one float64
+// conversion instead of two.
 __device__ __forceinline__ double warp_dot_f64(const uint16_t* x, const uint16_t* y) {
   constexpr int PER = HD / 32;
   const int l = threadIdx.x & 31;
   double acc = 0.0;
 #pragma unroll
   for (int e = 0; e < PER; ++e)
-    acc = fma(static_cast<double>(bf16_to_f32(x[l * PER + e])), static_cast<double>(bf16_to_f32(y[l * PER + e])), acc);
+    acc += static_cast<double>(bf16_to_f32(x[l * PER + e]) * bf16_to_f32(y[l * PER + e]));   // exact fp32 product
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
   return acc;
@@ -622,7 +625,7 @@ __global__ void __launch_bounds__(256) kap_rescan_kernel(KapArgs a) {
         float kf[8];
         load8_bf16(kr + e, kf);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) dacc = fma(static_cast<double>(qf[e + i]), static_cast<double>(kf[i]), dacc);
+        for (int i = 0; i < 8; ++i) dacc += static_cast<double>(qf[e + i] * kf[i]);
       }
       const double lx = dacc * a.sm_scale;
       best = fmax(best, lx);
@@ -661,7 +664,7 @@ __global__ void __launch_bounds__(256) kap_rescan_kernel(KapArgs a) {
         for (int e = 0; e < HD; e += 8) {
           float kf[8];
           load8_bf16(kr + e, kf);
-          for (int i = 0; i < 8; ++i) dacc = fma(static_cast<double>(qf[e + i]), static_cast<double>(kf[i]), dacc);
+          for (int i = 0; i < 8; ++i) dacc += static_cast<double>(qf[e + i] * kf[i]);
         }
         if (dacc * a.sm_scale == M) {
           const int j = (c * a.stride) / a.block_size;
@@ -1136,9 +1139,8 @@ __global__ void __launch_bounds__(kSelectThreads, 3) kap_select_kernel(KapArgs a
               for (int e = lane * (HD / 32); e < (lane + 1) * (HD / 32); e += 2) {
                 const uint32_t qw = *reinterpret_cast<const uint32_t*>(qrow + e);
                 const uint32_t kw = *reinterpret_cast<const uint32_t*>(krow + e);
-                dp = fma(static_cast<double>(__uint_as_float(qw << 16)), static_cast<double>(__uint_as_float(kw << 16)), dp);
-                dp = fma(static_cast<double>(__uint_as_float(qw & 0xffff0000u)),
-                         static_cast<double>(__uint_as_float(kw & 0xffff0000u)), dp);
+                dp += static_cast<double>(__uint_as_float(qw << 16) * __uint_as_float(kw << 16));
+                dp += static_cast<double>(__uint_as_float(qw & 0xffff0000u) * __uint_as_float(kw & 0xffff0000u));
               }
 #pragma unroll
               for (int o = 16; o > 0; o >>= 1) dp += __shfl_xor_sync(0xffffffffu, dp, o);
