@@ -414,7 +414,7 @@ def run_cosa(args, spec, workload_name, delta):
         "dense_equiv_tflops": dense_equiv_flops(spec) / (osk_avg * 1e-3) / 1e12,
         "visits": visited, "computed": computed, "realized_stage1": visited / causal,
         "realized_stage2": computed / causal,
-        "roofline": {"bound": "tensor", "kernel": "osk_kernel<128,128>", "achieved": achieved, "peak": peak,
+        "roofline": {"bound": "tensor", "kernel": "osk_kernel<128,128,false>", "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"bf16_tflops ({pk_src}, burst)"},
         "e2e": {"value": world * step_flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
@@ -494,6 +494,123 @@ def run_sweep(args):
     return 0
 
 
+def run_ablation(args):
+    """Kernel-side ablations on synthetic data (one JSON line per point, not the bench line).
+
+    remap: in-kernel skip ratio and OSK time against Delta, visiting in the computation order of
+      Eq. (14) (with KV page remapping) or in ascending block order (without), for stage-1 budgets
+      B1 in {100, 54, 42, 32, 28} %: the kernel-side analogue of CoSA Fig. 6 and Fig. C.  Skip ratio =
+      skipped / visited blocks; budget = computed blocks / causal candidate blocks.
+    jump: OSK time with skipping off (Delta = -1) at budgets {25, 50, 75} % and 32K-128K tokens for the
+      same selected blocks visited (a) as an ascending ID list (physical jumps), (b) through the binary
+      mask with logical skipping of the unselected blocks (BSA-style loop), (c) in the computation
+      order; each against the dense endpoint of the same kernel: the analogue of CoSA Fig. B.
+    Inputs have the 128K workload's structure at the given length."""
+    import torch
+    from block_sparse_long_gb300 import cosa as C
+    dev = torch.device("cuda", 0)
+
+    def bf(x):
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    def timed(fn, reps):
+        fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    def setup(n_tok):
+        spec = synth.spec_for(4, lengths=(n_tok,), name=f"c4_structure_{n_tok // 1024}k")
+        w = synth.make_workload(spec)
+        t = dict(q=bf(w.q), k=bf(w.k_cache), v=bf(w.v_cache), pt=torch.from_numpy(w.page_table).to(dev),
+                 cu=torch.from_numpy(w.cu_seqlens).to(dev))
+        return spec, t
+
+    def params(spec, t, ppm, pitch, delta, flags=0):
+        return C.params_for(t["q"], t["k"], t["pt"], t["cu"], block_size=spec.block_size, max_seqlen=spec.max_seqlen,
+                            stride=spec.stride, budget_ppm=ppm, mask_pitch=pitch, skip_delta=delta, flags=flags)
+
+    def kap(spec, t, ppm, flags):
+        nqb = -(-spec.max_seqlen // spec.block_size)
+        pitch = C.stage1_pitch(ppm, spec.max_seqlen, spec.block_size)
+        p = params(spec, t, ppm, pitch, -1.0, flags)
+        mask = torch.empty((1, spec.num_q_heads, nqb, pitch), dtype=torch.int32, device=dev)
+        ml = torch.empty((1, spec.num_q_heads, nqb), dtype=torch.int32, device=dev)
+        C.cosa_proxy_select(p, t["q"], t["cu"], t["k"], t["pt"], mask=mask, mask_len=ml)
+        return mask, ml, pitch
+
+    def binary(spec, ids, ml):
+        nqb = ids.shape[2]
+        ar = torch.arange(ids.shape[3], device=dev)
+        live = ar[None, None, None, :] < ml[..., None]
+        m01 = torch.zeros((1, spec.num_q_heads, nqb, nqb + 1), dtype=torch.int32, device=dev)
+        m01.scatter_(3, torch.where(live, ids, nqb).long(), 1)
+        l01 = torch.where(ml > 0, torch.arange(1, nqb + 1, dtype=torch.int32, device=dev)[None, None, :], 0)
+        return m01[..., :nqb].contiguous(), l01.to(torch.int32).contiguous()
+
+    out_lines = []
+    if args.ablation == "remap":
+        n_tok = args.ablation_tokens
+        spec, t = setup(n_tok)
+        out = torch.empty_like(t["q"])
+        for ppm in (1_000_000, 540_000, 420_000, 320_000, 280_000):
+            masks = {"remap": kap(spec, t, ppm, 0), "ascending": kap(spec, t, ppm, C.COSA_FLAG_ASCENDING_ORDER)}
+            nqb = masks["remap"][0].shape[2]
+            cand = spec.num_q_heads * nqb * (nqb + 1) // 2
+            for delta in (-1.0, 250.0, 500.0, 1000.0, 2000.0, 3000.0, 5000.0, 10000.0, 15000.0, 30000.0):
+                rec = {"ablation": "remap", "workload": spec.name, "tokens": n_tok, "stage1_budget": ppm / 1e6,
+                       "skip_delta": delta}
+                for mode, (mask, ml, pitch) in masks.items():
+                    p = params(spec, t, ppm, pitch, delta)
+                    flags = torch.empty(mask.shape, dtype=torch.uint8, device=dev)
+                    ms = timed(lambda: C.cosa_sparse_prefill(p, t["q"], t["cu"], t["k"], t["v"], t["pt"], mask, ml,
+                                                             out=out, visit_flags=flags), 3)
+                    computed = int((flags == C.VISIT_COMPUTED).sum())
+                    skipped = int((flags == C.VISIT_SKIPPED).sum())
+                    rec[f"{mode}_skip_ratio"] = skipped / max(1, computed + skipped)
+                    rec[f"{mode}_budget"] = computed / cand
+                    rec[f"{mode}_osk_ms"] = ms
+                print(json.dumps(rec), flush=True)
+            del masks
+            torch.cuda.empty_cache()
+    else:
+        for n_tok in (32768, 65536, 131072):
+            spec, t = setup(n_tok)
+            out = torch.empty_like(t["q"])
+            nqb = -(-n_tok // spec.block_size)
+            full, fl, fpitch = kap(spec, t, 1_000_000, C.COSA_FLAG_ASCENDING_ORDER)
+            dense_ms = timed(lambda: C.cosa_sparse_prefill(params(spec, t, 1_000_000, fpitch, -1.0), t["q"], t["cu"],
+                                                           t["k"], t["v"], t["pt"], full, fl, out=out), 3)
+            for ppm in (250_000, 500_000, 750_000):
+                ids, ml, pitch = kap(spec, t, ppm, C.COSA_FLAG_ASCENDING_ORDER)
+                rho, rl, _ = kap(spec, t, ppm, 0)
+                m01, l01 = binary(spec, ids, ml)
+                p = params(spec, t, ppm, pitch, -1.0)
+                pb = params(spec, t, ppm, nqb, -1.0, C.COSA_FLAG_BINARY_MASK)
+                jump_ms = timed(lambda: C.cosa_sparse_prefill(p, t["q"], t["cu"], t["k"], t["v"], t["pt"], ids, ml,
+                                                              out=out), 5)
+                logical_ms = timed(lambda: C.cosa_sparse_prefill(pb, t["q"], t["cu"], t["k"], t["v"], t["pt"], m01,
+                                                                 l01, out=out), 5)
+                order_ms = timed(lambda: C.cosa_sparse_prefill(p, t["q"], t["cu"], t["k"], t["v"], t["pt"], rho, rl,
+                                                               out=out), 5)
+                print(json.dumps({"ablation": "jump", "workload": spec.name, "tokens": n_tok, "budget": ppm / 1e6,
+                                  "dense_ms": dense_ms, "jump_ascending_ms": jump_ms,
+                                  "logical_binary_ms": logical_ms, "jump_rho_order_ms": order_ms,
+                                  "speedup_jump": dense_ms / jump_ms, "speedup_logical": dense_ms / logical_ms}),
+                      flush=True)
+                del ids, rho, m01
+            del t, full
+            torch.cuda.empty_cache()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -504,9 +621,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true",
                     help="time CoSA against the dense endpoint of the same kernel from 4K to 128K tokens")
+    ap.add_argument("--ablation", choices=["remap", "jump"],
+                    help="remap: skip ratio vs Delta with and without remapping over stage-1 budgets; "
+                         "jump: physical jumps vs logical skipping of a binary mask")
+    ap.add_argument("--ablation-tokens", type=int, default=131072, help="context length of --ablation remap")
     args = ap.parse_args()
     if args.sweep:
         return run_sweep(args)
+    if args.ablation:
+        return run_ablation(args)
     spec = synth.spec_for(args.workload)
     delta = delta_for(args.workload) if args.workload != 1 else 2000.0
     name = spec.name

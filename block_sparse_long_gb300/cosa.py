@@ -94,6 +94,8 @@ def cosa_status_string(code: int) -> str:
 
 
 COSA_FLAG_TEST_STALL = 1   # test hook of cosa_sparse_prefill: every in-kernel wait runs out
+COSA_FLAG_ASCENDING_ORDER = 2   # cosa_proxy_select writes the selected blocks in ascending order
+COSA_FLAG_BINARY_MASK = 4       # cosa_sparse_prefill reads mask rows as binary block masks
 
 
 def make_params(*, num_reqs, num_q_heads, num_kv_heads, head_dim, block_size, page_size, stride=None,
@@ -143,7 +145,7 @@ def _check(t: torch.Tensor, name: str, dtype: torch.dtype):
 def params_for(q: torch.Tensor, k_cache: torch.Tensor, page_table: torch.Tensor, cu_seqlens: torch.Tensor, *,
                block_size: int, max_seqlen: int, stride: Optional[int] = None, budget_ppm: int = 1_000_000,
                mask_pitch: Optional[int] = None, skip_delta: float = -1.0,
-               sm_scale: Optional[float] = None) -> CosaParams:
+               sm_scale: Optional[float] = None, flags: int = 0) -> CosaParams:
     T, Hq, d = q.shape
     num_pages, P, Hkv, d2 = k_cache.shape
     assert d == d2
@@ -153,7 +155,7 @@ def params_for(q: torch.Tensor, k_cache: torch.Tensor, page_table: torch.Tensor,
     return make_params(num_reqs=B, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d, block_size=block_size,
                        page_size=P, stride=stride, total_tokens=T, max_seqlen=max_seqlen, num_pages=num_pages,
                        max_pages_per_req=page_table.shape[1], mask_pitch=mask_pitch, budget_ppm=budget_ppm,
-                       sm_scale=sm_scale, skip_delta=skip_delta)
+                       sm_scale=sm_scale, skip_delta=skip_delta, flags=flags)
 
 
 def cosa_proxy_select(p: CosaParams, q: torch.Tensor, cu_seqlens: torch.Tensor, k_cache: torch.Tensor,

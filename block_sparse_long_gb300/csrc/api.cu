@@ -46,7 +46,8 @@ int check_common(const cosa_params* p) {
   if (p->total_tokens < 0 || p->max_seqlen < 1 || p->num_pages < 1 || p->max_pages_per_req < 1) return COSA_ERR_INVALID_ARG;
   if (p->mask_pitch < 1) return COSA_ERR_INVALID_ARG;
   if (!(p->sm_scale > 0.0) || !std::isfinite(p->sm_scale) || std::isnan(p->skip_delta)) return COSA_ERR_INVALID_ARG;
-  if ((p->flags & ~COSA_FLAG_TEST_STALL) != 0) return COSA_ERR_INVALID_ARG;
+  if ((p->flags & ~(COSA_FLAG_TEST_STALL | COSA_FLAG_ASCENDING_ORDER | COSA_FLAG_BINARY_MASK)) != 0)
+    return COSA_ERR_INVALID_ARG;
   if (p->head_dim != 64 && p->head_dim != 128) return COSA_ERR_UNSUPPORTED;
   if (p->block_size != 64 && p->block_size != 128) return COSA_ERR_UNSUPPORTED;
   if (p->page_size != 16 && p->page_size != 32 && p->page_size != 64 && p->page_size != 128) return COSA_ERR_UNSUPPORTED;
@@ -140,6 +141,7 @@ int cosa_proxy_select(const cosa_params* p, const void* q, const int32_t* cu_seq
   L.mask_pitch = p->mask_pitch;
   L.budget_ppm = p->budget_ppm;
   L.sm_scale = p->sm_scale;
+  L.flags = p->flags;
   const cudaError_t e = cosa::launch_kap(L, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? COSA_OK : COSA_ERR_CUDA;
 }

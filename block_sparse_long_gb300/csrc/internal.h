@@ -61,6 +61,7 @@ struct KapLaunch {
   int num_reqs, num_q_heads, num_kv_heads, head_dim, block_size, page_size, stride;
   int total_tokens, max_seqlen, num_pages, max_pages_per_req, mask_pitch, budget_ppm;
   double sm_scale;
+  int flags;             // COSA_FLAG_*
 };
 
 size_t kap_workspace_bytes(int num_reqs, int num_q_heads, int num_kv_heads, int block_size, int stride,

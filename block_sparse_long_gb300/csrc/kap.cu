@@ -33,6 +33,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "cosa.h"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -89,6 +90,7 @@ struct KapArgs {
   int total_tokens, max_seqlen, num_pages, max_pages_per_req, mask_pitch, budget_ppm;
   int nqb_max, nrow_tiles_max, words_per_row;
   double sm_scale;
+  int ascending;         // write the selected blocks in ascending block order
 };
 
 struct ReqInfo {
@@ -1193,7 +1195,39 @@ __global__ void __launch_bounds__(kSelectThreads, 3) kap_select_kernel(KapArgs a
     }
     __syncthreads();
   }
-  for (int k = tid; k < a.mask_pitch; k += blockDim.x) out[k] = (k < K) ? key_block(key[k]) : -1;
+  if (a.ascending) {
+    // the same K_i blocks in ascending block order (visiting without remapping): mark them in
+    // hrm[] (no longer needed), then compact the marks with a block scan
+    __syncthreads();
+    for (int j = tid; j < J; j += blockDim.x) hrm[j] = 0;
+    __syncthreads();
+    for (int k = tid; k < K; k += blockDim.x) hrm[key_block(key[k])] = 1;
+    __syncthreads();
+    const int E = (J + kSelectThreads - 1) / kSelectThreads;
+    const int lane = tid & 31, w = tid >> 5;
+    int cnt = 0;
+    for (int e = 0; e < E; ++e) {
+      const int j = tid * E + e;
+      if (j < J && hrm[j]) ++cnt;
+    }
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_cnt_s[w] = incl;
+    __syncthreads();
+    int pos = incl - cnt;
+    for (int q = 0; q < w; ++q) pos += warp_cnt_s[q];
+    for (int e = 0; e < E; ++e) {
+      const int j = tid * E + e;
+      if (j < J && hrm[j]) out[pos++] = j;
+    }
+    for (int k = K + tid; k < a.mask_pitch; k += blockDim.x) out[k] = -1;
+  } else {
+    for (int k = tid; k < a.mask_pitch; k += blockDim.x) out[k] = (k < K) ? key_block(key[k]) : -1;
+  }
   if (tid == 0) a.mask_len[mrow] = K;
 }
 
@@ -1335,6 +1369,7 @@ cudaError_t launch_kap(const KapLaunch& L, cudaStream_t stream) {
   a.mask_pitch = L.mask_pitch;
   a.budget_ppm = L.budget_ppm;
   a.sm_scale = L.sm_scale;
+  a.ascending = (L.flags & COSA_FLAG_ASCENDING_ORDER) ? 1 : 0;
   a.nqb_max = (L.max_seqlen + L.block_size - 1) / L.block_size;
   const int rmax = (L.max_seqlen + L.stride - 1) / L.stride;
   a.nrow_tiles_max = (rmax + kRowTile - 1) / kRowTile;

@@ -64,7 +64,12 @@ struct alignas(1024) OskSmem {
   uint8_t k[NK][TILE];                        // [HD/64][BLK rows][128 B], SW128
   uint8_t v[NV][TILE];
   uint64_t q_full, q_free;
-  uint64_t k_full[NK], k_free[NK];
+  // k_full[slot][x]: K(v) landed, for the visits v of that slot with v % 2 == x.  A slot's visits
+  // alternate between the two S issuers, and a parity wait only tells two phases apart: with one
+  // barrier per slot, an issuer could wait for K(v) while K(v - NK) (the other issuer's) was still
+  // in flight and take that earlier phase for its own.  Split by issuer, each barrier's phases are
+  // waited for by one thread, in order.
+  uint64_t k_full[NK][2], k_free[NK];
   uint64_t v_full[NV], v_free[NV];
   uint64_t s_full[2], s_free[2];
   uint64_t p_full[4];                         // per computed visit c: P written (slot c & 3)
@@ -150,7 +155,8 @@ __device__ __forceinline__ Item decode_item(const OskArgs& a, int idx, int blk) 
   return it;
 }
 
-template <int BLK, int HD>
+// BIN: the mask rows are binary block masks walked in ascending order (logical skipping)
+template <int BLK, int HD, bool BIN>
 __global__ void __launch_bounds__(kThreads, 1)
     osk_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap_blk,
                const __grid_constant__ CUtensorMap kmap_pg, const __grid_constant__ CUtensorMap vmap_blk,
@@ -174,7 +180,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(&sm.q_full, 1);
     mbar_init(&sm.q_free, 2);        // one commit from each S issuer
-    for (int s = 0; s < NK; ++s) { mbar_init(&sm.k_full[s], 1); mbar_init(&sm.k_free[s], 1); }
+    for (int s = 0; s < NK; ++s) {
+      mbar_init(&sm.k_full[s][0], 1);
+      mbar_init(&sm.k_full[s][1], 1);
+      mbar_init(&sm.k_free[s], 1);
+    }
     for (int s = 0; s < NV; ++s) { mbar_init(&sm.v_full[s], 1); mbar_init(&sm.v_free[s], 1); }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&sm.s_full[s], 2);   // plain arrive (visit info) + UMMA commit
@@ -245,9 +255,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ++n;
       const int32_t* pt_row = a.page_table + static_cast<size_t>(it.b) * a.max_pages_per_req;
+      // binary mask: entry k selects block k; every causal block k < n_walk takes a turn through
+      // the pipeline, the unselected ones as empty visits
+      const int n_walk = BIN ? min(n_entries, i + 1) : 0;
       for (int k0 = 0; k0 < n_entries && ok; k0 += 32) {
         const int k = k0 + static_cast<int>(lane);
-        const int j = (k < n_entries) ? mask_row[k] : -1;
+        const int j = (k < n_entries) ? (BIN ? (mask_row[k] != 0 ? k : -1) : mask_row[k]) : -1;
         const bool valid = (k < n_entries) && j >= 0 && j <= i && j < nblk;
         const unsigned peers = __match_any_sync(0xffffffffu, valid ? j : -1 - static_cast<int>(lane));
         const bool first = valid && (static_cast<int>(lane) == __ffs(peers) - 1);
@@ -269,11 +282,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         __syncwarp();
-        unsigned todo = __ballot_sync(0xffffffffu, keep);
+        unsigned todo = __ballot_sync(0xffffffffu, keep || (BIN && k < n_walk));
         while (todo && ok) {
           const int src = __ffs(todo) - 1;
           todo &= todo - 1;
-          const int jj = __shfl_sync(0xffffffffu, j, src);
+          const int jj = __shfl_sync(0xffffffffu, (BIN && !keep) ? -2 : j, src);
           const uint32_t pg = __shfl_sync(0xffffffffu, pages, src);
           int ph[kMaxPagesPerBlock];
 #pragma unroll
@@ -289,17 +302,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             ki.kvh = kvh;
 #pragma unroll
             for (int u = 0; u < kMaxPagesPerBlock; ++u) ki.phys[u] = ph[u];
-            if (pages_consecutive(pg, all_pages, ph, pages_per_blk)) {
+            if (BIN && jj < 0) {
+              // a block the binary mask drops: nothing to load
+              mbar_arrive(&sm.k_full[slot][v & 1]);
+            } else if (pages_consecutive(pg, all_pages, ph, pages_per_blk)) {
               // the block's pages follow each other in the cache: one copy of the whole tile
-              mbar_arrive_expect_tx(&sm.k_full[slot], BLK * HD * 2);
-              tma_load_4d(&sm.k[slot][0], &kmap_blk, &sm.k_full[slot], 0, ph[0] * P, 0, kvh);
+              mbar_arrive_expect_tx(&sm.k_full[slot][v & 1], BLK * HD * 2);
+              tma_load_4d(&sm.k[slot][0], &kmap_blk, &sm.k_full[slot][v & 1], 0, ph[0] * P, 0, kvh);
             } else {
               const uint32_t bytes = static_cast<uint32_t>(__popc(pg)) * DH * P * 128u;
-              mbar_arrive_expect_tx(&sm.k_full[slot], bytes);
+              mbar_arrive_expect_tx(&sm.k_full[slot][v & 1], bytes);
               for (int u = 0; u < pages_per_blk; ++u) {
                 if (!((pg >> u) & 1u)) continue;
                 for (int dh = 0; dh < DH; ++dh)
-                  tma_load_4d(&sm.k[slot][dh * S::HALF + u * P * 128], &kmap_pg, &sm.k_full[slot], 0, ph[u] * P, dh, kvh);
+                  tma_load_4d(&sm.k[slot][dh * S::HALF + u * P * 128], &kmap_pg, &sm.k_full[slot][v & 1], 0, ph[u] * P, dh, kvh);
               }
             }
           }
@@ -313,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (v >= NK) ok = warp_wait(&sm.k_free[slot], ((v / NK) - 1) & 1, abort_flag, a.status);
         if (ok && lane == 0) {
           sm.info[v & 7].blk = -1;
-          mbar_arrive(&sm.k_full[slot]);
+          mbar_arrive(&sm.k_full[slot][v & 1]);
         }
         __syncwarp();
         ++v;
@@ -323,8 +339,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (*abort_flag && lane == 0) {
       if (n > 0) wait_parity_bounded(&sm.q_full, (n - 1) & 1, nullptr, nullptr);
       for (int s = 0; s < NK; ++s) {
-        const int issued = (v - s + NK - 1) / NK;  // loads issued into slot s
-        if (issued > 0) wait_parity_bounded(&sm.k_full[s], (issued - 1) & 1, nullptr, nullptr);
+        for (int x = 0; x < 2; ++x) {
+          // visits u < v of slot s with u % 2 == x are u = r, r + 2 NK, ...
+          const int r = (s % 2 == x) ? s : s + NK;
+          const int issued = (v > r) ? (v - r + 2 * NK - 1) / (2 * NK) : 0;
+          if (issued > 0) wait_parity_bounded(&sm.k_full[s][x], (issued - 1) & 1, nullptr, nullptr);
+        }
       }
     }
   } else if (warp == kWarpMma || warp == kWarpS2) {
@@ -348,7 +368,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         while (ok) {
           const int slot = vv % NK, sb = X;
-          if (!wait_parity_bounded(&sm.k_full[slot], (vv / NK) & 1, abort_flag, a.status)) { ok = false; break; }
+          if (!wait_parity_bounded(&sm.k_full[slot][X], (vv / (2 * NK)) & 1, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
           if (vv >= 2 && !wait_parity_bounded(&sm.s_free[sb], ((vv >> 1) - 1) & 1, abort_flag, a.status)) {
             ok = false;
             break;
@@ -357,11 +380,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int blk = sm.info[vv & 7].blk;
           mbar_arrive(&sm.s_full[sb]);
           if (blk < 0) {
-            // end of the item: no product; the K slot and the S buffer pass on unused
+            // end of the item (-1) or a dropped block (-2): no product; the K slot and the S
+            // buffer pass on unused
             mbar_arrive(&sm.s_full[sb]);
             mbar_arrive(&sm.k_free[slot]);
             vv += 2;
-            break;
+            if (!BIN || blk == -1) break;
+            continue;
           }
           tc_fence_after();
           const uint64_t kslot = kdesc + static_cast<uint64_t>(slot * (S::TILE >> 4));
@@ -542,6 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // end of the item or a wait that ran out: every softmax warp learns it at the same barrier
         if (named_bar_red_or(1, kSoftmaxThreads, !okw || ki_blk < 0)) {
           if (named_bar_red_or(2, kSoftmaxThreads, !okw)) ok = false;
+          if (BIN && ok && ki_blk == -2) continue;   // a block the binary mask drops
           if (ok) {
             // the item's second end marker (the other S issuer's): release that buffer too
             const int v1 = v + 1;
@@ -712,8 +738,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BLK, int HD>
-cudaError_t launch_osk_t(const OskLaunch& L, cudaStream_t stream) {
+template <int BLK, int HD, bool BIN>
+cudaError_t launch_osk_b(const OskLaunch& L, cudaStream_t stream) {
   OskArgs a;
   a.cu_seqlens = L.cu_seqlens;
   a.page_table = L.page_table;
@@ -736,7 +762,7 @@ cudaError_t launch_osk_t(const OskLaunch& L, cudaStream_t stream) {
   a.skip_delta = L.skip_delta;
   a.stall = (L.flags & COSA_FLAG_TEST_STALL) ? 1 : 0;
   const size_t smem = sizeof(OskSmem<BLK, HD>) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(osk_kernel<BLK, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(osk_kernel<BLK, HD, BIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const long long items =
@@ -751,8 +777,14 @@ cudaError_t launch_osk_t(const OskLaunch& L, cudaStream_t stream) {
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(items < sms ? items : sms);
-  osk_kernel<BLK, HD><<<grid, kThreads, smem, stream>>>(L.qmap, L.kmap_blk, L.kmap_pg, L.vmap_blk, L.vmap_pg, a);
+  osk_kernel<BLK, HD, BIN><<<grid, kThreads, smem, stream>>>(L.qmap, L.kmap_blk, L.kmap_pg, L.vmap_blk, L.vmap_pg, a);
   return cudaGetLastError();
+}
+
+template <int BLK, int HD>
+cudaError_t launch_osk_t(const OskLaunch& L, cudaStream_t stream) {
+  return (L.flags & COSA_FLAG_BINARY_MASK) ? launch_osk_b<BLK, HD, true>(L, stream)
+                                           : launch_osk_b<BLK, HD, false>(L, stream);
 }
 
 }  // namespace

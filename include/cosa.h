@@ -76,6 +76,18 @@ extern "C" {
    nothing, so every wait inside the kernel runs out after its 2 s budget, the kernel stops cleanly and
    *device_status becomes COSA_ERR_DEVICE_TIMEOUT; out is then undefined.  The CUDA context stays usable. */
 #define COSA_FLAG_TEST_STALL 1
+/* Ablation switch of cosa_proxy_select (ignored by cosa_sparse_prefill): write the same K_i selected
+   blocks in ascending block order instead of the computation order rho_i of Eq. (14), i.e. visiting
+   without KV page remapping (the "w/o remap" arm of the paper's Sec. 5.4, Fig. 6 and App. D.4). */
+#define COSA_FLAG_ASCENDING_ORDER 2
+/* Ablation switch of cosa_sparse_prefill (ignored by cosa_proxy_select): read each mask row as the
+   binary block mask M_01 of the paper's Eq. (3) instead of a list of block IDs.  Entry j != 0 selects
+   key block j.  The kernel walks every block j < min(mask_len, i + 1) in ascending order and drops the
+   unselected ones by a logical test, each still taking one turn through its pipeline (the logical
+   mask skipping of BSA kernels, Sec. 4.3 and App. D.3); visit_flags[j] reports block j, and
+   entries past the walk are IGNORED.  The output equals that of the ascending ID list of the selected
+   blocks. */
+#define COSA_FLAG_BINARY_MASK 4
 
 /* values written to visit_flags (one per mask entry) */
 #define COSA_VISIT_COMPUTED 0 /* softmax and P.V accumulated (pattern 3 of the paper's Fig. 4) */

@@ -190,12 +190,14 @@ def kap_request_head(Q: np.ndarray, K: np.ndarray, exists: np.ndarray, prm: Para
 
 
 def kap_mask(q_bits, k_bits, page_table, cu_seqlens, num_q_heads, num_kv_heads, prm: Params, kmax: int,
-             heads: Optional[Sequence[int]] = None, qblocks: Optional[dict] = None):
+             heads: Optional[Sequence[int]] = None, qblocks: Optional[dict] = None, ascending: bool = False):
     """Eq. (14) for every (request, head, query block): returns (mask, mask_len, rows).
 
     mask [B, Hq, nqb_max, kmax] int32 (-1 padded), mask_len [B, Hq, nqb_max] int32,
     rows {(b, h, i): KapRow}.  ``qblocks`` may restrict the work to {(b, h): [i, ...]}; rows
-    not computed keep mask_len 0.
+    not computed keep mask_len 0.  ``ascending`` writes the same K_i blocks in ascending block
+    order: visiting without KV page remapping, the "w/o remap" arm of Sec. 5.4 (Fig. 6) and
+    App. D.4 (Fig. C).
     """
     B = len(cu_seqlens) - 1
     G = num_q_heads // num_kv_heads
@@ -215,7 +217,8 @@ def kap_mask(q_bits, k_bits, page_table, cu_seqlens, num_q_heads, num_kv_heads, 
             for i, row in kap_request_head(Q, K, ex, prm, sel).items():
                 if row.K > kmax:
                     raise ValueError("mask pitch too small")
-                mask[bi, h, i, :row.K] = row.order[:row.K]
+                sel = row.order[:row.K]
+                mask[bi, h, i, :row.K] = np.sort(sel) if ascending else sel
                 mask_len[bi, h, i] = row.K
                 rows[(bi, h, i)] = row
     return mask, mask_len, rows
@@ -293,6 +296,43 @@ def osk_qblock(Q: np.ndarray, K: np.ndarray, V: np.ndarray, exists: np.ndarray, 
     return OskResult(out=out, flags=flags, margins=margins, row_max=m, row_sum=l)
 
 
+def binary_mask(mask: np.ndarray, mask_len: np.ndarray, nqb_max: int) -> Tuple[np.ndarray, np.ndarray]:
+    """The binary block mask M_01 of Eq. (3) (Sec. 3.2) holding the same selection as an ID-list
+    mask: M01[b, h, i, j] = 1 iff block j is among the first mask_len[b, h, i] entries of row i
+    and 0 <= j <= i (entries outside the causal candidates select nothing).  Returns (M01, lengths)
+    with length i + 1 (every causal candidate) for rows that hold entries, else 0."""
+    B, H, nqb, _ = mask.shape
+    m01 = np.zeros((B, H, nqb, nqb_max), dtype=np.int32)
+    len01 = np.where(mask_len > 0, np.arange(nqb, dtype=np.int32)[None, None, :] + 1, 0).astype(np.int32)
+    for b in range(B):
+        for h in range(H):
+            for i in range(nqb):
+                for k in range(int(mask_len[b, h, i])):
+                    j = int(mask[b, h, i, k])
+                    if 0 <= j <= i:
+                        m01[b, h, i, j] = 1
+    return m01, len01
+
+
+def osk_qblock_binary(Q: np.ndarray, K: np.ndarray, V: np.ndarray, exists: np.ndarray, i: int,
+                      m01_row: Sequence[int], n: int, prm: Params,
+                      force: Optional[Sequence[int]] = None) -> OskResult:
+    """Query block i driven by a binary block mask (Eq. (3)) with logical skipping, as BSA kernels
+    do (Sec. 3.2, Sec. 4.3): the loop runs over blocks j = 0 .. min(n, i + 1) - 1 in ascending order
+    and works on those with m01_row[j] != 0.  Flags and margins are indexed by j; unselected and
+    unwalked entries are IGNORED.  ``force`` is indexed by j as well."""
+    walk = min(n, i + 1)
+    sel = [j for j in range(walk) if int(m01_row[j]) != 0]
+    f = None if force is None else [force[j] for j in sel]
+    r = osk_qblock(Q, K, V, exists, i, sel, len(sel), prm, f)
+    flags = np.full(n, IGNORED, dtype=np.int8)
+    margins = np.full(n, np.nan)
+    for x, j in enumerate(sel):
+        flags[j] = r.flags[x]
+        margins[j] = r.margins[x]
+    return OskResult(out=r.out, flags=flags, margins=margins, row_max=r.row_max, row_sum=r.row_sum)
+
+
 def computed_tokens(flags: np.ndarray, mask_row: Sequence[int], L: int, b: int, exists: np.ndarray,
                     row_pos: int) -> List[int]:
     """Token set of one query row: PageWeaver Eq. (1) over the blocks the OSK computed."""
@@ -302,10 +342,12 @@ def computed_tokens(flags: np.ndarray, mask_row: Sequence[int], L: int, b: int, 
 
 
 def osk_all(q_bits, k_bits, v_bits, page_table, cu_seqlens, num_q_heads, num_kv_heads, prm: Params,
-            mask, mask_len, items: Optional[Sequence[Tuple[int, int, int]]] = None, force=None):
+            mask, mask_len, items: Optional[Sequence[Tuple[int, int, int]]] = None, force=None,
+            binary: bool = False):
     """OSK over (request, head, query block) items (all if ``items`` is None).
 
     Returns {(b, h, i): OskResult}.  ``force`` maps items to per-entry forced decisions.
+    ``binary``: the mask rows are binary block masks (see osk_qblock_binary).
     """
     B = len(cu_seqlens) - 1
     G = num_q_heads // num_kv_heads
@@ -325,7 +367,8 @@ def osk_all(q_bits, k_bits, v_bits, page_table, cu_seqlens, num_q_heads, num_kv_
         for i in blocks:
             n = int(mask_len[b, h, i])
             f = None if force is None else force.get((b, h, i))
-            res[(b, h, i)] = osk_qblock(Q, K, V, ex, i, mask[b, h, i], n, prm, f)
+            run = osk_qblock_binary if binary else osk_qblock
+            res[(b, h, i)] = run(Q, K, V, ex, i, mask[b, h, i], n, prm, f)
     return res
 
 

@@ -59,6 +59,34 @@ def cosa_params(dw: DevWorkload, *, delta: float, mask_pitch: int, budget_ppm: O
                         mask_pitch=mask_pitch, skip_delta=delta)
 
 
+def binary_of(mask: np.ndarray, mask_len: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
+    """Binary block masks (entry j = 1 iff block j is listed, 0 <= j <= i) of ID-list masks, with
+    walk length i + 1 on rows that list something (vectorised form of the oracle's binary_mask)."""
+    B, H, nqb, pitch = mask.shape
+    i_idx = np.arange(nqb)[None, None, :, None]
+    k_idx = np.arange(pitch)[None, None, None, :]
+    ok = (k_idx < mask_len[..., None]) & (mask >= 0) & (mask <= i_idx)
+    m01 = np.zeros((B, H, nqb, nqb + 1), dtype=np.int32)
+    bb, hh, ii, kk = np.nonzero(ok)
+    m01[bb, hh, ii, mask[bb, hh, ii, kk]] = 1
+    len01 = np.where(mask_len > 0, np.arange(nqb, dtype=np.int32)[None, None, :] + 1, 0).astype(np.int32)
+    return m01[..., :nqb], len01
+
+
+def ascending_of(m01: np.ndarray, len01: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
+    """ID lists of the selected blocks in ascending order (the visits a binary mask walk makes)."""
+    B, H, nqb, _ = m01.shape
+    ids = np.full((B, H, nqb, nqb), -1, dtype=np.int32)
+    lens = np.zeros((B, H, nqb), dtype=np.int32)
+    for b in range(B):
+        for h in range(H):
+            for i in range(nqb):
+                sel = np.nonzero(m01[b, h, i, :len01[b, h, i]])[0]
+                ids[b, h, i, :len(sel)] = sel
+                lens[b, h, i] = len(sel)
+    return ids, lens
+
+
 def run_kap(dw: DevWorkload, p) -> Tuple[np.ndarray, np.ndarray]:
     status = torch.zeros(1, dtype=torch.int32, device=dw.q.device)
     mask, mask_len = C.cosa_proxy_select(p, dw.q, dw.cu, dw.k, dw.pt, status=status)
@@ -102,12 +130,13 @@ class OskReport:
 
 
 def compare_osk(w: synth.Workload, prm: orc.Params, mask, mask_len, out_gpu, flags_gpu,
-                items) -> OskReport:
+                items, binary: bool = False) -> OskReport:
     """Oracle vs GPU on the given items.  Skip decisions may differ only near a zero margin;
-    the oracle is then replayed with the GPU's decisions so outputs compare like for like."""
+    the oracle is then replayed with the GPU's decisions so outputs compare like for like.
+    ``binary``: the masks are binary block masks (COSA_FLAG_BINARY_MASK)."""
     sp = w.spec
     ref = orc.osk_all(w.q, w.k_cache, w.v_cache, w.page_table, w.cu_seqlens, sp.num_q_heads, sp.num_kv_heads,
-                      prm, mask, mask_len, items=items)
+                      prm, mask, mask_len, items=items, binary=binary)
     n_tested = 0
     dis = []
     force = {}
@@ -127,7 +156,8 @@ def compare_osk(w: synth.Workload, prm: orc.Params, mask, mask_len, out_gpu, fla
         assert (flags_gpu[b, h, i, n:] == orc.IGNORED).all()
     if force:
         ref.update(orc.osk_all(w.q, w.k_cache, w.v_cache, w.page_table, w.cu_seqlens, sp.num_q_heads,
-                               sp.num_kv_heads, prm, mask, mask_len, items=list(force), force=force))
+                               sp.num_kv_heads, prm, mask, mask_len, items=list(force), force=force,
+                               binary=binary))
     errs = []
     cu = w.cu_seqlens
     for (b, h, i), r in ref.items():

@@ -405,9 +405,92 @@ def check_kap_mask_layout(orc):
     assert (ml[1, :, nqb1:] == 0).all() and (mask[1, :, nqb1:] == -1).all()
 
 
+# --------------------------------------------------------------------------- #
+# ablation modes: ascending-order visiting (no remap) and binary-mask visiting
+# --------------------------------------------------------------------------- #
+def check_ascending_mask(orc):
+    # hand case of _kap_hand: rho_2 = [1, 0, 2]; K_2 = ceil(0.6 * 3) = 2 keeps {1, 0}, written as [0, 1]
+    q, kc, _ = hand_problem([2, 0, 1, 3, 0, 1], [0] * 6, [1.0] * 6, 6)
+    kc = kc.reshape(3, 2, 1, 1)
+    prm = orc.Params(2, 2, 1, 600_000, 1.0, -1.0)
+    cu = np.array([0, 6], np.int32)
+    pt = np.arange(3, dtype=np.int32)[None, :]
+    m, ml, _ = orc.kap_mask(q, kc, pt, cu, 1, 1, prm, 3)
+    assert list(m[0, 0, 2]) == [1, 0, -1] and ml[0, 0, 2] == 2
+    m, ml, _ = orc.kap_mask(q, kc, pt, cu, 1, 1, prm, 3, ascending=True)
+    assert list(m[0, 0, 2]) == [0, 1, -1] and ml[0, 0, 2] == 2
+    # on a seeded workload: same lengths, same sets, strictly ascending rows, -1 tails
+    spec = tiny_spec(seed=67)
+    w = synth.make_workload(spec)
+    prm = params(orc, spec)
+    args = (w.q, w.k_cache, w.page_table, w.cu_seqlens, spec.num_q_heads, spec.num_kv_heads, prm, 9)
+    m0, l0, _ = orc.kap_mask(*args)
+    m1, l1, _ = orc.kap_mask(*args, ascending=True)
+    assert np.array_equal(l0, l1)
+    for idx in np.ndindex(l0.shape):
+        n = int(l0[idx])
+        row = m1[idx]
+        assert sorted(m0[idx][:n].tolist()) == row[:n].tolist()
+        assert (np.diff(row[:n]) > 0).all() and (row[n:] == -1).all()
+
+
+def check_binary_mask_visiting(orc):
+    e = math.exp
+    # Eq. (3) from an ID list: invalid, future and repeated IDs select nothing
+    ids = np.full((1, 1, 4, 5), -1, np.int32)
+    ids[0, 0, 3] = [2, 0, -1, 5, 2]
+    ids[0, 0, 1] = [1, 0, 0, 1, 0]
+    m01, l01 = orc.binary_mask(ids, np.array([[[0, 2, 0, 5]]], np.int32), 6)
+    assert m01[0, 0, 3].tolist() == [1, 0, 1, 0, 0, 0] and m01[0, 0, 1].tolist() == [1, 1, 0, 0, 0, 0]
+    assert m01[0, 0, 0].tolist() == [0] * 6 and m01[0, 0, 2].tolist() == [0] * 6
+    assert l01[0, 0].tolist() == [0, 2, 0, 4]
+    # the hand case of _skip_case, walked in ascending order under the binary mask {0, 3, 5, 7}
+    k = [1, 0, 0, 4, 0, 3, 0, 5]
+    v = [10, 0, 0, 20, 0, 30, 0, 40]
+    q, kc, vc = hand_problem(k, v, [1.0] * 8, 8)
+    K = f64(kc[:, 0, 0, :])
+    V = f64(vc[:, 0, 0, :])
+    Q = f64(q[:, 0, :])
+    row = [1, 0, 0, 1, 0, 1, 0, 1]
+    # delta = 1 (tau = ln(1/8)): ascending visiting skips nothing
+    r = orc.osk_qblock_binary(Q, K, V, np.ones(8, bool), 7, row, 8, orc.Params(1, 1, 1, 1_000_000, 1.0, 1.0))
+    assert list(r.flags) == [0, 2, 2, 0, 2, 0, 2, 0]
+    want = (e(1) * 10 + e(4) * 20 + e(3) * 30 + e(5) * 40) / (e(1) + e(4) + e(3) + e(5))
+    np.testing.assert_allclose(r.out[0, 0], want, rtol=1e-13)
+    # delta = N (tau = 0): block 5 (logit 3) comes after block 3 (logit 4) and is skipped
+    r = orc.osk_qblock_binary(Q, K, V, np.ones(8, bool), 7, row, 8, orc.Params(1, 1, 1, 1_000_000, 1.0, 8.0))
+    assert list(r.flags) == [0, 2, 2, 0, 2, 1, 2, 0]
+    np.testing.assert_allclose(r.margins[[0, 3, 5, 7]], [0.0, 0.0, -1.0, 0.0], atol=1e-12)
+    want = (e(1) * 10 + e(4) * 20 + e(5) * 40) / (e(1) + e(4) + e(5))
+    np.testing.assert_allclose(r.out[0, 0], want, rtol=1e-13)
+    # a walk shorter than the candidates: blocks past it are not visited
+    r = orc.osk_qblock_binary(Q, K, V, np.ones(8, bool), 7, row, 4, orc.Params(1, 1, 1, 1_000_000, 1.0, -1.0))
+    assert list(r.flags) == [0, 2, 2, 0]
+    np.testing.assert_allclose(r.out[0, 0], (e(1) * 10 + e(4) * 20) / (e(1) + e(4)), rtol=1e-13)
+    # every block selected and skipping off: dense causal attention
+    import torch
+    spec = tiny_spec(lengths=(200,), seed=12)
+    w = synth.make_workload(spec)
+    prm = params(orc, spec, delta=-1.0)
+    b = spec.block_size
+    nqb = -(-200 // b)
+    ones = np.ones((1, spec.num_q_heads, nqb, nqb), np.int32)
+    lens = np.broadcast_to(np.arange(1, nqb + 1, dtype=np.int32), (1, spec.num_q_heads, nqb)).copy()
+    res = orc.osk_all(w.q, w.k_cache, w.v_cache, w.page_table, w.cu_seqlens, spec.num_q_heads,
+                      spec.num_kv_heads, prm, ones, lens, items=[(0, 3, i) for i in range(nqb)], binary=True)
+    Kd, Vd = logical_kv(w, 0, 3 // (spec.num_q_heads // spec.num_kv_heads))
+    Qd = f64(w.q[:, 3, :])
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(Qd)[None, None], torch.from_numpy(Kd)[None, None],
+        torch.from_numpy(Vd)[None, None], is_causal=True, scale=prm.sm_scale)[0, 0].numpy()
+    for i in range(nqb):
+        np.testing.assert_allclose(res[(0, 3, i)].out, ref[i * b:min(200, (i + 1) * b)], rtol=0, atol=1e-12)
+        assert (res[(0, 3, i)].flags == orc.COMPUTED).all()
+
+
 ALL_CHECKS = [
     check_token_set_worked_example, check_dense_reduction, check_order_invariance,
     check_direct_definition, check_skip_hand_cases, check_skip_bucket_case, check_skip_invariants,
     check_stage1_count, check_kap_hand_cases, check_kap_brute_force, check_kap_invariants,
-    check_kap_mask_layout,
+    check_kap_mask_layout, check_ascending_mask, check_binary_mask_visiting,
 ]

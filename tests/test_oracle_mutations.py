@@ -48,6 +48,13 @@ MUTATIONS = {
     "budget_floor": ("return max(1, min(J, -(-budget_ppm * J // 1_000_000)))",
                      "return max(1, min(J, budget_ppm * J // 1_000_000))"),
     "no_scale_in_kap": ("logits = (Qs_rows @ Ks.T) * sm_scale", "logits = (Qs_rows @ Ks.T)"),
+    # ablation modes
+    "ascending_left_unsorted": ("mask[bi, h, i, :row.K] = np.sort(sel) if ascending else sel",
+                                "mask[bi, h, i, :row.K] = sel"),
+    "ascending_sorts_before_truncation": ("sel = row.order[:row.K]", "sel = np.sort(row.order)[:row.K]"),
+    "binary_flags_by_visit": ("flags[j] = r.flags[x]", "flags[x] = r.flags[x]"),
+    "binary_walk_includes_diagonal_only": ("walk = min(n, i + 1)", "walk = min(n, i)"),
+    "binary_mask_keeps_future": ("if 0 <= j <= i:", "if 0 <= j:"),
 }
 
 
