@@ -505,6 +505,8 @@ def run_ablation(args):
       same selected blocks visited (a) as an ascending ID list (physical jumps), (b) through the binary
       mask with logical skipping of the unselected blocks (BSA-style loop), (c) in the computation
       order; each against the dense endpoint of the same kernel: the analogue of CoSA Fig. B.
+    topp: the top-p stage-1 rule (p in {0.8, 0.9, 0.95, 0.99}; the paper runs Qwen at 0.95): realised
+      stage-1 budget, KAP time, and OSK time with skipping off and at the workload's Delta.
     Inputs have the 128K workload's structure at the given length."""
     import torch
     from block_sparse_long_gb300 import cosa as C
@@ -555,7 +557,34 @@ def run_ablation(args):
         l01 = torch.where(ml > 0, torch.arange(1, nqb + 1, dtype=torch.int32, device=dev)[None, None, :], 0)
         return m01[..., :nqb].contiguous(), l01.to(torch.int32).contiguous()
 
-    out_lines = []
+    if args.ablation == "topp":
+        n_tok = args.ablation_tokens
+        spec, t = setup(n_tok)
+        out = torch.empty_like(t["q"])
+        nqb = -(-n_tok // spec.block_size)
+        cand = spec.num_q_heads * nqb * (nqb + 1) // 2
+        delta = 15000.0 * n_tok / 131072
+        mask = torch.empty((1, spec.num_q_heads, nqb, nqb), dtype=torch.int32, device=dev)
+        ml = torch.empty((1, spec.num_q_heads, nqb), dtype=torch.int32, device=dev)
+        for ppm in (800_000, 900_000, 950_000, 990_000):
+            p = params(spec, t, ppm, nqb, delta, C.COSA_FLAG_TOP_P)
+            ws = torch.empty(C.cosa_proxy_workspace_size(p), dtype=torch.uint8, device=dev)
+            kap_ms = timed(lambda: C.cosa_proxy_select(p, t["q"], t["cu"], t["k"], t["pt"], mask=mask, mask_len=ml,
+                                                       workspace=ws), 3)
+            rec = {"ablation": "topp", "workload": spec.name, "tokens": n_tok, "top_p": ppm / 1e6,
+                   "stage1_budget": int(ml.sum()) / cand, "kap_ms": kap_ms}
+            for name, d in (("osk_no_skip_ms", -1.0), ("osk_ms", delta)):
+                pd = params(spec, t, ppm, nqb, d)
+                rec[name] = timed(lambda: C.cosa_sparse_prefill(pd, t["q"], t["cu"], t["k"], t["v"], t["pt"], mask,
+                                                                ml, out=out), 3)
+            flags = torch.empty(mask.shape, dtype=torch.uint8, device=dev)
+            C.cosa_sparse_prefill(params(spec, t, ppm, nqb, delta), t["q"], t["cu"], t["k"], t["v"], t["pt"], mask, ml,
+                                  out=out, visit_flags=flags)
+            rec["skip_delta"] = delta
+            rec["budget_after_skip"] = int((flags == C.VISIT_COMPUTED).sum()) / cand
+            print(json.dumps(rec), flush=True)
+            del ws, flags
+        return 0
     if args.ablation == "remap":
         n_tok = args.ablation_tokens
         spec, t = setup(n_tok)
@@ -621,10 +650,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true",
                     help="time CoSA against the dense endpoint of the same kernel from 4K to 128K tokens")
-    ap.add_argument("--ablation", choices=["remap", "jump"],
+    ap.add_argument("--ablation", choices=["remap", "jump", "topp"],
                     help="remap: skip ratio vs Delta with and without remapping over stage-1 budgets; "
-                         "jump: physical jumps vs logical skipping of a binary mask")
-    ap.add_argument("--ablation-tokens", type=int, default=131072, help="context length of --ablation remap")
+                         "jump: physical jumps vs logical skipping of a binary mask; topp: the top-p stage-1 rule")
+    ap.add_argument("--ablation-tokens", type=int, default=131072, help="context length of --ablation remap/topp")
     args = ap.parse_args()
     if args.sweep:
         return run_sweep(args)

@@ -96,6 +96,7 @@ def cosa_status_string(code: int) -> str:
 COSA_FLAG_TEST_STALL = 1   # test hook of cosa_sparse_prefill: every in-kernel wait runs out
 COSA_FLAG_ASCENDING_ORDER = 2   # cosa_proxy_select writes the selected blocks in ascending order
 COSA_FLAG_BINARY_MASK = 4       # cosa_sparse_prefill reads mask rows as binary block masks
+COSA_FLAG_TOP_P = 8             # cosa_proxy_select: budget_ppm is the top-p threshold p
 
 
 def make_params(*, num_reqs, num_q_heads, num_kv_heads, head_dim, block_size, page_size, stride=None,
@@ -110,10 +111,11 @@ def make_params(*, num_reqs, num_q_heads, num_kv_heads, head_dim, block_size, pa
         skip_delta=float(skip_delta))
 
 
-def stage1_pitch(budget_ppm: int, max_seqlen: int, block_size: int) -> int:
-    """Smallest mask pitch that holds K_i = ceil(B1 (i+1)) for every query block."""
+def stage1_pitch(budget_ppm: int, max_seqlen: int, block_size: int, top_p: bool = False) -> int:
+    """Smallest mask pitch that holds K_i = ceil(B1 (i+1)) for every query block (with top-p, every
+    causal candidate)."""
     nqb = -(-max_seqlen // block_size)
-    return max(1, -(-budget_ppm * nqb // 1_000_000))
+    return nqb if top_p else max(1, -(-budget_ppm * nqb // 1_000_000))
 
 
 def cosa_proxy_workspace_size(p: CosaParams) -> int:

@@ -91,6 +91,7 @@ struct KapArgs {
   int nqb_max, nrow_tiles_max, words_per_row;
   double sm_scale;
   int ascending;         // write the selected blocks in ascending block order
+  int top_p;             // budget_ppm is the top-p threshold p, not the fraction B1
 };
 
 struct ReqInfo {
@@ -863,6 +864,48 @@ __device__ void select_top_keys(unsigned long long* key, const uint8_t* hrm, con
   sort_keys_desc<1>(s1, key, kSelectThreads);
 }
 
+// Top-p length: the shortest prefix of the sorted candidates key[0..J) whose fp32 scores (summed in
+// float64) reach p = ppm / 1e6 of the total; at least 1.  Thread t scans positions t*E .. t*E+E-1.
+__device__ int top_p_count(const unsigned long long* key, const float* score, int J, int ppm, double* warp_sum,
+                           int& first_s) {
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int E = (J + kSelectThreads - 1) / kSelectThreads;
+  double part = 0.0;
+  for (int e = 0; e < E; ++e) {
+    const int x = tid * E + e;
+    if (x < J) part += static_cast<double>(fmaxf(score[key_block(key[x])], 0.0f));
+  }
+  double incl = part;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_sum[w] = incl;
+  if (tid == 0) first_s = J;
+  __syncthreads();
+  double before = incl - part, total = 0.0;
+  for (int q = 0; q < kSelectThreads / 32; ++q) {
+    if (q < w) before += warp_sum[q];
+    total += warp_sum[q];
+  }
+  const double thr = static_cast<double>(ppm) / 1e6 * total;
+  double run = before;
+  for (int e = 0; e < E; ++e) {
+    const int x = tid * E + e;
+    if (x >= J) break;
+    run += static_cast<double>(fmaxf(score[key_block(key[x])], 0.0f));
+    if (run >= thr) {
+      atomicMin(&first_s, x);
+      break;
+    }
+  }
+  __syncthreads();
+  const int k = first_s + 1;
+  __syncthreads();
+  return k < 1 ? 1 : (k > J ? J : k);
+}
+
 template <int E>
 __device__ void select_top_dispatch(unsigned long long* key, const uint8_t* hrm, const float* score,
                                     const float* serr, int J, int K, TopkShared& sh) {
@@ -882,7 +925,8 @@ __global__ void __launch_bounds__(kSelectThreads, 3) kap_select_kernel(KapArgs a
   double* terms = reinterpret_cast<double*>(
       (reinterpret_cast<uintptr_t>(hrm + 2 * cap) + 15) & ~uintptr_t(15));     // [kRepChunk * KB] row terms
   uint8_t* cutf = hrm + cap;                                                   // [cap] certain-cut flags
-  __shared__ int32_t n_rep_s, n_hrm_s, cstar_s[2], warp_cnt_s[kSelectThreads / 32], sentinel_marked_s;
+  __shared__ int32_t n_rep_s, n_hrm_s, cstar_s[2], warp_cnt_s[kSelectThreads / 32], sentinel_marked_s, topk_s;
+  __shared__ double warp_sum_s[kSelectThreads / 32];
   __shared__ TopkShared topk;
 
   const int tid = threadIdx.x;
@@ -900,7 +944,8 @@ __global__ void __launch_bounds__(kSelectThreads, 3) kap_select_kernel(KapArgs a
     return;
   }
   const int J = i + 1;
-  const int K = max(1, min(J, static_cast<int>((static_cast<long long>(a.budget_ppm) * J + 999999) / 1000000)));
+  // K_i of the fraction rule; the top-p rule replaces it once the candidates are sorted
+  int K = max(1, min(J, static_cast<int>((static_cast<long long>(a.budget_ppm) * J + 999999) / 1000000)));
   const int kvh = h / (a.num_q_heads / a.num_kv_heads);
   const int nqb = ri.nqb;
   const int64_t sbase = a.sc_off[b] + static_cast<int64_t>(h) * nqb * nqb + static_cast<int64_t>(i) * nqb;
@@ -940,7 +985,7 @@ __global__ void __launch_bounds__(kSelectThreads, 3) kap_select_kernel(KapArgs a
   int Jl = J, nh = nh_all, n2 = 1, Nl = kSelectThreads;
   bool sentinel = false;
   float sentinel_hi = -INFINITY;
-  for (int attempt = (K <= kTopFast && K < J) ? 0 : 1; attempt < 2; ++attempt) {
+  for (int attempt = (!a.top_p && K <= kTopFast && K < J) ? 0 : 1; attempt < 2; ++attempt) {
     int N2 = 1;
     while (N2 < J) N2 <<= 1;
     const int N = N2 < kSelectThreads ? kSelectThreads : N2;
@@ -965,6 +1010,7 @@ __global__ void __launch_bounds__(kSelectThreads, 3) kap_select_kernel(KapArgs a
         case 8: sort_block_keys<8>(key, hrm, sc, J, N); break;
         default: sort_block_keys<16>(key, hrm, sc, J, N); break;
       }
+      if (a.top_p) K = top_p_count(key, sc, J, a.budget_ppm, warp_sum_s, topk_s);
       sentinel = false;
       Jl = J;
       nh = nh_all;
@@ -1370,6 +1416,7 @@ cudaError_t launch_kap(const KapLaunch& L, cudaStream_t stream) {
   a.budget_ppm = L.budget_ppm;
   a.sm_scale = L.sm_scale;
   a.ascending = (L.flags & COSA_FLAG_ASCENDING_ORDER) ? 1 : 0;
+  a.top_p = (L.flags & COSA_FLAG_TOP_P) ? 1 : 0;
   a.nqb_max = (L.max_seqlen + L.block_size - 1) / L.block_size;
   const int rmax = (L.max_seqlen + L.stride - 1) / L.stride;
   a.nrow_tiles_max = (rmax + kRowTile - 1) / kRowTile;

@@ -88,6 +88,12 @@ extern "C" {
    entries past the walk are IGNORED.  The output equals that of the ascending ID list of the selected
    blocks. */
 #define COSA_FLAG_BINARY_MASK 4
+/* Stage-1 budget by top-p (cosa_proxy_select; the paper's Sec. 5.1 and App. D.1 use p = 0.95): budget_ppm
+   holds p in parts per million and K_i is the length of the shortest prefix of rho_i (Eq. (13)) whose
+   block scores s_ij (Eq. (11)) sum to at least p times the sum over all causal candidates j <= i.  The
+   cut is taken on the kernel's fp32 scores (summed in float64); mask_pitch must be >= ceil(max_seqlen /
+   block_size), since K_i can reach i + 1. */
+#define COSA_FLAG_TOP_P 8
 
 /* values written to visit_flags (one per mask entry) */
 #define COSA_VISIT_COMPUTED 0 /* softmax and P.V accumulated (pattern 3 of the paper's Fig. 4) */
@@ -108,7 +114,8 @@ typedef struct cosa_params {
   int32_t max_pages_per_req; /* page-table row pitch, >= ceil(max_seqlen / P)                 */
   int32_t mask_pitch;        /* Kmax: mask row pitch (entries per query block)                */
   int32_t budget_ppm;        /* stage-1 fraction B1 in parts per million, 1..1000000:
-                                K_i = ceil(B1 * (i + 1)), i the query block (0-based)          */
+                                K_i = ceil(B1 * (i + 1)), i the query block (0-based); with
+                                COSA_FLAG_TOP_P the top-p threshold p instead                   */
   int32_t flags;             /* COSA_FLAG_*                                                   */
   double sm_scale;           /* logit scale, normally 1/sqrt(d)                                */
   double skip_delta;         /* Delta of the skip threshold ln(Delta / L_b); <= 0 disables
@@ -127,8 +134,9 @@ const char* cosa_status_string(int status);
  *   q, cu_seqlens, k_cache, page_table   inputs as above (V is not read)
  *   mask       out: for every request b, head h and query block i < ceil(L_b / b):
  *              mask[b,h,i,0:K_i] = the ordered block IDs, mask[b,h,i,K_i:mask_pitch] = -1,
- *              with K_i = ceil(budget_ppm * (i+1) / 1e6).  Rows of absent query blocks
- *              (i >= ceil(L_b / b)) are set to -1.  Requires mask_pitch >= K_i for all i.
+ *              with K_i = ceil(budget_ppm * (i+1) / 1e6), or the top-p length (COSA_FLAG_TOP_P).
+ *              Rows of absent query blocks (i >= ceil(L_b / b)) are set to -1.  Requires
+ *              mask_pitch >= K_i for all i.
  *   mask_len   out: K_i per row (0 for absent query blocks).
  *   workspace  scratch of at least cosa_proxy_workspace_size(p) bytes (256-byte aligned);
  *              its content on entry does not matter and is undefined on exit.
@@ -136,7 +144,9 @@ const char* cosa_status_string(int status);
  * Selections are exact: the fp32 tensor-core scores carry error bounds, and every
  * order or cut they cannot certify is settled with float64 logits, so the mask equals
  * the one computed from exact real-number scores except where two scores agree to
- * within float64 rounding.  Stride sampling keeps token positions 0, s, 2s, ...;
+ * within float64 rounding.  The top-p length is the exception: it is decided on the fp32
+ * scores, so it can differ from the exact one where the prefix mass is within the scores'
+ * error of p times the total.  Stride sampling keeps token positions 0, s, 2s, ...;
  * ties in score go to the lower block ID.
  */
 size_t cosa_proxy_workspace_size(const cosa_params* p);

@@ -25,6 +25,7 @@ Readings taken where the pages are silent (each is listed in the design doc):
   * ties in Eq. (13) are broken by ascending block index, inside each group;
   * candidates of query block i are the blocks j <= i (Algorithm A line 5);
   * the stage-1 budget is a fraction: K_i = ceil(budget_ppm * J_i / 1e6), J_i = i + 1;
+    with top-p, K_i is the shortest prefix of rho_i whose scores reach p of the row's total;
   * the skip threshold uses the request's own length: ln(delta / L); delta <= 0
     disables the skip (paper App. D.1: delta = -1 is the stage-1-only endpoint);
   * a row with no visible key in a visited block votes "skip" for that block;
@@ -59,6 +60,7 @@ class Params:
     budget_ppm: int           # stage-1 fraction in parts per million
     sm_scale: float           # 1/sqrt(d)
     skip_delta: float         # Delta; <= 0 disables the in-kernel skip
+    top_p: bool = False       # budget_ppm holds the top-p threshold p instead of the fraction
 
 
 def request_keys(cache_bits: np.ndarray, page_table_row: np.ndarray, L: int, P: int, kv_head: int):
@@ -123,6 +125,15 @@ def stage1_count(budget_ppm: int, J: int) -> int:
     return max(1, min(J, -(-budget_ppm * J // 1_000_000)))
 
 
+def stage1_count_top_p(scores: np.ndarray, order: np.ndarray, p_ppm: int) -> int:
+    """Top-p stage-1 length (Sec. 4.2 "Top-p selection", Sec. 5.1, App. D.1): the shortest prefix of
+    rho_i whose scores s_ij reach p = p_ppm / 1e6 of the total over the causal candidates, summed in
+    rho_i order; at least 1."""
+    csum = np.cumsum(scores[order])                 # sequential, in visiting order
+    thr = (p_ppm / 1e6) * csum[-1]
+    return int(np.argmax(csum >= thr)) + 1
+
+
 def kap_sampled(Q: np.ndarray, K: np.ndarray, exists: np.ndarray, s: int):
     """Stride downsampling (Sec. 4.2): sampled query rows and keys at positions 0, s, 2s, ..."""
     pos = np.arange(0, Q.shape[0], s)
@@ -185,7 +196,8 @@ def kap_request_head(Q: np.ndarray, K: np.ndarray, exists: np.ndarray, prm: Para
             scores = scores + pbar[r]
         hrm = (pbar == 1.0).any(axis=0) if pbar.shape[0] else np.zeros(J, dtype=bool)   # Eq. (12)
         order = flag_grouped_order(scores, hrm)                             # Eq. (13)
-        out[i] = KapRow(scores=scores, hrm=hrm, order=order, K=stage1_count(prm.budget_ppm, J), pbar=pbar)
+        K = stage1_count_top_p(scores, order, prm.budget_ppm) if prm.top_p else stage1_count(prm.budget_ppm, J)
+        out[i] = KapRow(scores=scores, hrm=hrm, order=order, K=K, pbar=pbar)
     return out
 
 

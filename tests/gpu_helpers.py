@@ -178,6 +178,33 @@ def assert_osk_ok(rep: OskReport):
     assert rep.max_disagree_margin <= SKIP_MARGIN_TOL, rep
 
 
+# top-p: the kernel takes the cut on fp32 scores; a cut that differs from the oracle's is accepted
+# only where the oracle's prefix mass is within this fraction of the total from p times the total
+TOP_P_RTOL = 1e-3
+
+
+def compare_masks_top_p(mask_gpu, len_gpu, rows: Dict, p_ppm: int) -> Tuple[List, List]:
+    """Top-p masks: the GPU row must be a prefix of the oracle's rho_i (float64 ties accepted as in
+    compare_masks) whose length is the oracle's K_i, or differs from it only across cuts the fp32
+    scores cannot tell apart (oracle prefix mass within TOP_P_RTOL * total of p * total).
+    Returns (accepted cut differences, accepted ties)."""
+    cuts, ties = [], []
+    p = p_ppm / 1e6
+    for key, row in rows.items():
+        b, h, i = key
+        kg, ko = int(len_gpu[b, h, i]), row.K
+        assert 1 <= kg <= i + 1, (key, kg)
+        if kg != ko:
+            csum = np.cumsum(row.scores[row.order])
+            T = csum[-1]
+            for k in range(min(kg, ko), max(kg, ko)):
+                assert abs(csum[k - 1] - p * T) <= TOP_P_RTOL * T, (key, kg, ko, k, csum[k - 1] / T)
+            cuts.append((key, kg, ko))
+        sub = type(row)(scores=row.scores, hrm=row.hrm, order=row.order, K=kg, pbar=row.pbar)
+        ties += compare_masks_rows(mask_gpu, len_gpu, {key: sub})
+    return cuts, ties
+
+
 def compare_masks_rows(mask_gpu, len_gpu, rows: Dict) -> List:
     """compare_masks restricted to the oracle's rows (no check of absent query blocks)."""
     return compare_masks(mask_gpu, len_gpu, rows, None, None)

@@ -405,6 +405,52 @@ def check_kap_mask_layout(orc):
     assert (ml[1, :, nqb1:] == 0).all() and (mask[1, :, nqb1:] == -1).all()
 
 
+def check_top_p_count(orc):
+    e = math.exp
+
+    def hand(k_vals, ppm):
+        q, kc, _ = hand_problem(k_vals, [0] * 6, [1.0] * 6, 6)
+        kc = kc.reshape(3, 2, 1, 1)
+        prm = orc.Params(2, 2, 1, ppm, 1.0, -1.0, top_p=True)
+        from oracle import cosa_oracle as base
+        K, ex = base.request_keys(kc, np.arange(3), 6, 2, 0)
+        return orc.kap_request_head(f64(q[:, 0, :]), K, ex, prm, [2])[2]
+
+    # scores [2/e, 2, e^-3 + e^-2], rho = [1, 0, 2], total T = 2.92088...
+    T = 2 * e(-1) + 2 + e(-3) + e(-2)
+    for ppm, want in ((500_000, 1), (900_000, 2), (950_000, 3), (1_000_000, 3), (1, 1)):
+        assert hand([2, 0, 1, 3, 0, 1], ppm).K == want, (ppm, want)
+    assert 2 < 0.9 * T <= 2 + 2 * e(-1) < 0.95 * T            # the closed form behind 2 and 3
+    # HRM first: scores [1 + e^-0.5, e^-0.25 + e^-0.75, e^-4 + 1], rho = [0, 2, 1].  At p = 0.7 the
+    # prefix {0, 2} holds 2.62 < 0.7 T = 2.71, so K = 3 (a score-ordered prefix {0, 1} would stop at 2)
+    row = hand([4, 0, 3.75, 0, 0, 4.5], 700_000)
+    assert list(row.order) == [0, 2, 1] and row.K == 3
+    assert hand([4, 0, 3.75, 0, 0, 4.5], 600_000).K == 2
+    # seeded batch: K_i is the shortest rho_i prefix reaching p T (plain loop), and grows with p
+    spec = tiny_spec(seed=68)
+    w = synth.make_workload(spec)
+    prev = None
+    for ppm in (300_000, 800_000, 950_000):
+        prm = orc.Params(spec.block_size, spec.page_size, spec.stride, ppm, 1.0 / math.sqrt(spec.head_dim),
+                         -1.0, top_p=True)
+        _, ml, rows = orc.kap_mask(w.q, w.k_cache, w.page_table, w.cu_seqlens, spec.num_q_heads,
+                                   spec.num_kv_heads, prm, 64)
+        for key, r in rows.items():
+            tot = 0.0
+            for j in range(len(r.scores)):
+                tot += r.scores[r.order[j]]
+            run, k = 0.0, 0
+            while True:
+                run += r.scores[r.order[k]]
+                k += 1
+                if run >= ppm / 1e6 * tot:
+                    break
+            assert r.K == k == ml[key], (key, r.K, k)
+        if prev is not None:
+            assert (ml >= prev).all()
+        prev = ml
+
+
 # --------------------------------------------------------------------------- #
 # ablation modes: ascending-order visiting (no remap) and binary-mask visiting
 # --------------------------------------------------------------------------- #
@@ -492,5 +538,5 @@ ALL_CHECKS = [
     check_token_set_worked_example, check_dense_reduction, check_order_invariance,
     check_direct_definition, check_skip_hand_cases, check_skip_bucket_case, check_skip_invariants,
     check_stage1_count, check_kap_hand_cases, check_kap_brute_force, check_kap_invariants,
-    check_kap_mask_layout, check_ascending_mask, check_binary_mask_visiting,
+    check_kap_mask_layout, check_ascending_mask, check_binary_mask_visiting, check_top_p_count,
 ]

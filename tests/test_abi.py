@@ -87,6 +87,7 @@ def test_host_validation(lib):
     assert osk(_params(lib), q=None) == lib.COSA_ERR_INVALID_ARG
     assert osk(_params(lib, flags=1 << 5)) == lib.COSA_ERR_INVALID_ARG      # unknown flag bit
     assert kap(_params(lib, flags=1 << 5)) == lib.COSA_ERR_INVALID_ARG
+    assert kap(_params(lib, flags=lib.COSA_FLAG_TOP_P, mask_pitch=7)) == lib.COSA_ERR_INVALID_ARG   # K_i up to 8
     assert osk(_params(lib, total_tokens=0)) == lib.COSA_OK                 # nothing to do
 
 

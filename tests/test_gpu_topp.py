@@ -1,0 +1,75 @@
+"""Top-p stage-1 budget (COSA_FLAG_TOP_P) on the GPU against the float64 oracle: K_i is the shortest
+prefix of rho_i (Eq. (13)) whose block scores (Eq. (11)) reach p of the row's total (CoSA Sec. 4.2,
+Sec. 5.1 and App. D.1, p = 0.95).  The order is exact as for the fraction rule; the cut is taken on the
+kernel's fp32 scores and may differ from the oracle's only where the prefix mass is within 1e-3 of
+the total from p times the total."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import synth
+from oracle import cosa_oracle as orc
+from tests import gpu_helpers as gh
+from tests.test_gpu_osk import SMALL, small_spec
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "delta_calibration.json")
+
+
+def _run(w, ppm, delta=-1.0, items=None):
+    sp = w.spec
+    nqb = -(-sp.max_seqlen // sp.block_size)
+    dw = gh.to_device(w)
+    p = gh.cosa_params(dw, delta=delta, mask_pitch=nqb, budget_ppm=ppm)
+    p.flags = gh.C.COSA_FLAG_TOP_P
+    mask_g, len_g = gh.run_kap(dw, p)
+    prm = gh.oracle_params(sp, delta, budget_ppm=ppm)
+    prm.top_p = True
+    by = None
+    if items is not None:
+        by = {}
+        for (b, h, i) in items:
+            by.setdefault((b, h), []).append(i)
+    _, len_o, rows = orc.kap_mask(w.q, w.k_cache, w.page_table, w.cu_seqlens, sp.num_q_heads, sp.num_kv_heads,
+                                  prm, nqb, qblocks=by)
+    cuts, ties = gh.compare_masks_top_p(mask_g, len_g, rows, ppm)
+    return dw, p, prm, mask_g, len_g, rows, cuts
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+@pytest.mark.parametrize("ppm", [500_000, 950_000])
+def test_top_p_small(name, ppm):
+    if SMALL[name]["block_size"] // SMALL[name]["stride"] not in (4, 8, 16):
+        pytest.skip("stride ratio not supported")
+    w = synth.make_workload(small_spec(name, seed=600 + len(name)))
+    _, _, _, mask_g, len_g, rows, cuts = _run(w, ppm)
+    assert len(cuts) <= max(1, len(rows) // 100), cuts
+    sp = w.spec
+    for b, L in enumerate(sp.lengths):
+        nqb = -(-L // sp.block_size)
+        assert (len_g[b, :, nqb:] == 0).all() and (mask_g[b, :, nqb:] == -1).all()
+
+
+def test_top_p_full_pipeline_config3():
+    """32K tokens, 32 heads, p = 0.95 and the workload's Delta: KAP + OSK through the C ABI, the oracle
+    on sampled (head, query block) items."""
+    from tests.test_gpu_full import sampled_items
+    sp = synth.spec_for(3)
+    delta = json.load(open(GOLDEN))["configs"]["3"]["delta"]
+    w = synth.make_workload(sp)
+    items = sampled_items(sp, 24, seed=95)
+    dw, p, prm, mask_g, len_g, rows, cuts = _run(w, 950_000, delta=delta, items=items)
+    assert len(cuts) <= 1, cuts
+    # realised stage-1 budget of the rule on this input, for the record
+    nqb = mask_g.shape[2]
+    frac = len_g.sum() / (sp.num_q_heads * nqb * (nqb + 1) / 2)
+    assert 0.0 < frac <= 1.0
+    out, flags = gh.run_osk(dw, p, mask_g, len_g)
+    exact = [it for it in items if not any(c[0] == it for c in cuts)]
+    mask_o = mask_g.copy()
+    rep = gh.compare_osk(w, prm, mask_o, len_g, out, flags, exact)
+    gh.assert_osk_ok(rep)
+    print(f"top-p 0.95 on {sp.name}: realised stage-1 budget {frac:.3f}, cut differences {len(cuts)}")

@@ -55,6 +55,10 @@ MUTATIONS = {
     "binary_flags_by_visit": ("flags[j] = r.flags[x]", "flags[x] = r.flags[x]"),
     "binary_walk_includes_diagonal_only": ("walk = min(n, i + 1)", "walk = min(n, i)"),
     "binary_mask_keeps_future": ("if 0 <= j <= i:", "if 0 <= j:"),
+    # top-p stage-1 length
+    "top_p_strict": ("return int(np.argmax(csum >= thr)) + 1", "return int(np.argmax(csum > thr)) + 1"),
+    "top_p_score_order": ("csum = np.cumsum(scores[order])", "csum = np.cumsum(np.sort(scores)[::-1])"),
+    "top_p_off_by_one": ("return int(np.argmax(csum >= thr)) + 1", "return max(1, int(np.argmax(csum >= thr)))"),
 }
 
 
