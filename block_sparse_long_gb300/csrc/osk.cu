@@ -78,7 +78,7 @@ struct alignas(1024) OskSmem {
   uint64_t cleanup;
   KInfo info[8];                              // visit info of visit v (slot v & 7), written with K(v)
   KInfo vreq[4];
-  float pmax[2][128];                         // partial row maxima of the two column halves
+  float pmax[2][2][128];                      // partial row maxima [visit & 1][column half][row]
   float lsum[2][128];                         // partial row sums, exchanged at the end
   int32_t pv_cmd[4];                          // per computed visit c: 2 = first of its item, 1 = accumulate, 0 = end
   uint32_t tmem_base;
@@ -564,8 +564,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             pm = fmax3f(fmax3f(m8[0], m8[1], m8[2]), fmax3f(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
           }
         }
-        // end of the item or a wait that ran out: every softmax warp learns it at the same barrier
-        if (named_bar_red_or(1, kSoftmaxThreads, !okw || ki_blk < 0)) {
+        // skip vote (Eq. (5)).  A row wants the block iff m_loc - max(m_run, m_loc) >= tau2; that
+        // test is monotone in m_loc, so it holds for the row iff it holds for one of the two
+        // column halves' partial maxima, and the block is computed iff some half of some row wants it.
+        const float p_loc = (pm == -INFINITY) ? -INFINITY : pm * sl2;
+        bool want = true;
+        if (use_skip) want = row_valid && (p_loc != -INFINITY) && (p_loc - fmaxf(m_run, p_loc) >= tau2);
+        // The partial row maxima go to shared memory before the vote (double-buffered by visit) and
+        // are read after it.  First barrier: some row wants the block, or the visit ends the item,
+        // or a wait ran out (all warps whose waits succeed see the same visit record); only then
+        // a second barrier tells these apart, so a skipped block costs one barrier.
+        sm.pmax[v & 1][g][t] = pm;
+        const bool stop = !okw || (ki_blk < 0);
+        bool compute = named_bar_red_or(2, kSoftmaxThreads, want || stop);
+        if (compute && named_bar_red_or(1, kSoftmaxThreads, stop)) {
           if (named_bar_red_or(2, kSoftmaxThreads, !okw)) ok = false;
           if (BIN && ok && ki_blk == -2) continue;   // a block the binary mask drops
           if (ok) {
@@ -583,19 +595,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           v += 2;
           break;
         }
-        // skip vote (Eq. (5)).  A row wants the block iff m_loc - max(m_run, m_loc) >= tau2; that
-        // test is monotone in m_loc, so it holds for the row iff it holds for one of the two
-        // column halves' partial maxima, and the block is computed iff some half of some row wants it.
-        const float p_loc = (pm == -INFINITY) ? -INFINITY : pm * sl2;
-        bool want = true;
-        if (use_skip) want = row_valid && (p_loc != -INFINITY) && (p_loc - fmaxf(m_run, p_loc) >= tau2);
-        const bool compute = named_bar_red_or(2, kSoftmaxThreads, want);
         // a skipped block leaves every row's running max unchanged (m_loc < m_run + tau2 <= m_run)
         float m_new = m_run;
         if (compute) {
-          sm.pmax[g][t] = pm;
-          named_bar_sync(3, kSoftmaxThreads);
-          const float mx = fmaxf(sm.pmax[0][t], sm.pmax[1][t]);
+          const float mx = fmaxf(sm.pmax[v & 1][0][t], sm.pmax[v & 1][1][t]);
           const float m_loc = (mx == -INFINITY) ? -INFINITY : mx * sl2;
           m_new = fmaxf(m_run, m_loc);
         }
