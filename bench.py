@@ -494,6 +494,49 @@ def run_sweep(args):
     return 0
 
 
+def group_loads(orders):
+    """Loads of a traversal shared by a GQA group whose heads keep their own visiting orders: each
+    load serves every head whose next pending block it is; greedily the block next for the most
+    heads (ties: lowest ID).  Returns (sum of |S_i|, |U_G|, shared loads)."""
+    seqs = [list(dict.fromkeys(int(x) for x in o)) for o in orders]
+    n_sel = sum(len(q) for q in seqs)
+    n_union = len(set(x for q in seqs for x in q))
+    pos = [0] * len(seqs)
+    loads = 0
+    while True:
+        cand = {}
+        for p_, q in zip(pos, seqs):
+            if p_ < len(q):
+                cand[q[p_]] = cand.get(q[p_], 0) + 1
+        if not cand:
+            break
+        blk = min(cand, key=lambda b: (-cand[b], b))
+        for h, q in enumerate(seqs):
+            if pos[h] < len(q) and q[pos[h]] == blk:
+                pos[h] += 1
+        loads += 1
+    return n_sel, n_union, loads
+
+
+def union_stats(mask: np.ndarray, mask_len: np.ndarray, group: int):
+    """PageWeaver's page reuse rate over the GQA groups (q heads sharing a kv head, same query block):
+    rho_Q = sum |S_i| / sum |U_G|, and the same with order-preserving shared loads."""
+    B, H, nqb, _ = mask.shape
+    tot_sel = tot_union = tot_loads = 0
+    for b in range(B):
+        for g0 in range(0, H, group):
+            for i in range(nqb):
+                rows = [mask[b, h, i, :mask_len[b, h, i]] for h in range(g0, g0 + group)]
+                if not any(len(r) for r in rows):
+                    continue
+                s_, u_, l_ = group_loads(rows)
+                tot_sel += s_
+                tot_union += u_
+                tot_loads += l_
+    return {"selections": tot_sel, "union_blocks": tot_union, "ordered_loads": tot_loads,
+            "rho_Q": tot_sel / max(1, tot_union), "rho_ordered": tot_sel / max(1, tot_loads)}
+
+
 def run_ablation(args):
     """Kernel-side ablations on synthetic data (one JSON line per point, not the bench line).
 
@@ -507,6 +550,8 @@ def run_ablation(args):
       order; each against the dense endpoint of the same kernel: the analogue of CoSA Fig. B.
     topp: the top-p stage-1 rule (p in {0.8, 0.9, 0.95, 0.99}; the paper runs Qwen at 0.95): realised
       stage-1 budget, KAP time, and OSK time with skipping off and at the workload's Delta.
+    union: PageWeaver's page reuse rate rho_Q of the GQA groups on the KAP masks, with and without
+      keeping each head's visiting order (the bound on what a shared K/V traversal could save).
     Inputs have the 128K workload's structure at the given length."""
     import torch
     from block_sparse_long_gb300 import cosa as C
@@ -557,6 +602,21 @@ def run_ablation(args):
         l01 = torch.where(ml > 0, torch.arange(1, nqb + 1, dtype=torch.int32, device=dev)[None, None, :], 0)
         return m01[..., :nqb].contiguous(), l01.to(torch.int32).contiguous()
 
+    if args.ablation == "union":
+        for cfg in (3, 4):
+            spec = synth.spec_for(cfg)
+            w = synth.make_workload(spec)
+            t = dict(q=bf(w.q), k=bf(w.k_cache), pt=torch.from_numpy(w.page_table).to(dev),
+                     cu=torch.from_numpy(w.cu_seqlens).to(dev))
+            group = spec.num_q_heads // spec.num_kv_heads
+            for flags, order in ((0, "rho"), (C.COSA_FLAG_ASCENDING_ORDER, "ascending")):
+                mask, ml, _ = kap(spec, t, spec.budget_ppm, flags)
+                st = union_stats(mask.cpu().numpy(), ml.cpu().numpy(), group)
+                print(json.dumps({"ablation": "union", "workload": spec.name, "group": group, "order": order,
+                                  "stage1_budget": spec.budget_ppm / 1e6, **st}), flush=True)
+            del t
+            torch.cuda.empty_cache()
+        return 0
     if args.ablation == "topp":
         n_tok = args.ablation_tokens
         spec, t = setup(n_tok)
@@ -650,9 +710,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true",
                     help="time CoSA against the dense endpoint of the same kernel from 4K to 128K tokens")
-    ap.add_argument("--ablation", choices=["remap", "jump", "topp"],
+    ap.add_argument("--ablation", choices=["remap", "jump", "topp", "union"],
                     help="remap: skip ratio vs Delta with and without remapping over stage-1 budgets; "
-                         "jump: physical jumps vs logical skipping of a binary mask; topp: the top-p stage-1 rule")
+                         "jump: physical jumps vs logical skipping of a binary mask; topp: the top-p stage-1 rule; "
+                         "union: GQA page reuse rates")
     ap.add_argument("--ablation-tokens", type=int, default=131072, help="context length of --ablation remap/topp")
     args = ap.parse_args()
     if args.sweep:

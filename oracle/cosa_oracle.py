@@ -384,6 +384,44 @@ def osk_all(q_bits, k_bits, v_bits, page_table, cu_seqlens, num_q_heads, num_kv_
     return res
 
 
+def query_union(sets: Sequence[Sequence[int]]) -> Tuple[List[int], np.ndarray]:
+    """PageWeaver Sec. 2.2: the group's shared traversal U_G (ascending) and the membership mask
+    M[i, p] = 1 if the p-th page of U_G is in S_i."""
+    U = sorted(set(int(x) for S in sets for x in S))
+    M = np.array([[1 if u in set(int(x) for x in S) else 0 for u in U] for S in sets], dtype=np.int8)
+    return U, M
+
+
+def reuse_rate(groups: Sequence[Sequence[Sequence[int]]]) -> float:
+    """PageWeaver's logical page reuse rate rho_Q = sum_i |S_i| / sum_G |U_G| over groups of sets
+    (duplicates within a set count once)."""
+    num = sum(len(set(int(x) for x in S)) for G in groups for S in G)
+    den = sum(len(query_union(G)[0]) for G in groups)
+    return num / den if den else 0.0
+
+
+def ordered_shared_loads(orders: Sequence[Sequence[int]]) -> int:
+    """Loads of a traversal shared by a group of heads that each keep their own visiting order (the
+    GQA union for CoSA's ordered visits): each load serves every head whose next pending block it
+    is.  Greedy: load the block that is next for the most heads (ties: lowest block ID).  An upper
+    bound on the shortest common supersequence of the orders; equal to sum |S_i| when no two heads
+    ever wait for the same block, and to |U_G| when all heads share one order."""
+    seqs = [list(dict.fromkeys(int(x) for x in o)) for o in orders]   # first occurrence of each ID
+    pos = [0] * len(seqs)
+    loads = 0
+    while any(p < len(q) for p, q in zip(pos, seqs)):
+        cand = {}
+        for p, q in zip(pos, seqs):
+            if p < len(q):
+                cand[q[p]] = cand.get(q[p], 0) + 1
+        blk = min(cand, key=lambda b: (-cand[b], b))
+        for h, q in enumerate(seqs):
+            if pos[h] < len(q) and q[pos[h]] == blk:
+                pos[h] += 1
+        loads += 1
+    return loads
+
+
 def realized_budget(results: dict, lengths: Sequence[int], b: int, num_heads: int,
                     items: Optional[Sequence[Tuple[int, int, int]]] = None) -> float:
     """Computed blocks over causal candidate blocks (sum of J_i = i + 1) for the given items."""

@@ -451,6 +451,27 @@ def check_top_p_count(orc):
         prev = ml
 
 
+def check_query_union(orc):
+    g = json.load(open(os.path.join(GOLDEN, "pageweaver_union.json")))
+    U, M = orc.query_union(g["S"])
+    assert U == g["U"]
+    assert M.tolist() == [[1, 1, 1, 0], [1, 1, 0, 1]]        # q0 skips page 9, q2 skips page 7
+    assert orc.reuse_rate([g["S"]]) == g["rho_Q"]
+    assert orc.reuse_rate([[[3, 3, 5]], [[5]]]) == 1.0         # singletons: no reuse; repeats count once
+    # ordered sharing: one common order loads |U| blocks; disjoint sets load sum |S_i|; reversed orders
+    # of the same set force a load per head and block except where both wait for the same one
+    assert orc.ordered_shared_loads([[1, 4, 7], [1, 4, 7]]) == 3
+    assert orc.ordered_shared_loads([[1, 2], [3, 4]]) == 4
+    assert orc.ordered_shared_loads([[1, 4, 7], [1, 4, 9]]) == 4
+    assert orc.ordered_shared_loads([[1, 2, 3], [3, 2, 1]]) == 5  # 1|3, then 2 for both, then 3|1
+    assert orc.ordered_shared_loads([[5, 5, 2], [2]]) == 3     # repeats count once; greedy takes 2 first (5, 2 would do)
+    rng = np.random.default_rng(4)
+    for _ in range(50):
+        G = [list(rng.choice(20, size=int(rng.integers(0, 8)), replace=False)) for _ in range(4)]
+        n = orc.ordered_shared_loads(G)
+        assert len(orc.query_union(G)[0]) <= n <= sum(len(S) for S in G)
+
+
 # --------------------------------------------------------------------------- #
 # ablation modes: ascending-order visiting (no remap) and binary-mask visiting
 # --------------------------------------------------------------------------- #
@@ -539,4 +560,5 @@ ALL_CHECKS = [
     check_direct_definition, check_skip_hand_cases, check_skip_bucket_case, check_skip_invariants,
     check_stage1_count, check_kap_hand_cases, check_kap_brute_force, check_kap_invariants,
     check_kap_mask_layout, check_ascending_mask, check_binary_mask_visiting, check_top_p_count,
+    check_query_union,
 ]

@@ -59,6 +59,10 @@ MUTATIONS = {
     "top_p_strict": ("return int(np.argmax(csum >= thr)) + 1", "return int(np.argmax(csum > thr)) + 1"),
     "top_p_score_order": ("csum = np.cumsum(scores[order])", "csum = np.cumsum(np.sort(scores)[::-1])"),
     "top_p_off_by_one": ("return int(np.argmax(csum >= thr)) + 1", "return max(1, int(np.argmax(csum >= thr)))"),
+    # PageWeaver union and reuse rate
+    "reuse_rate_counts_repeats": ("num = sum(len(set(int(x) for x in S)) for G in groups for S in G)",
+                                  "num = sum(len(S) for G in groups for S in G)"),
+    "shared_load_serves_one_head": ("                pos[h] += 1\n", "                pos[h] += 1\n                break\n"),
 }
 
 
