@@ -937,6 +937,7 @@ __global__ void __launch_bounds__(kSelectThreads, 3) kap_select_kernel(KapArgs a
   const int i = a.nqb_max - 1 - idx / a.num_reqs;
   const ReqInfo ri = req_info(a, b);
   const size_t mrow = (static_cast<size_t>(b) * a.num_q_heads + h) * a.nqb_max + i;
+  if (a.mask_len[mrow] != -1) return;   // settled by kap_select_warp_kernel
   int32_t* out = a.mask + mrow * a.mask_pitch;
   if (i >= ri.nqb) {
     for (int k = tid; k < a.mask_pitch; k += blockDim.x) out[k] = -1;
@@ -1277,6 +1278,443 @@ __global__ void __launch_bounds__(kSelectThreads, 3) kap_select_kernel(KapArgs a
   if (tid == 0) a.mask_len[mrow] = K;
 }
 
+
+// ---------------------------------------------------------------------------
+// The same selection, one warp per mask row, for the common rows: fraction budget, J <= 1024,
+// K <= 128 and K < J.  The K largest keys are found by radix select, sorted, certified against one
+// sentinel standing for every unselected key (as in kap_select_kernel's top-K path) and up to
+// kWarpRepMax uncertain positions are repaired in float64.  Every other row (and a row whose cut
+// the sentinel cannot certify) is left to kap_select_kernel, marked by mask_len = -1.
+// ---------------------------------------------------------------------------
+constexpr int kWarpSelMaxJ = 1024;
+constexpr int kWarpSelMaxK = 128;
+constexpr int kWarpRepMax = 16;
+constexpr int kWarpSelWarps = 4;
+
+struct WarpSelSmem {
+  unsigned long long key[kWarpSelMaxK];   // selected keys, sorted descending
+  double rep_val[kWarpRepMax];
+  double terms[kWarpRepMax * 16];         // (repaired position, sampled row) exponents, then terms
+  uint32_t hist[256];
+  int32_t rep_pos[kWarpRepMax];
+  uint8_t hrm[kWarpSelMaxJ];
+};
+
+// bitonic sort (descending) of 32 * E keys held E per lane, lane l holding positions l*E .. l*E+E-1
+template <int E>
+__device__ __forceinline__ void warp_sort_desc(unsigned long long (&v)[E], int lane) {
+#pragma unroll 1
+  for (int k = 2; k <= 32 * E; k <<= 1) {
+#pragma unroll 1
+    for (int jj = k >> 1; jj > 0; jj >>= 1) {
+      if (jj < E) {
+        if (jj == 1) sort_stage_reg<1, E>(v, k, lane);
+        else if constexpr (E > 2) {
+          if (jj == 2) sort_stage_reg<2, E>(v, k, lane);
+        }
+      } else {
+        const int ld = jj / E;
+        const bool lower = (lane & ld) == 0;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const unsigned long long o = __shfl_xor_sync(0xffffffffu, v[e], ld);
+          const bool desc = ((lane * E + e) & k) == 0;
+          const bool take_max = (lower == desc);
+          v[e] = take_max ? (v[e] > o ? v[e] : o) : (v[e] < o ? v[e] : o);
+        }
+      }
+    }
+  }
+}
+
+template <int E>
+__device__ __forceinline__ void warp_sort_keys(unsigned long long* key, int K, int lane) {
+  unsigned long long v[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) v[e] = (lane * E + e < K) ? key[lane * E + e] : 0ull;
+  __syncwarp();
+  warp_sort_desc<E>(v, lane);
+#pragma unroll
+  for (int e = 0; e < E; ++e) key[lane * E + e] = v[e];
+  __syncwarp();
+}
+
+__device__ __forceinline__ float warp_max_f(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+
+__device__ __forceinline__ int warp_min_i(int x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = min(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+
+// exclusive prefix sum over the lanes
+__device__ __forceinline__ int warp_excl_sum(int x, int lane) {
+  int incl = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  return incl - x;
+}
+
+template <int HD, int KB>
+__global__ void __launch_bounds__(kWarpSelWarps * 32, 4) kap_select_warp_kernel(KapArgs a) {
+  __shared__ WarpSelSmem wsm[kWarpSelWarps];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  WarpSelSmem& sm = wsm[w];
+  const long long nrow_all = static_cast<long long>(a.num_reqs) * a.num_q_heads * a.nqb_max;
+  long long idx = static_cast<long long>(blockIdx.x) * kWarpSelWarps + w;
+  if (idx >= nrow_all) return;
+  // the row order of kap_select_kernel: heads fastest, then requests, heaviest query blocks first
+  const int h = static_cast<int>(idx % a.num_q_heads);
+  idx /= a.num_q_heads;
+  const int b = static_cast<int>(idx % a.num_reqs);
+  const int i = a.nqb_max - 1 - static_cast<int>(idx / a.num_reqs);
+  const ReqInfo ri = req_info(a, b);
+  const size_t mrow = (static_cast<size_t>(b) * a.num_q_heads + h) * a.nqb_max + i;
+  int32_t* out = a.mask + mrow * a.mask_pitch;
+  if (i >= ri.nqb) {
+    for (int k = lane; k < a.mask_pitch; k += 32) out[k] = -1;
+    if (lane == 0) a.mask_len[mrow] = 0;
+    return;
+  }
+  const int J = i + 1;
+  const int K = max(1, min(J, static_cast<int>((static_cast<long long>(a.budget_ppm) * J + 999999) / 1000000)));
+  if (a.top_p || a.ascending || J > kWarpSelMaxJ || K > kWarpSelMaxK || K >= J) {
+    if (lane == 0) a.mask_len[mrow] = -1;
+    return;
+  }
+  const int kvh = h / (a.num_q_heads / a.num_kv_heads);
+  const int nqb = ri.nqb;
+  const int64_t sbase = a.sc_off[b] + static_cast<int64_t>(h) * nqb * nqb + static_cast<int64_t>(i) * nqb;
+  const float* sc = a.score + sbase;
+  const float* se = a.score_err + sbase;
+  const int r0 = i * a.kb, r1 = min((i + 1) * a.kb, ri.R);
+  const int64_t rbase = a.row_off[b] + static_cast<int64_t>(h) * ri.R;
+
+  // HRM flags of the candidates (exact, from the float64 row maxima)
+  for (int j = lane; j < J; j += 32) sm.hrm[j] = 0;
+  __syncwarp();
+  if (lane < r1 - r0) {
+    const int r = r0 + lane;
+    const int fl = a.rflags[rbase + r];
+    if (fl & 1) {
+      const uint32_t* bits = a.hrm_bits + (rbase + r) * a.words_per_row;
+      for (int j = 0; j < J; ++j)
+        if ((bits[j >> 5] >> (j & 31)) & 1u) sm.hrm[j] = 1;
+    } else if (!(fl & 2)) {
+      sm.hrm[(a.c1[rbase + r] * a.stride) / a.block_size] = 1;
+    }
+  }
+  __syncwarp();
+  // lane l owns candidates j = l, l + 32, ...; their keys are rebuilt from the scores (cached) each pass
+  auto key_of = [&](int j) { return sort_key(sm.hrm[j] != 0, fmaxf(sc[j], 0.0f), j); };
+  int nh_part = 0;
+  for (int j = lane; j < J; j += 32) nh_part += sm.hrm[j] != 0 ? 1 : 0;
+  const int nh_all = __reduce_add_sync(0xffffffffu, nh_part);
+
+  // radix select of the K largest keys on 8-bit digits from the top
+  unsigned long long prefix = 0ull, pmask = 0ull;
+  int krem = K;
+#pragma unroll 1
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    for (int d = lane; d < 256; d += 32) sm.hist[d] = 0u;
+    __syncwarp();
+    for (int j = lane; j < J; j += 32) {
+      const unsigned long long kv = key_of(j);
+      if ((kv & pmask) == prefix) atomicAdd(&sm.hist[(kv >> shift) & 255u], 1u);
+    }
+    __syncwarp();
+    // lane l holds digits 255 - 8l .. 248 - 8l (highest first)
+    int cq[8], sum = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) { cq[q] = static_cast<int>(sm.hist[255 - 8 * lane - q]); sum += cq[q]; }
+    int run = warp_excl_sum(sum, lane);
+    int dg = -1, ab = 0, ct = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (run < krem && run + cq[q] >= krem) { dg = 255 - 8 * lane - q; ab = run; ct = cq[q]; }
+      run += cq[q];
+    }
+    const int src = __ffs(__ballot_sync(0xffffffffu, dg >= 0)) - 1;
+    dg = __shfl_sync(0xffffffffu, dg, src);
+    ab = __shfl_sync(0xffffffffu, ab, src);
+    ct = __shfl_sync(0xffffffffu, ct, src);
+    krem -= ab;
+    prefix |= static_cast<unsigned long long>(dg) << shift;
+    pmask |= 0xFFull << shift;
+    __syncwarp();
+    if (ct == krem) break;   // every key with this prefix is among the K
+  }
+  // compact the K winners; the largest upper bound of the unselected keys of each group
+  int cnt = 0;
+  float hiR = -INFINITY, hiH = -INFINITY;
+  for (int j = lane; j < J; j += 32) {
+    const unsigned long long kv = key_of(j);
+    if ((kv & pmask) >= prefix) {
+      ++cnt;
+    } else {
+      const float hv = fmaxf(sc[j], 0.0f) + se[j];
+      if (kv >> 63) hiH = fmaxf(hiH, hv);
+      else hiR = fmaxf(hiR, hv);
+    }
+  }
+  hiR = warp_max_f(hiR);
+  hiH = warp_max_f(hiH);
+  {
+    int pos = warp_excl_sum(cnt, lane);
+    for (int j = lane; j < J; j += 32) {
+      const unsigned long long kv = key_of(j);
+      if ((kv & pmask) >= prefix) sm.key[pos++] = kv;
+    }
+  }
+  __syncwarp();
+  if (K <= 32) warp_sort_keys<1>(sm.key, K, lane);
+  else if (K <= 64) warp_sort_keys<2>(sm.key, K, lane);
+  else warp_sort_keys<4>(sm.key, K, lane);
+
+  // certification over K + 1 positions: the K keys, then one sentinel with the unselected keys'
+  // largest upper bound (in the HRM group iff HRM keys were left out)
+  const int Jl = K + 1;
+  const int nh = (nh_all > K) ? K + 1 : nh_all;
+  const float sentinel_hi = (nh_all > K) ? hiH : hiR;
+  constexpr int E3 = (kWarpSelMaxK + 1 + 31) / 32;
+  float lo[E3], hi[E3];
+#pragma unroll
+  for (int e = 0; e < E3; ++e) {
+    const int p = lane * E3 + e;
+    if (p == K) {
+      lo[e] = -INFINITY;
+      hi[e] = sentinel_hi;
+    } else if (p < K) {
+      const int j = key_block(sm.key[p]);
+      const float s = fmaxf(sc[j], 0.0f);
+      const float er = se[j];
+      lo[e] = s - er;
+      hi[e] = s + er;
+    } else {
+      lo[e] = -INFINITY;
+      hi[e] = -INFINITY;
+    }
+  }
+  // within each group: suffix maximum of hi and prefix minimum of lo
+  float suf[E3], pre[E3];
+  {
+    float sH[E3], sR[E3], pH[E3], pR[E3];
+    float aH = -INFINITY, aR = -INFINITY;
+#pragma unroll
+    for (int e = E3 - 1; e >= 0; --e) {
+      const int p = lane * E3 + e;
+      aH = fmaxf(aH, p < nh ? hi[e] : -INFINITY);
+      aR = fmaxf(aR, p >= nh ? hi[e] : -INFINITY);
+      sH[e] = aH;
+      sR[e] = aR;
+    }
+    float bH = INFINITY, bR = INFINITY;
+#pragma unroll
+    for (int e = 0; e < E3; ++e) {
+      const int p = lane * E3 + e;
+      bH = fminf(bH, p < nh ? lo[e] : INFINITY);
+      bR = fminf(bR, p >= nh ? lo[e] : INFINITY);
+      pH[e] = bH;
+      pR[e] = bR;
+    }
+    // lanes after this one (suffix) and before it (prefix)
+    float xH = aH, xR = aR, yH = bH, yR = bR;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float tH = __shfl_down_sync(0xffffffffu, xH, o), tR = __shfl_down_sync(0xffffffffu, xR, o);
+      const float uH = __shfl_up_sync(0xffffffffu, yH, o), uR = __shfl_up_sync(0xffffffffu, yR, o);
+      if (lane + o < 32) { xH = fmaxf(xH, tH); xR = fmaxf(xR, tR); }
+      if (lane >= o) { yH = fminf(yH, uH); yR = fminf(yR, uR); }
+    }
+    float nxH = __shfl_down_sync(0xffffffffu, xH, 1), nxR = __shfl_down_sync(0xffffffffu, xR, 1);
+    float pvH = __shfl_up_sync(0xffffffffu, yH, 1), pvR = __shfl_up_sync(0xffffffffu, yR, 1);
+    if (lane == 31) { nxH = -INFINITY; nxR = -INFINITY; }
+    if (lane == 0) { pvH = INFINITY; pvR = INFINITY; }
+#pragma unroll
+    for (int e = 0; e < E3; ++e) {
+      const int p = lane * E3 + e;
+      suf[e] = (p < nh) ? fmaxf(sH[e], nxH) : fmaxf(sR[e], nxR);
+      pre[e] = (p < nh) ? fminf(pH[e], pvH) : fminf(pR[e], pvR);
+    }
+  }
+  // the cut after position p is certain iff everything up to p (in its group) stays above
+  // everything after it
+  bool cutf[E3];
+  {
+    const float suf_next_lane = __shfl_down_sync(0xffffffffu, suf[0], 1);
+#pragma unroll
+    for (int e = 0; e < E3; ++e) {
+      const int p = lane * E3 + e;
+      const int g1 = p < nh ? nh : Jl;
+      const float sn = (e + 1 < E3) ? suf[(e + 1 < E3) ? e + 1 : e] : suf_next_lane;
+      cutf[e] = (p < Jl) && ((p == g1 - 1) || (pre[e] > sn));
+    }
+  }
+  int cs0 = 0x7fffffff, cs1 = 0x7fffffff;
+#pragma unroll
+  for (int e = 0; e < E3; ++e) {
+    const int p = lane * E3 + e;
+    if (p >= Jl || !cutf[e]) continue;
+    const int g = p < nh ? 0 : 1;
+    const int g1 = g ? Jl : nh;
+    if (p >= min(K, g1) - 1) {
+      if (g) cs1 = min(cs1, p);
+      else cs0 = min(cs0, p);
+    }
+  }
+  cs0 = warp_min_i(cs0);
+  cs1 = warp_min_i(cs1);
+  // positions to repair: runs of two or more between certain cuts that start before the cut
+  bool mk[E3];
+  int nmk = 0;
+  bool sentinel_marked = false;
+  {
+    const bool prev_cut_lane = __shfl_up_sync(0xffffffffu, cutf[E3 - 1], 1);
+#pragma unroll
+    for (int e = 0; e < E3; ++e) {
+      const int x = lane * E3 + e;
+      mk[e] = false;
+      if (x >= Jl) continue;
+      const int g = x < nh ? 0 : 1;
+      const int g0 = g ? nh : 0, g1 = g ? Jl : nh;
+      const int kg = min(K, g1);
+      if (kg > g0) {
+        const bool prev_cut = (e > 0) ? cutf[(e > 0) ? e - 1 : 0] : prev_cut_lane;
+        const bool multi = !cutf[e] || (x > g0 && !prev_cut);
+        mk[e] = multi && (x < kg || x <= (g ? cs1 : cs0));
+      }
+      if (mk[e]) {
+        ++nmk;
+        if (x == K) sentinel_marked = true;
+      }
+    }
+  }
+  const int n_rep = __reduce_add_sync(0xffffffffu, nmk);
+  if (__any_sync(0xffffffffu, sentinel_marked) || n_rep > kWarpRepMax) {
+    if (lane == 0) a.mask_len[mrow] = -1;   // the CTA kernel takes this row
+    return;
+  }
+  if (n_rep > 0) {
+    {
+      int pos = warp_excl_sum(nmk, lane);
+#pragma unroll
+      for (int e = 0; e < E3; ++e)
+        if (mk[e]) sm.rep_pos[pos++] = lane * E3 + e;
+    }
+    __syncwarp();
+    // exact scores s_ij = sum over rows r (ascending) of exp(bm[r,j] - M_r) with float64 logits, as
+    // in kap_select_kernel: lane group kgrp holds key j*KB + kgrp, its LPK lanes split d
+    constexpr int LPK = 32 / KB;
+    constexpr int SL = HD / LPK;
+    const int kgrp = lane / LPK, sub = lane % LPK;
+    const int nrows = r1 - r0;
+    const int rp = (ri.R + kRowTile - 1) / kRowTile * kRowTile;
+    const uint16_t* qbase = a.qs + (a.qs_off[b] + static_cast<int64_t>(h) * rp) * HD;
+    const int64_t krow0 = a.ks_off[b] + static_cast<int64_t>(kvh) * rp;
+    const float scl = static_cast<float>(a.sm_scale);
+#pragma unroll 1
+    for (int item = 0; item < n_rep * nrows; ++item) {
+      const int m = item / nrows, r = r0 + item % nrows;
+      const int j = key_block(sm.key[sm.rep_pos[m]]);
+      const double Mr = a.M[rbase + r];
+      double term = -INFINITY;
+      if (Mr != -INFINITY) {
+        const int kc = j * KB + kgrp;
+        const bool vis = kc <= r && ((a.kvalid[(krow0 + kc) >> 5] >> ((krow0 + kc) & 31)) & 1u);
+        const uint16_t* qr = qbase + static_cast<int64_t>(r) * HD + sub * SL;
+        const uint16_t* kr = vis ? a.ks + (krow0 + kc) * HD + sub * SL : qr;
+        float p0 = 0.0f, p1 = 0.0f;
+#pragma unroll 1
+        for (int e = 0; e < SL; e += 8) {
+          float qv[8], kv[8];
+          load8_bf16(qr + e, qv);
+          load8_bf16(kr + e, kv);
+#pragma unroll
+          for (int q = 0; q < 8; q += 2) {
+            p0 = fmaf(qv[q], kv[q], p0);
+            p1 = fmaf(qv[q + 1], kv[q + 1], p1);
+          }
+        }
+        float part = p0 + p1;
+#pragma unroll
+        for (int o = LPK / 2; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        const float x = vis ? part * scl : -INFINITY;
+        float mx = x;
+#pragma unroll
+        for (int o = LPK; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (mx != -INFINITY) {
+          const bool cand = vis && x >= mx - 2.0f * a.err[rbase + r];
+          uint32_t cmask = __ballot_sync(0xffffffffu, cand && sub == 0);
+          double dv = -INFINITY;
+          const uint16_t* qrow = qbase + static_cast<int64_t>(r) * HD;
+          while (cmask) {
+            const int gk = (__ffs(cmask) - 1) / LPK;
+            cmask &= cmask - 1;
+            const uint16_t* krow = a.ks + (krow0 + j * KB + gk) * HD;
+            double dp = 0.0;
+#pragma unroll
+            for (int e = lane * (HD / 32); e < (lane + 1) * (HD / 32); e += 2) {
+              const uint32_t qw = *reinterpret_cast<const uint32_t*>(qrow + e);
+              const uint32_t kw = *reinterpret_cast<const uint32_t*>(krow + e);
+              dp += static_cast<double>(__uint_as_float(qw << 16) * __uint_as_float(kw << 16));
+              dp += static_cast<double>(__uint_as_float(qw & 0xffff0000u) * __uint_as_float(kw & 0xffff0000u));
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) dp += __shfl_xor_sync(0xffffffffu, dp, o);
+            dv = fmax(dv, dp * a.sm_scale);
+          }
+          term = dv - Mr;
+        }
+      }
+      if (lane == 0) sm.terms[item] = term;
+    }
+    __syncwarp();
+    for (int item = lane; item < n_rep * nrows; item += 32) sm.terms[item] = exp(sm.terms[item]);
+    __syncwarp();
+    if (lane < n_rep) {
+      double sum = 0.0;
+      for (int rr = 0; rr < nrows; ++rr) sum += sm.terms[lane * nrows + rr];
+      sm.rep_val[lane] = sum;
+    }
+    __syncwarp();
+    // re-sort the repaired runs by (exact score desc, block asc); a run never crosses the groups
+    if (lane == 0) {
+      int m0 = 0;
+      while (m0 < n_rep) {
+        int m1 = m0;
+        while (m1 + 1 < n_rep && sm.rep_pos[m1 + 1] == sm.rep_pos[m1] + 1 && sm.rep_pos[m1 + 1] != nh) ++m1;
+        for (int x = m0 + 1; x <= m1; ++x) {
+          const double vx = sm.rep_val[x];
+          const unsigned long long kx = sm.key[sm.rep_pos[x]];
+          int y = x - 1;
+          while (y >= m0) {
+            const double vy = sm.rep_val[y];
+            const unsigned long long ky = sm.key[sm.rep_pos[y]];
+            const bool before = (vx > vy) || (vx == vy && key_block(kx) < key_block(ky));
+            if (!before) break;
+            sm.rep_val[y + 1] = vy;
+            sm.key[sm.rep_pos[y + 1]] = ky;
+            --y;
+          }
+          sm.rep_val[y + 1] = vx;
+          sm.key[sm.rep_pos[y + 1]] = kx;
+        }
+        m0 = m1 + 1;
+      }
+    }
+    __syncwarp();
+  }
+  for (int k = lane; k < a.mask_pitch; k += 32) out[k] = (k < K) ? key_block(sm.key[k]) : -1;
+  if (lane == 0) a.mask_len[mrow] = K;
+}
+
 template <typename T>
 T* carve(uint8_t*& p, size_t n) {
   uintptr_t x = (reinterpret_cast<uintptr_t>(p) + 255) & ~uintptr_t(255);
@@ -1337,7 +1775,10 @@ cudaError_t launch_kap_t(KapArgs a, size_t qs_rows, size_t ks_rows, cudaStream_t
   const size_t ssm = select_smem_bytes(cap);
   e = cudaFuncSetAttribute(kap_select_kernel<HD, KB>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ssm));
   if (e != cudaSuccess) return e;
-  kap_select_kernel<HD, KB><<<static_cast<unsigned>(a.num_reqs) * a.num_q_heads * a.nqb_max, kSelectThreads, ssm, stream>>>(a, cap);
+  const long long nrows_mask = static_cast<long long>(a.num_reqs) * a.num_q_heads * a.nqb_max;
+  kap_select_warp_kernel<HD, KB><<<static_cast<unsigned>((nrows_mask + kWarpSelWarps - 1) / kWarpSelWarps),
+                                   kWarpSelWarps * 32, 0, stream>>>(a);
+  kap_select_kernel<HD, KB><<<static_cast<unsigned>(nrows_mask), kSelectThreads, ssm, stream>>>(a, cap);
   return cudaGetLastError();
 }
 
