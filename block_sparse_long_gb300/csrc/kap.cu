@@ -86,6 +86,7 @@ struct KapArgs {
   uint16_t* qs;          // gathered sampled queries, bf16 [rows, d]: row qs_off[b] + h * Rp + r
   uint16_t* ks;          // gathered sampled keys, bf16 [rows, d]: row ks_off[b] + kvh * Rp + c (zero if absent)
   uint32_t* kvalid;      // one bit per gathered key row: the key exists
+  int32_t* defer;        // [0] = count, [1..] = mask rows left to the block-per-row select kernel
   int num_reqs, num_q_heads, num_kv_heads, head_dim, block_size, page_size, stride, kb;
   int total_tokens, max_seqlen, num_pages, max_pages_per_req, mask_pitch, budget_ppm;
   int nqb_max, nrow_tiles_max, words_per_row;
@@ -193,6 +194,7 @@ __global__ void kap_setup_kernel(KapArgs a) {
     a.qs_off[a.num_reqs] = qo;
     a.ks_off[a.num_reqs] = ko;
     a.amb[0] = 0;
+    a.defer[0] = 0;
   }
   for (int e = threadIdx.x; e < a.num_reqs * a.num_kv_heads; e += blockDim.x) a.knorm[e] = 0.0f;
   for (int e = threadIdx.x; e < a.num_reqs * a.num_kv_heads * a.nqb_max; e += blockDim.x) a.kbnorm[e] = 0.0f;
@@ -912,8 +914,9 @@ __device__ void select_top_dispatch(unsigned long long* key, const uint8_t* hrm,
   select_top_keys<E>(key, hrm, score, serr, J, K, sh);
 }
 
+// Selection of mask row `row` by the whole block (the rows kap_select_warp_kernel leaves).
 template <int HD, int KB>
-__global__ void __launch_bounds__(kSelectThreads, 3) kap_select_kernel(KapArgs a, int cap) {
+__device__ void kap_select_row(const KapArgs& a, int cap, int row) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   unsigned long long* key = reinterpret_cast<unsigned long long*>(smem_raw);  // [cap] sort keys
   double* rep_val = reinterpret_cast<double*>(key + cap);                      // [cap] exact scores
@@ -930,14 +933,13 @@ __global__ void __launch_bounds__(kSelectThreads, 3) kap_select_kernel(KapArgs a
   __shared__ TopkShared topk;
 
   const int tid = threadIdx.x;
-  int idx = blockIdx.x;
+  int idx = row;
   const int h = idx % a.num_q_heads;
   idx /= a.num_q_heads;
   const int b = idx % a.num_reqs;
   const int i = a.nqb_max - 1 - idx / a.num_reqs;
   const ReqInfo ri = req_info(a, b);
   const size_t mrow = (static_cast<size_t>(b) * a.num_q_heads + h) * a.nqb_max + i;
-  if (a.mask_len[mrow] != -1) return;   // settled by kap_select_warp_kernel
   int32_t* out = a.mask + mrow * a.mask_pitch;
   if (i >= ri.nqb) {
     for (int k = tid; k < a.mask_pitch; k += blockDim.x) out[k] = -1;
@@ -1286,6 +1288,14 @@ __global__ void __launch_bounds__(kSelectThreads, 3) kap_select_kernel(KapArgs a
 // kWarpRepMax uncertain positions are repaired in float64.  Every other row (and a row whose cut
 // the sentinel cannot certify) is left to kap_select_kernel, marked by mask_len = -1.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ size_t mrow_of(const KapArgs& a, int row) {
+  const int h = row % a.num_q_heads;
+  row /= a.num_q_heads;
+  const int b = row % a.num_reqs;
+  const int i = a.nqb_max - 1 - row / a.num_reqs;
+  return (static_cast<size_t>(b) * a.num_q_heads + h) * a.nqb_max + i;
+}
+
 constexpr int kWarpSelMaxJ = 1024;
 constexpr int kWarpSelMaxK = 128;
 constexpr int kWarpRepMax = 16;
@@ -1370,6 +1380,14 @@ __global__ void __launch_bounds__(kWarpSelWarps * 32, 4) kap_select_warp_kernel(
   const long long nrow_all = static_cast<long long>(a.num_reqs) * a.num_q_heads * a.nqb_max;
   long long idx = static_cast<long long>(blockIdx.x) * kWarpSelWarps + w;
   if (idx >= nrow_all) return;
+  const int row = static_cast<int>(idx);
+  // rows left to kap_select_kernel: mask_len = -1 until it writes them
+  auto defer = [&]() {
+    if (lane == 0) {
+      a.mask_len[mrow_of(a, row)] = -1;
+      a.defer[1 + atomicAdd(&a.defer[0], 1)] = row;
+    }
+  };
   // the row order of kap_select_kernel: heads fastest, then requests, heaviest query blocks first
   const int h = static_cast<int>(idx % a.num_q_heads);
   idx /= a.num_q_heads;
@@ -1386,7 +1404,7 @@ __global__ void __launch_bounds__(kWarpSelWarps * 32, 4) kap_select_warp_kernel(
   const int J = i + 1;
   const int K = max(1, min(J, static_cast<int>((static_cast<long long>(a.budget_ppm) * J + 999999) / 1000000)));
   if (a.top_p || a.ascending || J > kWarpSelMaxJ || K > kWarpSelMaxK || K >= J) {
-    if (lane == 0) a.mask_len[mrow] = -1;
+    defer();
     return;
   }
   const int kvh = h / (a.num_q_heads / a.num_kv_heads);
@@ -1598,7 +1616,7 @@ __global__ void __launch_bounds__(kWarpSelWarps * 32, 4) kap_select_warp_kernel(
   }
   const int n_rep = __reduce_add_sync(0xffffffffu, nmk);
   if (__any_sync(0xffffffffu, sentinel_marked) || n_rep > kWarpRepMax) {
-    if (lane == 0) a.mask_len[mrow] = -1;   // the CTA kernel takes this row
+    defer();
     return;
   }
   if (n_rep > 0) {
@@ -1631,7 +1649,7 @@ __global__ void __launch_bounds__(kWarpSelWarps * 32, 4) kap_select_warp_kernel(
         const uint16_t* qr = qbase + static_cast<int64_t>(r) * HD + sub * SL;
         const uint16_t* kr = vis ? a.ks + (krow0 + kc) * HD + sub * SL : qr;
         float p0 = 0.0f, p1 = 0.0f;
-#pragma unroll 1
+#pragma unroll 4
         for (int e = 0; e < SL; e += 8) {
           float qv[8], kv[8];
           load8_bf16(qr + e, qv);
@@ -1715,6 +1733,16 @@ __global__ void __launch_bounds__(kWarpSelWarps * 32, 4) kap_select_warp_kernel(
   if (lane == 0) a.mask_len[mrow] = K;
 }
 
+// The rows kap_select_warp_kernel deferred (list in a.defer), a block per row, grid-stride.
+template <int HD, int KB>
+__global__ void __launch_bounds__(kSelectThreads, 3) kap_select_kernel(KapArgs a, int cap) {
+  const int n = a.defer[0];
+  for (int li = blockIdx.x; li < n; li += gridDim.x) {
+    kap_select_row<HD, KB>(a, cap, a.defer[1 + li]);
+    __syncthreads();   // shared memory is reused by the next row
+  }
+}
+
 template <typename T>
 T* carve(uint8_t*& p, size_t n) {
   uintptr_t x = (reinterpret_cast<uintptr_t>(p) + 255) & ~uintptr_t(255);
@@ -1778,7 +1806,8 @@ cudaError_t launch_kap_t(KapArgs a, size_t qs_rows, size_t ks_rows, cudaStream_t
   const long long nrows_mask = static_cast<long long>(a.num_reqs) * a.num_q_heads * a.nqb_max;
   kap_select_warp_kernel<HD, KB><<<static_cast<unsigned>((nrows_mask + kWarpSelWarps - 1) / kWarpSelWarps),
                                    kWarpSelWarps * 32, 0, stream>>>(a);
-  kap_select_kernel<HD, KB><<<static_cast<unsigned>(nrows_mask), kSelectThreads, ssm, stream>>>(a, cap);
+  kap_select_kernel<HD, KB><<<static_cast<unsigned>(nrows_mask < 1024 ? nrows_mask : 1024), kSelectThreads, ssm,
+                              stream>>>(a, cap);
   return cudaGetLastError();
 }
 
@@ -1809,6 +1838,7 @@ size_t kap_workspace_bytes(int num_reqs, int num_q_heads, int num_kv_heads, int 
   add(sizeof(uint16_t) * static_cast<size_t>(num_q_heads) * w.padded * 128);
   add(sizeof(uint16_t) * static_cast<size_t>(num_kv_heads) * w.padded * 128);
   add(sizeof(uint32_t) * (static_cast<size_t>(num_kv_heads) * w.padded / 32 + 1));
+  add(sizeof(int32_t) * (static_cast<size_t>(num_reqs) * num_q_heads * ((max_seqlen + block_size - 1) / block_size) + 1));
   return n + 256;
 }
 
@@ -1884,6 +1914,7 @@ cudaError_t launch_kap(const KapLaunch& L, cudaStream_t stream) {
   a.qs = carve<uint16_t>(p, static_cast<size_t>(L.num_q_heads) * w.padded * 128);
   a.ks = carve<uint16_t>(p, static_cast<size_t>(L.num_kv_heads) * w.padded * 128);
   a.kvalid = carve<uint32_t>(p, static_cast<size_t>(L.num_kv_heads) * w.padded / 32 + 1);
+  a.defer = carve<int32_t>(p, static_cast<size_t>(L.num_reqs) * L.num_q_heads * a.nqb_max + 1);
   if (static_cast<size_t>(p - static_cast<uint8_t*>(L.workspace)) > L.workspace_bytes) return cudaErrorInvalidValue;
   const int kb = a.kb;
   const size_t qs_rows = static_cast<size_t>(L.num_q_heads) * w.padded;
