@@ -419,7 +419,7 @@ def run_cosa(args, spec, workload_name, delta):
                      "peak_source": f"bf16_tflops ({pk_src}, burst)"},
         "e2e": {"value": world * step_flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 8 * args.steps,
+        "gpu_launches": 9 * args.steps,
         "clocks": cl,
     }
     if cpu is not None:
