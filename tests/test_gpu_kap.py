@@ -61,3 +61,26 @@ def test_kap_constant_keys_ties():
     w = synth.make_workload(sp)
     w.k_cache[...] = w.k_cache[0, 0, 0, :]
     _kap_check(w, budget_ppm=500_000)
+
+
+def test_kap_long_rows_both_select_paths():
+    """b = 64 over 70,000 tokens: query blocks up to 1,094, so rows with J_i <= 1024 and K_i <= 128
+    are selected one warp per row and the others (J_i > 1024, or K_i > 128 at a 20 % budget) by the
+    block-per-row kernel from its list.  Rows on both sides of each limit against the oracle."""
+    sp = synth.WorkloadSpec(name="long_b64", lengths=(70000,), num_q_heads=2, num_kv_heads=1, head_dim=64,
+                            block_size=64, page_size=32, stride=8, budget_ppm=200_000, stage2_budget_ppm=0,
+                            seed=303, shuffle_pages=True, salient_pages=4)
+    w = synth.make_workload(sp)
+    prm = gh.oracle_params(sp, -1.0)
+    pitch = gh.C.stage1_pitch(sp.budget_ppm, sp.max_seqlen, sp.block_size)
+    dw = gh.to_device(w)
+    mask_g, len_g = gh.run_kap(dw, gh.cosa_params(dw, delta=-1.0, mask_pitch=pitch))
+    # K_i = ceil(0.2 (i + 1)) passes 128 at i = 640; J_i passes 1024 at i = 1024
+    rows = [0, 5, 600, 639, 640, 641, 1000, 1022, 1023, 1024, 1025, 1093]
+    by = {(0, h): rows for h in range(sp.num_q_heads)}
+    _, _, orows = orc.kap_mask(w.q, w.k_cache, w.page_table, w.cu_seqlens, sp.num_q_heads, sp.num_kv_heads,
+                               prm, pitch, qblocks=by)
+    gh.compare_masks_rows(mask_g, len_g, orows)
+    nqb = -(-70000 // 64)
+    want = np.maximum(1, -(-200_000 * np.arange(1, nqb + 1) // 1_000_000))
+    assert (len_g[0, :, :nqb] == want[None, :]).all()
