@@ -87,6 +87,9 @@ struct KapArgs {
   uint16_t* ks;          // gathered sampled keys, bf16 [rows, d]: row ks_off[b] + kvh * Rp + c (zero if absent)
   uint32_t* kvalid;      // one bit per gathered key row: the key exists
   int32_t* defer;        // [0] = count, [1..] = mask rows left to the block-per-row select kernel
+  int64_t* bm_off;       // [B+1]: first block maximum of request b (times Hq)
+  float* bm;             // per (request, head, sampled row r, key block j <= r / kb): the largest
+                         // visible fp32 logit of block j (raw, unscaled), -inf if none
   int num_reqs, num_q_heads, num_kv_heads, head_dim, block_size, page_size, stride, kb;
   int total_tokens, max_seqlen, num_pages, max_pages_per_req, mask_pitch, budget_ppm;
   int nqb_max, nrow_tiles_max, words_per_row;
@@ -110,6 +113,22 @@ __device__ __forceinline__ ReqInfo req_info(const KapArgs& a, int b) {
   r.nqb = (r.L + a.block_size - 1) / a.block_size;
   r.req_pages = (r.L + a.page_size - 1) / a.page_size;
   return r;
+}
+
+// Block maxima layout: per (request, head), query block i holds its kb sampled rows one after
+// another, each padded to bm_pitch(i) = (i + 1) rounded up to 64 / kb floats, so that a thread of the
+// logits epilogue stores the 64 / kb block maxima of its columns as aligned 16-byte vectors.
+__host__ __device__ __forceinline__ int64_t bm_pitch(int i, int kb) {
+  const int ng = 64 / kb;
+  return (static_cast<int64_t>(i) + ng) / ng * ng;
+}
+// floats before query block i (sum over i' < i of kb * bm_pitch(i'))
+__host__ __device__ __forceinline__ int64_t bm_block_base(int i, int kb) {
+  const int64_t ng = 64 / kb;
+  const int64_t full = i / ng;                   // complete groups of ng query blocks
+  // blocks g*ng .. g*ng + ng - 1 have pitch (g + 1) * ng
+  int64_t sum = ng * ng * full * (full + 1) / 2 + (i - full * ng) * (full + 1) * ng;
+  return kb * sum;
 }
 
 // Address of sampled key c of request b, kv head kvh, or nullptr if its page does not exist.
@@ -175,12 +194,13 @@ __device__ __forceinline__ double warp_dot_f64(const uint16_t* x, const uint16_t
 // ---------------------------------------------------------------------------
 __global__ void kap_setup_kernel(KapArgs a) {
   if (threadIdx.x == 0) {
-    int64_t ro = 0, so = 0, qo = 0, ko = 0;
+    int64_t ro = 0, so = 0, qo = 0, ko = 0, bo = 0;
     for (int b = 0; b < a.num_reqs; ++b) {
       a.row_off[b] = ro;
       a.sc_off[b] = so;
       a.qs_off[b] = qo;
       a.ks_off[b] = ko;
+      a.bm_off[b] = bo;
       const ReqInfo ri = req_info(a, b);
       if (!ri.ok) report_status(a.status, kStatusBadInput);
       const int64_t rp = (ri.R + kRowTile - 1) / kRowTile * kRowTile;
@@ -188,7 +208,9 @@ __global__ void kap_setup_kernel(KapArgs a) {
       so += static_cast<int64_t>(a.num_q_heads) * ri.nqb * ri.nqb;
       qo += static_cast<int64_t>(a.num_q_heads) * rp;
       ko += static_cast<int64_t>(a.num_kv_heads) * rp;
+      bo += static_cast<int64_t>(a.num_q_heads) * bm_block_base(ri.nqb, a.kb);
     }
+    a.bm_off[a.num_reqs] = bo;
     a.row_off[a.num_reqs] = ro;
     a.sc_off[a.num_reqs] = so;
     a.qs_off[a.num_reqs] = qo;
@@ -257,8 +279,6 @@ __global__ void __launch_bounds__(256) kap_gather_kernel(KapArgs a) {
 // ---------------------------------------------------------------------------
 // sampled logits on tcgen05: 128 sampled rows x all causal sampled keys
 // ---------------------------------------------------------------------------
-enum { kModeRowMax = 0, kModeScores = 1 };
-
 constexpr int kKeyStages = 2;           // K~ tiles in flight (two CTAs fit per SM)
 constexpr int kLogitsThreads = 320;      // warp 0 TMA, warp 1 UMMA, warps 2-9 epilogue
 
@@ -277,14 +297,14 @@ struct alignas(1024) KapTileSmem {
 };
 
 // Sampled logits l = q~ . k~ (fp32, tcgen05) for 128 sampled rows against every causal key tile of
-// 128 sampled keys, with one of two epilogues:
-//   ROWMAX  the four largest logits of each row and their keys (candidates for the exact maximum);
-//   SCORES  per (row, key block) the block maximum, P~ = exp(bm - M_r) with the float64 M_r, and its
-//           error bound; summed over the sampled rows of each query block into the score s_ij.
+// 128 sampled keys.  The epilogue keeps the two largest logits of each row and the key of the first
+// (candidates for the exact maximum) and stores, per (row, key block j <= the row's query block), the
+// block maximum of Eq. (9) before normalisation; kap_block_scores_kernel turns those into s_ij once
+// the float64 row maxima are known.
 // Warp 0 streams the K~ tiles with TMA, warp 1 issues the UMMAs into two TMEM accumulators, warps
 // 2-9 read the accumulators: warp w serves TMEM lanes 32 (w % 4) .. + 31 and columns [64 g, 64 g + 64)
 // with g = (w - 2) / 4.
-template <int HD, int KB, int MODE>
+template <int HD, int KB>
 __global__ void __launch_bounds__(kLogitsThreads, 2)
     kap_logits_kernel(const __grid_constant__ CUtensorMap qs_map, const __grid_constant__ CUtensorMap ks_map,
                       KapArgs a) {
@@ -389,15 +409,13 @@ __global__ void __launch_bounds__(kLogitsThreads, 2)
     const uint32_t* kval = a.kvalid + (krow0 >> 5);
     float r1 = -INFINITY, r2 = -INFINITY;     // largest and second largest raw logit of this half
     int rc1 = -1;
-    float M32 = -INFINITY, ebase = 0.0f;
     const int nqb = ri.nqb;
-    const int64_t sbase = a.sc_off[b] + static_cast<int64_t>(h) * nqb * nqb;
-    const float* kbn = a.kbnorm + (static_cast<size_t>(b) * a.num_kv_heads + kvh) * a.nqb_max;
-    if (MODE == kModeScores && row_ok) {
-      M32 = static_cast<float>(a.M[rec]);
-      ebase = kKappa * scale * a.qnorm[rec] * 1.001f;
-    }
     const int qblk = r / KB;
+    // this row's block maxima: blocks 0 .. qblk of its (request, head), rows of a query block
+    // stored one after another
+    float* bm_row = a.bm + a.bm_off[b] + static_cast<int64_t>(h) * bm_block_base(nqb, KB) + bm_block_base(qblk, KB) +
+                    static_cast<int64_t>(r - qblk * KB) * bm_pitch(qblk, KB);
+    constexpr int NG = 64 / KB;                   // key blocks in this thread's 64 columns
     for (int kt = 0; kt < nkt; ++kt) {
       const int ab = kt & 1;
       const bool okw = __all_sync(0xffffffffu,
@@ -417,19 +435,20 @@ __global__ void __launch_bounds__(kLogitsThreads, 2)
       const int last = r - c0;                    // causal: columns <= last
       // every column of this thread's half is visible: below the diagonal tile, all keys valid
       const bool interior = row_ok && kt < rt && (bits0 & bits1) == 0xffffffffu;
-      if (MODE == kModeRowMax && interior) {
-        // tile maximum by a three-input max tree; the first index and the tile's second largest
-        // value are only needed when the running maximum rises (a few tiles per row)
-        float m8[8];
+      float bmg[NG];
+      if (interior) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q) m8[q] = fmaxf(__uint_as_float(va[2 * q]), __uint_as_float(va[2 * q + 1]));
+        for (int gg = 0; gg < NG; ++gg) {
+          float m = __uint_as_float(gg * KB < 32 ? va[gg * KB] : vb[gg * KB - 32]);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) m8[q] = fmax3f(m8[q], __uint_as_float(va[16 + 2 * q]), __uint_as_float(va[17 + 2 * q]));
+          for (int e = gg * KB + 1; e < (gg + 1) * KB; ++e) m = fmaxf(m, __uint_as_float(e < 32 ? va[e] : vb[e - 32]));
+          bmg[gg] = m;
+        }
+        // tile maximum from the block maxima; the first index and the tile's second largest value
+        // are only needed when the running maximum rises (a few tiles per row)
+        float t1 = bmg[0];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) m8[q] = fmax3f(m8[q], __uint_as_float(vb[2 * q]), __uint_as_float(vb[2 * q + 1]));
-#pragma unroll
-        for (int q = 0; q < 8; ++q) m8[q] = fmax3f(m8[q], __uint_as_float(vb[16 + 2 * q]), __uint_as_float(vb[17 + 2 * q]));
-        const float t1 = fmax3f(fmax3f(m8[0], m8[1], m8[2]), fmax3f(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+        for (int gg = 1; gg < NG; ++gg) t1 = fmaxf(t1, bmg[gg]);
         if (t1 > r1) {
           int e1 = 0;
 #pragma unroll
@@ -445,80 +464,42 @@ __global__ void __launch_bounds__(kLogitsThreads, 2)
         } else {
           r2 = fmaxf(r2, t1);
         }
-      } else if (MODE == kModeRowMax) {
+      } else {
+#pragma unroll
+        for (int gg = 0; gg < NG; ++gg) bmg[gg] = -INFINITY;
         // branch-free: second max = max(second, min(x, max)); argmax follows the first strict increase
 #pragma unroll
         for (int e = 0; e < 64; ++e) {
           const uint32_t bits = e < 32 ? bits0 : bits1;
           const bool vis = row_ok && e <= last && ((bits >> (e & 31)) & 1u);
           const float x = vis ? __uint_as_float(e < 32 ? va[e] : vb[e - 32]) : -INFINITY;
+          bmg[e / KB] = fmaxf(bmg[e / KB], x);
           r2 = fmaxf(r2, fminf(x, r1));
           rc1 = (x > r1) ? c0 + e : rc1;
           r1 = fmaxf(r1, x);
         }
-      } else {
-        // key-block norms of this half's blocks, loaded up front (blocks past the request read 0)
-        float kbv[64 / KB];
+      }
+      // the group of NG blocks starts at a multiple of NG <= qblk, so it fits the padded row
+      if (row_ok && c0 / KB <= qblk) {
 #pragma unroll
-        for (int gg = 0; gg < 64 / KB; ++gg) {
-          const int j = (c0 + gg * KB) / KB;
-          kbv[gg] = (j < nqb) ? __ldg(kbn + j) : 0.0f;
-        }
-#pragma unroll
-        for (int gg = 0; gg < 64 / KB; ++gg) {
-          float bm = -INFINITY;
-          if (interior) {
-#pragma unroll
-            for (int e = gg * KB; e < (gg + 1) * KB; ++e) bm = fmaxf(bm, __uint_as_float(e < 32 ? va[e] : vb[e - 32]));
-          } else {
-#pragma unroll
-            for (int e = gg * KB; e < (gg + 1) * KB; ++e) {
-              const uint32_t bits = e < 32 ? bits0 : bits1;
-              const float x = __uint_as_float(e < 32 ? va[e] : vb[e - 32]);
-              if (row_ok && e <= last && ((bits >> (e & 31)) & 1u)) bm = fmaxf(bm, x);
-            }
-          }
-          const int j = (c0 + gg * KB) / KB;
-          float x = 0.0f, xe = 0.0f;
-          if (bm != -INFINITY && M32 != -INFINITY) {
-            const float u = fmaf(bm, scale, -M32);
-            x = expf(u);
-            // |u - exact| <= kappa * scale * ||q|| * (largest ||k|| of block j) plus the rounding of
-            // the scaled logit, of M_r and of the subtraction; expf adds at most 2 ulp; exp(du) - 1 <=
-            // 1.02 du for du <= 0.03; a value below exp(-80) is only bounded absolutely
-            const float du = ebase * kbv[gg] + 1.2e-7f * (2.0f * fabsf(M32) + fabsf(u) + 1.0f);
-            const float rel = (du <= 0.03f) ? 1.02f * du : expm1f(du) * 1.01f;
-            xe = x * (rel + 3.0e-7f) + ((u < -80.0f) ? 2.0e-35f : 0.0f);
-          }
-#pragma unroll
-          for (int o = KB / 2; o > 0; o >>= 1) {
-            x += __shfl_xor_sync(0xffffffffu, x, o);
-            xe += __shfl_xor_sync(0xffffffffu, xe, o);
-          }
-          if ((lane % KB) == 0 && qblk < nqb && j <= qblk) {
-            const int64_t o = sbase + static_cast<int64_t>(qblk) * nqb + j;
-            a.score[o] = x;
-            a.score_err[o] = xe + x * (4.0f * 6.0e-8f);   // rounding of the kb-term sum
-          }
-        }
+        for (int gg = 0; gg < NG; gg += 4)
+          *reinterpret_cast<float4*>(bm_row + c0 / KB + gg) = make_float4(bmg[gg], bmg[gg + 1], bmg[gg + 2], bmg[gg + 3]);
       }
     }
-    if (MODE == kModeRowMax) {
-      // merge the two column halves; half 0 writes the row's record
-      sm.hv1[g][t] = r1;
-      sm.hv2[g][t] = r2;
-      sm.hc1[g][t] = rc1;
-      named_bar_sync(1, 256);
-      if (g == 0 && row_ok) {
-        const float a1 = sm.hv1[0][t], b1 = sm.hv1[1][t];
-        const int ac = sm.hc1[0][t], bc = sm.hc1[1][t];
-        const float m1 = fmaxf(a1, b1);
-        const float m2 = fmaxf(fminf(a1, b1), fmaxf(sm.hv2[0][t], sm.hv2[1][t]));
-        const int mc = (a1 > b1 || (a1 == b1 && ac >= 0)) ? ac : bc;
-        a.v1[rec] = (m1 == -INFINITY) ? -INFINITY : m1 * scale;
-        a.v2[rec] = (m2 == -INFINITY) ? -INFINITY : m2 * scale;
-        a.c1[rec] = mc;
-      }
+    // merge the two column halves; half 0 writes the row's record
+    sm.hv1[g][t] = r1;
+    sm.hv2[g][t] = r2;
+    sm.hc1[g][t] = rc1;
+    named_bar_sync(1, 256);
+    if (g == 0 && row_ok) {
+      const float a1 = sm.hv1[0][t], b1 = sm.hv1[1][t];
+      const int ac = sm.hc1[0][t], bc = sm.hc1[1][t];
+      const float m1 = fmaxf(a1, b1);
+      const float m2 = fmaxf(fminf(a1, b1), fmaxf(sm.hv2[0][t], sm.hv2[1][t]));
+      const int mc = (a1 > b1 || (a1 == b1 && ac >= 0)) ? ac : bc;
+      a.v1[rec] = (m1 == -INFINITY) ? -INFINITY : m1 * scale;
+      a.v2[rec] = (m2 == -INFINITY) ? -INFINITY : m2 * scale;
+      a.c1[rec] = mc;
     }
   }
   tc_fence_before();
@@ -526,6 +507,70 @@ __global__ void __launch_bounds__(kLogitsThreads, 2)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 256);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// block scores (Eqs. (9)-(11)): s_ij = sum over the sampled rows r of query block i of
+// Pbar[r, j] = exp(bm[r, j] * scale - M_r), with the float64 row maxima M_r (rounded to fp32), and a
+// bound on |s_ij - exact|.  A block per (request, head, query block), a thread per key block j <= i.
+// ---------------------------------------------------------------------------
+template <int KB>
+__global__ void __launch_bounds__(128) kap_block_scores_kernel(KapArgs a) {
+  const int i = a.nqb_max - 1 - static_cast<int>(blockIdx.x);   // heaviest query blocks first
+  const int h = blockIdx.y, b = blockIdx.z;
+  const ReqInfo ri = req_info(a, b);
+  if (i >= ri.nqb) return;
+  const int nqb = ri.nqb;
+  const int kvh = h / (a.num_q_heads / a.num_kv_heads);
+  const float scale = static_cast<float>(a.sm_scale);
+  const int64_t rbase = a.row_off[b] + static_cast<int64_t>(h) * ri.R;
+  const float* bm_blk = a.bm + a.bm_off[b] + static_cast<int64_t>(h) * bm_block_base(nqb, KB) + bm_block_base(i, KB);
+  const int64_t pitch = bm_pitch(i, KB);
+  const float* kbn = a.kbnorm + (static_cast<size_t>(b) * a.num_kv_heads + kvh) * a.nqb_max;
+  const int64_t sbase = a.sc_off[b] + static_cast<int64_t>(h) * nqb * nqb + static_cast<int64_t>(i) * nqb;
+  // the query block's sampled rows: rounded row maximum and the logit error scale
+  float M32[KB], ebase[KB];
+#pragma unroll
+  for (int q = 0; q < KB; ++q) {
+    const int r = i * KB + q;
+    M32[q] = -INFINITY;
+    ebase[q] = 0.0f;
+    if (r < ri.R) {
+      M32[q] = static_cast<float>(a.M[rbase + r]);
+      ebase[q] = kKappa * scale * a.qnorm[rbase + r] * 1.001f;
+    }
+  }
+  for (int j = threadIdx.x; j <= i; j += blockDim.x) {
+    const float kbv = __ldg(kbn + j);
+    float x[KB], xe[KB];
+#pragma unroll
+    for (int q = 0; q < KB; ++q) {
+      x[q] = 0.0f;
+      xe[q] = 0.0f;
+      const float bm = (i * KB + q < ri.R) ? bm_blk[q * pitch + j] : -INFINITY;
+      if (bm != -INFINITY && M32[q] != -INFINITY) {
+        const float u = fmaf(bm, scale, -M32[q]);
+        x[q] = expf(u);
+        // |u - exact| <= kappa * scale * ||q|| * (largest ||k|| of block j) plus the rounding of the
+        // scaled logit, of M_r and of the subtraction; expf adds at most 2 ulp; exp(du) - 1 <=
+        // 1.02 du for du <= 0.03; a value below exp(-80) is only bounded absolutely
+        const float du = ebase[q] * kbv + 1.2e-7f * (2.0f * fabsf(M32[q]) + fabsf(u) + 1.0f);
+        const float rel = (du <= 0.03f) ? 1.02f * du : expm1f(du) * 1.01f;
+        xe[q] = x[q] * (rel + 3.0e-7f) + ((u < -80.0f) ? 2.0e-35f : 0.0f);
+      }
+    }
+    // pairwise sum over the rows (log2 KB levels)
+#pragma unroll
+    for (int o = KB / 2; o > 0; o >>= 1) {
+#pragma unroll
+      for (int q = 0; q < o; ++q) {
+        x[q] += x[q + o];
+        xe[q] += xe[q + o];
+      }
+    }
+    a.score[sbase + j] = x[0];
+    a.score_err[sbase + j] = xe[0] + x[0] * (4.0f * 6.0e-8f);   // rounding of the kb-term sum
   }
 }
 
@@ -1753,6 +1798,7 @@ T* carve(uint8_t*& p, size_t n) {
 
 struct WsLayout {
   size_t rows, scores, words, padded;  // padded: sampled rows of one head summed over requests, 128-padded
+  size_t bms;                          // block maxima: Hq * kb * sum_b nqb_b (nqb_b + 1) / 2, bounded above
 };
 
 WsLayout ws_layout(int num_reqs, int num_q_heads, int block_size, int stride, int total_tokens, int max_seqlen) {
@@ -1762,6 +1808,9 @@ WsLayout ws_layout(int num_reqs, int num_q_heads, int block_size, int stride, in
   w.scores = static_cast<size_t>(num_q_heads) * nqb_max * (static_cast<size_t>(total_tokens) / block_size + num_reqs);
   w.words = (nqb_max + 31) / 32;
   w.padded = static_cast<size_t>(total_tokens) / stride + static_cast<size_t>(num_reqs) * (kRowTile + 1);
+  // sum_b sum_{i < nqb_b} bm_pitch(i) <= sum_b nqb_b ((nqb_b + 1) / 2 + 16) <= (T / b + B) (nqb_max / 2 + 17)
+  w.bms = static_cast<size_t>(num_q_heads) * (block_size / stride) * (nqb_max / 2 + 17) *
+          (static_cast<size_t>(total_tokens) / block_size + num_reqs);
   return w;
 }
 
@@ -1783,21 +1832,18 @@ cudaError_t launch_kap_t(KapArgs a, size_t qs_rows, size_t ks_rows, cudaStream_t
     if (!encode_tiled_bf16(&ks_map, a.ks, 2, dims_k, strides, box)) return cudaErrorInvalidValue;
   }
   const size_t tsm = sizeof(KapTileSmem<HD>) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(kap_logits_kernel<HD, KB, kModeRowMax>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(tsm));
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(kap_logits_kernel<HD, KB, kModeScores>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(tsm));
+  cudaError_t e = cudaFuncSetAttribute(kap_logits_kernel<HD, KB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(tsm));
   if (e != cudaSuccess) return e;
   const unsigned tiles = static_cast<unsigned>(a.num_reqs) * a.num_q_heads * a.nrow_tiles_max;
-  kap_logits_kernel<HD, KB, kModeRowMax><<<tiles, kLogitsThreads, tsm, stream>>>(qs_map, ks_map, a);
+  kap_logits_kernel<HD, KB><<<tiles, kLogitsThreads, tsm, stream>>>(qs_map, ks_map, a);
   {
     const size_t rows = static_cast<size_t>(a.num_q_heads) * (static_cast<size_t>(a.total_tokens) / a.stride + a.num_reqs);
     const unsigned blocks = static_cast<unsigned>((rows + 7) / 8);
     kap_exact_kernel<HD><<<blocks, 256, 0, stream>>>(a);
     kap_rescan_kernel<HD><<<1024, 256, 0, stream>>>(a);
   }
-  kap_logits_kernel<HD, KB, kModeScores><<<tiles, kLogitsThreads, tsm, stream>>>(qs_map, ks_map, a);
+  kap_block_scores_kernel<KB><<<dim3(a.nqb_max, a.num_q_heads, a.num_reqs), 128, 0, stream>>>(a);
   int cap = kSelectThreads;   // the sort works on at least one key per thread
   while (cap < a.nqb_max) cap <<= 1;
   const size_t ssm = select_smem_bytes(cap);
@@ -1839,6 +1885,8 @@ size_t kap_workspace_bytes(int num_reqs, int num_q_heads, int num_kv_heads, int 
   add(sizeof(uint16_t) * static_cast<size_t>(num_kv_heads) * w.padded * 128);
   add(sizeof(uint32_t) * (static_cast<size_t>(num_kv_heads) * w.padded / 32 + 1));
   add(sizeof(int32_t) * (static_cast<size_t>(num_reqs) * num_q_heads * ((max_seqlen + block_size - 1) / block_size) + 1));
+  add(sizeof(int64_t) * (num_reqs + 1));
+  add(sizeof(float) * w.bms);
   return n + 256;
 }
 
@@ -1915,6 +1963,8 @@ cudaError_t launch_kap(const KapLaunch& L, cudaStream_t stream) {
   a.ks = carve<uint16_t>(p, static_cast<size_t>(L.num_kv_heads) * w.padded * 128);
   a.kvalid = carve<uint32_t>(p, static_cast<size_t>(L.num_kv_heads) * w.padded / 32 + 1);
   a.defer = carve<int32_t>(p, static_cast<size_t>(L.num_reqs) * L.num_q_heads * a.nqb_max + 1);
+  a.bm_off = carve<int64_t>(p, L.num_reqs + 1);
+  a.bm = carve<float>(p, w.bms);
   if (static_cast<size_t>(p - static_cast<uint8_t*>(L.workspace)) > L.workspace_bytes) return cudaErrorInvalidValue;
   const int kb = a.kb;
   const size_t qs_rows = static_cast<size_t>(L.num_q_heads) * w.padded;
