@@ -543,12 +543,16 @@ __global__ void __launch_bounds__(128) kap_block_scores_kernel(KapArgs a) {
   }
   for (int j = threadIdx.x; j <= i; j += blockDim.x) {
     const float kbv = __ldg(kbn + j);
+    // every row's block maximum is requested before any is used
+    float bmv[KB];
+#pragma unroll
+    for (int q = 0; q < KB; ++q) bmv[q] = (i * KB + q < ri.R) ? __ldcs(bm_blk + q * pitch + j) : -INFINITY;
     float x[KB], xe[KB];
 #pragma unroll
     for (int q = 0; q < KB; ++q) {
       x[q] = 0.0f;
       xe[q] = 0.0f;
-      const float bm = (i * KB + q < ri.R) ? bm_blk[q * pitch + j] : -INFINITY;
+      const float bm = bmv[q];
       if (bm != -INFINITY && M32[q] != -INFINITY) {
         const float u = fmaf(bm, scale, -M32[q]);
         x[q] = expf(u);
@@ -1418,7 +1422,7 @@ __device__ __forceinline__ int warp_excl_sum(int x, int lane) {
 }
 
 template <int HD, int KB>
-__global__ void __launch_bounds__(kWarpSelWarps * 32, 4) kap_select_warp_kernel(KapArgs a) {
+__global__ void __launch_bounds__(kWarpSelWarps * 32, 8) kap_select_warp_kernel(KapArgs a) {
   __shared__ WarpSelSmem wsm[kWarpSelWarps];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   WarpSelSmem& sm = wsm[w];
