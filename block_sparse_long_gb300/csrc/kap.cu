@@ -583,47 +583,70 @@ __global__ void __launch_bounds__(128) kap_block_scores_kernel(KapArgs a) {
 // ---------------------------------------------------------------------------
 template <int HD>
 __global__ void __launch_bounds__(256) kap_exact_kernel(KapArgs a) {
-  const int warps_per_cta = blockDim.x / 32;
-  const int64_t gw = static_cast<int64_t>(blockIdx.x) * warps_per_cta + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  // locate (b, h, r) of record gw
+  // four rows per warp, eight lanes per row: the float64 work of the row's dot product (its cost on
+  // GB300's slow FP64 pipe sets this kernel's time) takes three shuffle rounds instead of five
+  constexpr int RPW = 4, LPR = 32 / RPW, PER = HD / LPR;
+  const int lane = threadIdx.x & 31, sub = lane % LPR, grp = lane / LPR;
+  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5)) * RPW + grp;
   const int64_t total = a.row_off[a.num_reqs];
-  if (gw >= total) return;
+  const bool live = gw < total;
+  // locate (b, h, r) of record gw (a lane group past the end works on record 0 and writes nothing)
+  const int64_t rec = live ? gw : 0;
   int b = 0;
-  while (b + 1 < a.num_reqs && a.row_off[b + 1] <= gw) ++b;
+  while (b + 1 < a.num_reqs && a.row_off[b + 1] <= rec) ++b;
   const ReqInfo ri = req_info(a, b);
-  const int64_t local = gw - a.row_off[b];
+  const int64_t local = rec - a.row_off[b];
   const int h = static_cast<int>(local / ri.R);
   const int r = static_cast<int>(local % ri.R);
   const int kvh = h / (a.num_q_heads / a.num_kv_heads);
-  const uint16_t* qr = query_ptr(a, ri, h, r);
+  const uint16_t* qr = query_ptr(a, ri, h, r) + sub * PER;
+  float qf[PER];
+#pragma unroll
+  for (int e = 0; e < PER; e += 8) {
+    float f[8];
+    load8_bf16(qr + e, f);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) qf[e + q] = f[q];
+  }
   // ||q_r||
   float s2 = 0.0f;
-  for (int e = lane; e < HD; e += 32) {
-    const float x = bf16_to_f32(qr[e]);
-    s2 = fmaf(x, x, s2);
-  }
-  for (int o = 16; o > 0; o >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+#pragma unroll
+  for (int e = 0; e < PER; ++e) s2 = fmaf(qf[e], qf[e], s2);
+#pragma unroll
+  for (int o = LPR / 2; o > 0; o >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
   const float qn = sqrtf(s2) * (1.0f + 1.0f / 65536.0f);
   // bound on |fp32 logit - exact| for every key of the row (largest key norm of the request)
   const float e_r = kKappa * static_cast<float>(a.sm_scale) * qn * a.knorm[b * a.num_kv_heads + kvh] * 1.001f + 1e-30f;
-  const float v1 = a.v1[gw], v2 = a.v2[gw];
-  if (lane == 0) { a.qnorm[gw] = qn; a.err[gw] = e_r; }
-  if (v1 == -INFINITY) {
-    if (lane == 0) { a.M[gw] = -INFINITY; a.rflags[gw] = 2; a.c1[gw] = -1; }
-    return;
-  }
+  const float v1 = a.v1[rec], v2 = a.v2[rec];
   // a key can hold the exact maximum only if its fp32 logit is within 2 e_r of the largest one
-  if (v2 < v1 - 2.0f * e_r) {
-    const double lx = warp_dot_f64<HD>(qr, key_ptr(a, ri, b, kvh, a.c1[gw])) * a.sm_scale;
-    if (lane == 0) { a.M[gw] = lx; a.rflags[gw] = 0; }
-    return;
+  const bool empty = v1 == -INFINITY;
+  const bool certain = !empty && v2 < v1 - 2.0f * e_r;
+  const uint16_t* kr = certain ? key_ptr(a, ri, b, kvh, a.c1[rec]) + sub * PER : qr;
+  double acc = 0.0;
+#pragma unroll
+  for (int e = 0; e < PER; e += 8) {
+    float kf[8];
+    load8_bf16(kr + e, kf);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc += static_cast<double>(qf[e + q] * kf[q]);   // exact fp32 product
   }
-  // not certain from fp32: settled by kap_rescan_kernel
-  if (lane == 0) {
-    a.rflags[gw] = 1;
+#pragma unroll
+  for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (!live || sub != 0) return;
+  a.qnorm[rec] = qn;
+  a.err[rec] = e_r;
+  if (empty) {
+    a.M[rec] = -INFINITY;
+    a.rflags[rec] = 2;
+    a.c1[rec] = -1;
+  } else if (certain) {
+    a.M[rec] = acc * a.sm_scale;
+    a.rflags[rec] = 0;
+  } else {
+    // not certain from fp32: settled by kap_rescan_kernel
+    a.rflags[rec] = 1;
     const unsigned long long slot = atomicAdd(reinterpret_cast<unsigned long long*>(&a.amb[0]), 1ull);
-    a.amb[1 + slot] = gw;
+    a.amb[1 + slot] = rec;
   }
 }
 
@@ -1843,7 +1866,7 @@ cudaError_t launch_kap_t(KapArgs a, size_t qs_rows, size_t ks_rows, cudaStream_t
   kap_logits_kernel<HD, KB><<<tiles, kLogitsThreads, tsm, stream>>>(qs_map, ks_map, a);
   {
     const size_t rows = static_cast<size_t>(a.num_q_heads) * (static_cast<size_t>(a.total_tokens) / a.stride + a.num_reqs);
-    const unsigned blocks = static_cast<unsigned>((rows + 7) / 8);
+    const unsigned blocks = static_cast<unsigned>((rows + 31) / 32);   // 8 warps of 4 rows
     kap_exact_kernel<HD><<<blocks, 256, 0, stream>>>(a);
     kap_rescan_kernel<HD><<<1024, 256, 0, stream>>>(a);
   }
