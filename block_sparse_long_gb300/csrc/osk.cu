@@ -46,7 +46,7 @@ constexpr float kRescaleLog2 = 8.0f;     // lazy-rescale threshold, log2 units
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO = 256, kTmemP0 = 384, kTmemP1 = 448;
 
-struct KInfo {
+struct alignas(16) KInfo {
   int32_t blk;     // block id, -1 = end of the list
   uint32_t pages;  // bit u set: page u of the block exists
   int32_t k;       // index of the entry in the mask row
@@ -524,19 +524,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         okw = __all_sync(0xffffffffu, okw);
         if (okw) {
           // slot v & 7 is rewritten with K(v + 8), which waits for S(v + 3) to be released
-          ki_blk = sm.info[v & 7].blk;
-          ki_pages = sm.info[v & 7].pages;
-          ki_k = sm.info[v & 7].k;
+          const int4 hd = *reinterpret_cast<const int4*>(&sm.info[v & 7]);
+          ki_blk = hd.x;
+          ki_pages = static_cast<uint32_t>(hd.y);
+          ki_k = hd.z;
           if (ki_blk >= 0) {
             tc_fence_after();
+            if constexpr (SC == 64) {
+              uint32_t r[64];
+              tmem_ld64(sbase, r);
+              tmem_wait_ld();
 #pragma unroll
-            for (int cc = 0; cc < SC / 32; ++cc) {
-              uint32_t r[32];
-              tmem_ld32(sbase + cc * 32, r);
+              for (int e = 0; e < 64; ++e) sv[e] = __uint_as_float(r[e]);
+            } else {
 #pragma unroll
-              for (int e = 0; e < 32; ++e) sv[cc * 32 + e] = __uint_as_float(r[e]);
+              for (int cc = 0; cc < SC / 32; ++cc) {
+                uint32_t r[32];
+                tmem_ld32(sbase + cc * 32, r);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) sv[cc * 32 + e] = __uint_as_float(r[e]);
+              }
+              tmem_wait_ld();
             }
-            tmem_wait_ld();
             tc_fence_before();
           }
           // the buffer is released for every visit, the end marker's included
