@@ -562,15 +562,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (col0 + e > lim || !((ki_pages >> ((col0 + e) >> pshift)) & 1u)) sv[e] = -INFINITY;
             }
             static_assert(SC % 16 == 0, "16-column groups");
-            float m8[8];
+            float m4[4];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) m8[q] = fmaxf(sv[2 * q], sv[2 * q + 1]);
+            for (int q = 0; q < 4; ++q) m4[q] = sv[q];
 #pragma unroll
-            for (int e = 16; e < SC; e += 16) {
+            for (int e = 4; e < SC; e += 4) {
 #pragma unroll
-              for (int q = 0; q < 8; ++q) m8[q] = fmax3f(m8[q], sv[e + 2 * q], sv[e + 2 * q + 1]);
+              for (int q = 0; q < 4; ++q) m4[q] = fmaxf(m4[q], sv[e + q]);
             }
-            pm = fmax3f(fmax3f(m8[0], m8[1], m8[2]), fmax3f(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+            pm = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
           }
         }
         // skip vote (Eq. (5)).  A row wants the block iff m_loc - max(m_run, m_loc) >= tau2; that
