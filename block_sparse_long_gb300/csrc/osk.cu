@@ -77,6 +77,7 @@ struct alignas(1024) OskSmem {
   uint64_t vreq_full[4];
   uint64_t cleanup;
   KInfo info[8];                              // visit info of visit v (slot v & 7), written with K(v)
+  KInfo stage[32];                            // the K producer's current batch of 32 mask entries
   KInfo vreq[4];
   float pmax[2][2][128];                      // partial row maxima [visit & 1][column half][row]
   float lsum[2][128];                         // partial row sums, exchanged at the end
@@ -281,27 +282,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (pp >= 0 && pp < a.num_pages) { phys[u] = pp; pages |= 1u << u; }
           }
         }
+        // each lane stages its entry's visit record; lane 0 issues the visits from the stage
+        const bool issue = keep || (BIN && k < n_walk);
+        if (issue) {
+          KInfo& st = sm.stage[lane];
+          st.blk = (BIN && !keep) ? -2 : j;
+          st.pages = pages;
+          st.k = k;
+          st.kvh = kvh;
+#pragma unroll
+          for (int u = 0; u < kMaxPagesPerBlock; ++u) st.phys[u] = phys[u];
+        }
         __syncwarp();
-        unsigned todo = __ballot_sync(0xffffffffu, keep || (BIN && k < n_walk));
+        unsigned todo = __ballot_sync(0xffffffffu, issue);
         while (todo && ok) {
           const int src = __ffs(todo) - 1;
           todo &= todo - 1;
-          const int jj = __shfl_sync(0xffffffffu, (BIN && !keep) ? -2 : j, src);
-          const uint32_t pg = __shfl_sync(0xffffffffu, pages, src);
-          int ph[kMaxPagesPerBlock];
-#pragma unroll
-          for (int u = 0; u < kMaxPagesPerBlock; ++u) ph[u] = __shfl_sync(0xffffffffu, phys[u], src);
           const int slot = v % NK;
           if (v >= NK) ok = warp_wait(&sm.k_free[slot], ((v / NK) - 1) & 1, abort_flag, a.status);
           if (!ok) break;
           if (lane == 0) {
+            const KInfo& st = sm.stage[src];
             KInfo& ki = sm.info[v & 7];
-            ki.blk = jj;
-            ki.pages = pg;
-            ki.k = k0 + src;
-            ki.kvh = kvh;
-#pragma unroll
-            for (int u = 0; u < kMaxPagesPerBlock; ++u) ki.phys[u] = ph[u];
+            ki = st;
+            const int jj = st.blk;
+            const uint32_t pg = st.pages;
+            const int32_t* ph = st.phys;
             if (BIN && jj < 0) {
               // a block the binary mask drops: nothing to load
               mbar_arrive(&sm.k_full[slot][v & 1]);
