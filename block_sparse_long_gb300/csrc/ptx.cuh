@@ -320,12 +320,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-// max of three (one instruction on sm_100 and later)
-__device__ __forceinline__ float fmax3f(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
 
 // (d0, d1) = (a0 * b + c, a1 * b + c), each rounded once (packed fp32 FMA)
 __device__ __forceinline__ void fma2_bc(float& d0, float& d1, float a0, float a1, float b, float c) {
