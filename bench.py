@@ -225,6 +225,22 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time (the job ends with it); the value itself on one rank."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world: int, flops_per_rank_step: float, ms_per_step: float) -> float:
+    """Whole-job throughput when every rank runs one replica of the step (weak scaling)."""
+    return world * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
 # --------------------------------------------------------------------------- #
 # reference arm: the oracle, as it stands, on the host cores
 # --------------------------------------------------------------------------- #
@@ -348,14 +364,11 @@ def run_cosa(args, spec, workload_name, delta):
     total_ms = start.elapsed_time(stop)
     kap_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(args.steps)]
     osk_ms = [ev[s][1].elapsed_time(ev[s][2]) for s in range(args.steps)]
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
     if int(status.item()) != 0:
         raise RuntimeError(C.cosa_status_string(int(status.item())))
     ms_step = total_ms / args.steps
-    value = world * step_flops / (ms_step * 1e-3) / 1e12
+    value = job_tflops(world, step_flops, ms_step)
 
     # end to end through the public API with host buffers (pinned), copies inside the timed region
     hq = torch.from_numpy(np.ascontiguousarray(w.q).view(np.int16)).pin_memory()
@@ -378,6 +391,8 @@ def run_cosa(args, spec, workload_name, delta):
 
     for _ in range(max(1, args.warmup)):
         e2e_step()
+    if world > 1:
+        torch.distributed.barrier()
     torch.cuda.synchronize()
     e_start, e_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e_start.record(stream)
@@ -385,7 +400,7 @@ def run_cosa(args, spec, workload_name, delta):
         e2e_step()
     e_stop.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e_start.elapsed_time(e_stop) / args.steps
+    e2e_ms = max_over_ranks(e_start.elapsed_time(e_stop) / args.steps, world, dev)
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hpt, hcu))
     d2h = hout.numel() * hout.element_size()
 
@@ -417,7 +432,7 @@ def run_cosa(args, spec, workload_name, delta):
         "roofline": {"bound": "tensor", "kernel": "osk_kernel<128,128,false>", "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"bf16_tflops ({pk_src}, burst)"},
-        "e2e": {"value": world * step_flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
+        "e2e": {"value": job_tflops(world, step_flops, e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 9 * args.steps,
         "clocks": cl,
