@@ -160,35 +160,6 @@ __device__ __forceinline__ void load8_bf16(const uint16_t* p, float (&f)[8]) {
   }
 }
 
-// warp dot products over d (lanes split d into contiguous slices)
-template <int HD>
-__device__ __forceinline__ float warp_dot_f32(const uint16_t* x, const uint16_t* y) {
-  constexpr int PER = HD / 32;
-  const int l = threadIdx.x & 31;
-  float acc = 0.0f;
-#pragma unroll
-  for (int e = 0; e < PER; ++e) acc = fmaf(bf16_to_f32(x[l * PER + e]), bf16_to_f32(y[l * PER + e]), acc);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  return acc;
-}
-
-template <int HD>
-// Products of two bf16 values are exact in fp32 (8-bit significands), so each float64 step below,
-// acc + (double)(x * y), rounds exactly like fma((double)x, (double)y, acc) with one float64
-// conversion instead of two.
-__device__ __forceinline__ double warp_dot_f64(const uint16_t* x, const uint16_t* y) {
-  constexpr int PER = HD / 32;
-  const int l = threadIdx.x & 31;
-  double acc = 0.0;
-#pragma unroll
-  for (int e = 0; e < PER; ++e)
-    acc += static_cast<double>(bf16_to_f32(x[l * PER + e]) * bf16_to_f32(y[l * PER + e]));   // exact fp32 product
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  return acc;
-}
-
 // ---------------------------------------------------------------------------
 // setup: per-request offsets into the workspace, zeroed key norms, input checks
 // ---------------------------------------------------------------------------
@@ -628,7 +599,9 @@ __global__ void __launch_bounds__(256) kap_exact_kernel(KapArgs a) {
     float kf[8];
     load8_bf16(kr + e, kf);
 #pragma unroll
-    for (int q = 0; q < 8; ++q) acc += static_cast<double>(qf[e + q] * kf[q]);   // exact fp32 product
+    // products of two bf16 values are exact in fp32 (8-bit significands), so acc + (double)(x * y)
+    // rounds exactly like fma((double)x, (double)y, acc) with one float64 conversion instead of two
+    for (int q = 0; q < 8; ++q) acc += static_cast<double>(qf[e + q] * kf[q]);
   }
 #pragma unroll
   for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
