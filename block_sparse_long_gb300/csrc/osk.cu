@@ -156,8 +156,10 @@ __device__ __forceinline__ Item decode_item(const OskArgs& a, int idx, int blk) 
   return it;
 }
 
-// BIN: the mask rows are binary block masks walked in ascending order (logical skipping)
-template <int BLK, int HD, bool BIN>
+// BIN: the mask rows are binary block masks walked in ascending order (logical skipping);
+// SKIP: the in-kernel skip rule is on (Delta > 0); FLAGS: visit flags are recorded.  Fixing the
+// last two at compile time keeps their tests and stores out of the per-visit loop.
+template <int BLK, int HD, bool BIN, bool SKIP, bool FLAGS>
 __global__ void __launch_bounds__(kThreads, 1)
     osk_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap_blk,
                const __grid_constant__ CUtensorMap kmap_pg, const __grid_constant__ CUtensorMap vmap_blk,
@@ -239,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int req_pages = (it.L + P - 1) / P;
       const size_t row_base = ((static_cast<size_t>(it.b) * a.num_q_heads + it.h) * a.nqb_max + i);
       const int32_t* mask_row = a.mask + row_base * a.mask_pitch;
-      uint8_t* flags_row = a.visit_flags ? a.visit_flags + row_base * a.mask_pitch : nullptr;
+      uint8_t* flags_row = FLAGS ? a.visit_flags + row_base * a.mask_pitch : nullptr;
       int n_entries = a.mask_len[row_base];
       n_entries = n_entries < 0 ? 0 : (n_entries > a.mask_pitch ? a.mask_pitch : n_entries);
       for (int w = lane; w < (nblk + 31) / 32; w += 32) sm.seen[w] = 0u;
@@ -497,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane = lane_id();
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int col0 = g * SC;              // first S column of this thread
-    const bool use_skip = a.skip_delta > 0.0;
+    constexpr bool use_skip = SKIP;
     const float sl2 = a.scale_log2;
     const int pshift = __ffs(P) - 1;
     const bool leader = threadIdx.x == 0;
@@ -514,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ln(Delta / L) in log2 units, in fp32 (the logits it is compared with are fp32)
       const float tau2 = use_skip ? log2f(static_cast<float>(a.skip_delta)) - log2f(static_cast<float>(L)) : 0.0f;
       const size_t row_base = ((static_cast<size_t>(it.b) * a.num_q_heads + it.h) * a.nqb_max + i);
-      uint8_t* flags_row = a.visit_flags ? a.visit_flags + row_base * a.mask_pitch : nullptr;
+      uint8_t* flags_row = FLAGS ? a.visit_flags + row_base * a.mask_pitch : nullptr;
       float m_run = -INFINITY;   // running max (log2 units), Algorithm A line 13
       float m_ref = -INFINITY;   // max the exponentials are taken against
       float l_part = 0.0f;       // this half's share of the row sum l
@@ -756,7 +758,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BLK, int HD, bool BIN>
+template <int BLK, int HD, bool BIN, bool SKIP, bool FLAGS>
 cudaError_t launch_osk_b(const OskLaunch& L, cudaStream_t stream) {
   OskArgs a;
   a.cu_seqlens = L.cu_seqlens;
@@ -780,7 +782,7 @@ cudaError_t launch_osk_b(const OskLaunch& L, cudaStream_t stream) {
   a.skip_delta = L.skip_delta;
   a.stall = (L.flags & COSA_FLAG_TEST_STALL) ? 1 : 0;
   const size_t smem = sizeof(OskSmem<BLK, HD>) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(osk_kernel<BLK, HD, BIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(osk_kernel<BLK, HD, BIN, SKIP, FLAGS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const long long items =
@@ -795,14 +797,21 @@ cudaError_t launch_osk_b(const OskLaunch& L, cudaStream_t stream) {
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(items < sms ? items : sms);
-  osk_kernel<BLK, HD, BIN><<<grid, kThreads, smem, stream>>>(L.qmap, L.kmap_blk, L.kmap_pg, L.vmap_blk, L.vmap_pg, a);
+  osk_kernel<BLK, HD, BIN, SKIP, FLAGS><<<grid, kThreads, smem, stream>>>(L.qmap, L.kmap_blk, L.kmap_pg, L.vmap_blk, L.vmap_pg, a);
   return cudaGetLastError();
+}
+
+template <int BLK, int HD, bool BIN>
+cudaError_t launch_osk_s(const OskLaunch& L, cudaStream_t stream) {
+  const bool skip = L.skip_delta > 0.0, flags = L.visit_flags != nullptr;
+  if (skip) return flags ? launch_osk_b<BLK, HD, BIN, true, true>(L, stream) : launch_osk_b<BLK, HD, BIN, true, false>(L, stream);
+  return flags ? launch_osk_b<BLK, HD, BIN, false, true>(L, stream) : launch_osk_b<BLK, HD, BIN, false, false>(L, stream);
 }
 
 template <int BLK, int HD>
 cudaError_t launch_osk_t(const OskLaunch& L, cudaStream_t stream) {
-  return (L.flags & COSA_FLAG_BINARY_MASK) ? launch_osk_b<BLK, HD, true>(L, stream)
-                                           : launch_osk_b<BLK, HD, false>(L, stream);
+  return (L.flags & COSA_FLAG_BINARY_MASK) ? launch_osk_s<BLK, HD, true>(L, stream)
+                                           : launch_osk_s<BLK, HD, false>(L, stream);
 }
 
 }  // namespace
