@@ -202,7 +202,7 @@ def peaks():
 
 def kernel_sha() -> str:
     h = hashlib.sha256()
-    for f in ("osk.cu", "ptx.cuh"):
+    for f in ("osk.cu", "osk_kernel.cuh", "ptx.cuh"):
         h.update(open(os.path.join(ROOT, "block_sparse_long_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
