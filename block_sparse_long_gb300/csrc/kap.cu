@@ -628,13 +628,13 @@ __global__ void __launch_bounds__(256) kap_exact_kernel(KapArgs a) {
 // fp32 dot (within 3 e_r of v1), re-evaluates the survivors in float64, and the CTA flags the blocks
 // of the keys that attain the exact maximum.
 template <int HD>
-__global__ void __launch_bounds__(256) kap_rescan_kernel(KapArgs a) {
+__global__ void __launch_bounds__(1024) kap_rescan_kernel(KapArgs a) {
   constexpr int kCand = 256;
   __shared__ float qf[HD];
   __shared__ double cval[kCand];
   __shared__ int ckey[kCand];
   __shared__ int ncand;
-  __shared__ double red[8];
+  __shared__ double red[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const long long n = a.amb[0];
   for (long long qi = blockIdx.x; qi < n; qi += gridDim.x) {
@@ -689,7 +689,7 @@ __global__ void __launch_bounds__(256) kap_rescan_kernel(KapArgs a) {
     for (int w = tid; w < a.words_per_row; w += blockDim.x) bits[w] = 0u;
     const int any_overflow = __syncthreads_or(overflow);
     double M = red[0];
-    for (int w = 1; w < 8; ++w) M = fmax(M, red[w]);
+    for (int w = 1; w < static_cast<int>(blockDim.x / 32); ++w) M = fmax(M, red[w]);
     const int nc = min(ncand, kCand);
     if (!any_overflow) {
       for (int x = tid; x < nc; x += blockDim.x)
@@ -1841,7 +1841,7 @@ cudaError_t launch_kap_t(KapArgs a, size_t qs_rows, size_t ks_rows, cudaStream_t
     const size_t rows = static_cast<size_t>(a.num_q_heads) * (static_cast<size_t>(a.total_tokens) / a.stride + a.num_reqs);
     const unsigned blocks = static_cast<unsigned>((rows + 31) / 32);   // 8 warps of 4 rows
     kap_exact_kernel<HD><<<blocks, 256, 0, stream>>>(a);
-    kap_rescan_kernel<HD><<<1024, 256, 0, stream>>>(a);
+    kap_rescan_kernel<HD><<<1024, 1024, 0, stream>>>(a);
   }
   kap_block_scores_kernel<KB><<<dim3(a.nqb_max, a.num_q_heads, a.num_reqs), 128, 0, stream>>>(a);
   int cap = kSelectThreads;   // the sort works on at least one key per thread
