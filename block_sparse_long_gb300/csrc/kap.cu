@@ -628,7 +628,7 @@ __global__ void __launch_bounds__(256) kap_exact_kernel(KapArgs a) {
 // fp32 dot (within 3 e_r of v1), re-evaluates the survivors in float64, and the CTA flags the blocks
 // of the keys that attain the exact maximum.
 template <int HD>
-__global__ void __launch_bounds__(1024) kap_rescan_kernel(KapArgs a) {
+__global__ void __launch_bounds__(512) kap_rescan_kernel(KapArgs a) {
   constexpr int kCand = 256;
   __shared__ float qf[HD];
   __shared__ double cval[kCand];
@@ -1841,7 +1841,7 @@ cudaError_t launch_kap_t(KapArgs a, size_t qs_rows, size_t ks_rows, cudaStream_t
     const size_t rows = static_cast<size_t>(a.num_q_heads) * (static_cast<size_t>(a.total_tokens) / a.stride + a.num_reqs);
     const unsigned blocks = static_cast<unsigned>((rows + 31) / 32);   // 8 warps of 4 rows
     kap_exact_kernel<HD><<<blocks, 256, 0, stream>>>(a);
-    kap_rescan_kernel<HD><<<1024, 1024, 0, stream>>>(a);
+    kap_rescan_kernel<HD><<<1024, 512, 0, stream>>>(a);
   }
   kap_block_scores_kernel<KB><<<dim3(a.nqb_max, a.num_q_heads, a.num_reqs), 128, 0, stream>>>(a);
   int cap = kSelectThreads;   // the sort works on at least one key per thread
