@@ -386,17 +386,22 @@ __global__ void __launch_bounds__(kLogitsThreads, 2)
     // stored one after another
     float* bm_row = a.bm + a.bm_off[b] + static_cast<int64_t>(h) * bm_block_base(nqb, KB) + bm_block_base(qblk, KB) +
                     static_cast<int64_t>(r - qblk * KB) * bm_pitch(qblk, KB);
-    constexpr int NG = 64 / KB;                   // key blocks in this thread's 64 columns
     for (int kt = 0; kt < nkt; ++kt) {
       const int ab = kt & 1;
       const bool okw = __all_sync(0xffffffffu,
                                   wait_parity_bounded(&sm.acc_full[ab], (kt >> 1) & 1, abort_flag, a.status));
       if (!okw) break;
       tc_fence_after();
-      uint32_t va[32], vb[32];
-      tmem_ld32(tmem + lane_addr + ab * 128 + g * 64, va);
-      tmem_ld32(tmem + lane_addr + ab * 128 + g * 64 + 32, vb);
+      // this thread's 64 logits as NG groups of KB columns (one key block each); each load also
+      // returns its group's maximum, which is the block maximum when every column is visible
+      constexpr int NG = 64 / KB;                 // key blocks in this thread's 64 columns
+      uint32_t vv[64];
+      float bmh[NG];
+#pragma unroll
+      for (int gg = 0; gg < NG; ++gg) tmem_ldn_max<KB>(tmem + lane_addr + ab * 128 + g * 64 + gg * KB, &vv[gg * KB], bmh[gg]);
       tmem_wait_ld();
+#pragma unroll
+      for (int gg = 0; gg < NG; ++gg) reg_after_wait(bmh[gg]);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.acc_free[ab]);
@@ -409,12 +414,7 @@ __global__ void __launch_bounds__(kLogitsThreads, 2)
       float bmg[NG];
       if (interior) {
 #pragma unroll
-        for (int gg = 0; gg < NG; ++gg) {
-          float m = __uint_as_float(gg * KB < 32 ? va[gg * KB] : vb[gg * KB - 32]);
-#pragma unroll
-          for (int e = gg * KB + 1; e < (gg + 1) * KB; ++e) m = fmaxf(m, __uint_as_float(e < 32 ? va[e] : vb[e - 32]));
-          bmg[gg] = m;
-        }
+        for (int gg = 0; gg < NG; ++gg) bmg[gg] = bmh[gg];
         // tile maximum from the block maxima; the first index and the tile's second largest value
         // are only needed when the running maximum rises (a few tiles per row)
         float t1 = bmg[0];
@@ -424,11 +424,11 @@ __global__ void __launch_bounds__(kLogitsThreads, 2)
           int e1 = 0;
 #pragma unroll
           for (int e = 63; e >= 0; --e)
-            if (__uint_as_float(e < 32 ? va[e] : vb[e - 32]) == t1) e1 = e;
+            if (__uint_as_float(vv[e]) == t1) e1 = e;
           float t2 = -INFINITY;
 #pragma unroll
           for (int e = 0; e < 64; ++e)
-            if (e != e1) t2 = fmaxf(t2, __uint_as_float(e < 32 ? va[e] : vb[e - 32]));
+            if (e != e1) t2 = fmaxf(t2, __uint_as_float(vv[e]));
           r2 = fmaxf(r1, t2);
           r1 = t1;
           rc1 = c0 + e1;
@@ -443,7 +443,7 @@ __global__ void __launch_bounds__(kLogitsThreads, 2)
         for (int e = 0; e < 64; ++e) {
           const uint32_t bits = e < 32 ? bits0 : bits1;
           const bool vis = row_ok && e <= last && ((bits >> (e & 31)) & 1u);
-          const float x = vis ? __uint_as_float(e < 32 ? va[e] : vb[e - 32]) : -INFINITY;
+          const float x = vis ? __uint_as_float(vv[e]) : -INFINITY;
           bmg[e / KB] = fmaxf(bmg[e / KB], x);
           r2 = fmaxf(r2, fminf(x, r1));
           rc1 = (x > r1) ? c0 + e : rc1;

@@ -541,22 +541,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           ki_pages = static_cast<uint32_t>(hd.y);
           ki_k = hd.z;
           if (ki_blk >= 0) {
+            // the load also reduces: pm = max of this thread's columns of S, before any mask
             tc_fence_after();
             if constexpr (SC == 64) {
               uint32_t r[64];
-              tmem_ld64(sbase, r);
+              tmem_ld64_max(sbase, r, pm);
               tmem_wait_ld();
+              reg_after_wait(pm);
 #pragma unroll
               for (int e = 0; e < 64; ++e) sv[e] = __uint_as_float(r[e]);
             } else {
-#pragma unroll
-              for (int cc = 0; cc < SC / 32; ++cc) {
-                uint32_t r[32];
-                tmem_ld32(sbase + cc * 32, r);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) sv[cc * 32 + e] = __uint_as_float(r[e]);
-              }
+              static_assert(SC == 32, "32 or 64 S columns per thread");
+              uint32_t r[32];
+              tmem_ld32_max(sbase, r, pm);
               tmem_wait_ld();
+              reg_after_wait(pm);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) sv[e] = __uint_as_float(r[e]);
             }
             tc_fence_before();
           }
@@ -568,21 +569,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int key0 = ki_blk * BLK;
             const bool need_mask = (ki_blk == i) || (key0 + BLK > L) || (ki_pages != all_pages) || !row_valid;
             if (need_mask) {
+              // masked columns leave the maximum: take it again over the masked values
               const int lim = row_valid ? min(pos, L - 1) - key0 : -1;  // last visible column
 #pragma unroll
               for (int e = 0; e < SC; ++e)
                 if (col0 + e > lim || !((ki_pages >> ((col0 + e) >> pshift)) & 1u)) sv[e] = -INFINITY;
+              static_assert(SC % 16 == 0, "16-column groups");
+              float m4[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) m4[q] = sv[q];
+#pragma unroll
+              for (int e = 4; e < SC; e += 4) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) m4[q] = fmaxf(m4[q], sv[e + q]);
+              }
+              pm = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
             }
-            static_assert(SC % 16 == 0, "16-column groups");
-            float m4[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) m4[q] = sv[q];
-#pragma unroll
-            for (int e = 4; e < SC; e += 4) {
-#pragma unroll
-              for (int q = 0; q < 4; ++q) m4[q] = fmaxf(m4[q], sv[e + q]);
-            }
-            pm = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
           }
         }
         // skip vote (Eq. (5)).  A row wants the block iff m_loc - max(m_run, m_loc) >= tau2; that
