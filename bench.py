@@ -1,6 +1,6 @@
 """Benchmark of CoSA sparse prefill (KAP + OSK) on one or more GB300s.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 4] [--impl cosa|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 128k_gqa_student_t] [--impl cosa|reference]
 
 One step is one pass of the whole hot path over the workload's batch:
 cosa_proxy_select (KAP: sampled logits, block scores, HRM-first ordered mask) followed by
@@ -22,9 +22,11 @@ import json
 import math
 import multiprocessing as mp
 import os
+import shutil
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 # BLAS threads pinned to one, so the oracle's core count is exactly the pool size
@@ -48,9 +50,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # --------------------------------------------------------------------------- #
 # workload and work accounting
 # --------------------------------------------------------------------------- #
-def delta_for(config: int) -> float:
+def delta_for(workload: str) -> float:
     cal = json.load(open(os.path.join(ROOT, "tests", "golden", "delta_calibration.json")))
-    return float(cal["configs"][str(config)]["delta"])
+    return float(cal["workloads"][workload]["delta"])
 
 
 def kap_flops(spec) -> float:
@@ -141,14 +143,15 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, bus_id: str):
+    def __init__(self, bus_id: str, keep: str = None):
         self.bus_id = bus_id
+        self.keep = keep            # optional path that receives the raw samples
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        fd, self.path = tempfile.mkstemp(prefix="cosa_clocks_", suffix=".csv")
+        os.close(fd)
 
     def __enter__(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", self.bus_id, f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.f,
@@ -176,6 +179,8 @@ class ClockSampler:
 
     def summary(self):
         if self.proc is None or not os.path.exists(self.path):
+            if os.path.exists(self.path):
+                os.remove(self.path)
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
@@ -191,6 +196,9 @@ class ClockSampler:
             for n, v in zip(names, parts[5:9]):
                 if v.lower() == "active":
                     reasons.add(n)
+        if self.keep:
+            shutil.copyfile(self.path, self.keep)
+        os.remove(self.path)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
@@ -358,7 +366,7 @@ def run_cosa(args, spec, workload_name, delta):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(bus_id) as clk:
+    with ClockSampler(bus_id, keep=args.clocks_log) as clk:
         start.record(stream)
         for s in range(args.steps):
             e0, e1, e2 = ev[s]
@@ -516,7 +524,7 @@ def run_sweep(args):
         return statistics.median(ts)
 
     for n_tok in (4096, 8192, 16384, 32768, 65536, 131072):
-        spec = synth.spec_for(4, lengths=(n_tok,), name=f"c4_structure_{n_tok // 1024}k")
+        spec = synth.spec_for("128k_gqa_student_t", lengths=(n_tok,), name=f"structure_{n_tok // 1024}k")
         delta = 15000.0 * n_tok / 131072
         w = synth.make_workload(spec)
         q, k, v = bf(w.q), bf(w.k_cache), bf(w.v_cache)
@@ -632,7 +640,7 @@ def run_ablation(args):
         return statistics.median(ts)
 
     def setup(n_tok):
-        spec = synth.spec_for(4, lengths=(n_tok,), name=f"c4_structure_{n_tok // 1024}k")
+        spec = synth.spec_for("128k_gqa_student_t", lengths=(n_tok,), name=f"structure_{n_tok // 1024}k")
         w = synth.make_workload(spec)
         t = dict(q=bf(w.q), k=bf(w.k_cache), v=bf(w.v_cache), pt=torch.from_numpy(w.page_table).to(dev),
                  cu=torch.from_numpy(w.cu_seqlens).to(dev))
@@ -661,8 +669,8 @@ def run_ablation(args):
         return m01[..., :nqb].contiguous(), l01.to(torch.int32).contiguous()
 
     if args.ablation == "union":
-        for cfg in (3, 4):
-            spec = synth.spec_for(cfg)
+        for wl in ("32k_gqa_shuffled", "128k_gqa_student_t"):
+            spec = synth.spec_for(wl)
             w = synth.make_workload(spec)
             t = dict(q=bf(w.q), k=bf(w.k_cache), pt=torch.from_numpy(w.page_table).to(dev),
                      cu=torch.from_numpy(w.cu_seqlens).to(dev))
@@ -763,9 +771,11 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", type=int, default=4, help="workload number (1-5); 4 = 128K GQA")
+    ap.add_argument("--workload", default="128k_gqa_student_t", choices=sorted(synth.WORKLOADS),
+                    help="workload name (default: one 128K-token request, 32 q / 8 kv heads)")
     ap.add_argument("--impl", choices=["cosa", "reference"], default="cosa")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clocks-log", default=None, help="also write the raw nvidia-smi clock samples here")
     ap.add_argument("--sweep", action="store_true",
                     help="time CoSA against the dense endpoint of the same kernel from 4K to 128K tokens")
     ap.add_argument("--ablation", choices=["remap", "jump", "topp", "union"],
@@ -779,7 +789,7 @@ def main():
     if args.ablation:
         return run_ablation(args)
     spec = synth.spec_for(args.workload)
-    delta = delta_for(args.workload) if args.workload != 1 else 2000.0
+    delta = delta_for(args.workload)
     name = spec.name
     if args.impl == "reference":
         return run_reference(args, spec, name, delta)

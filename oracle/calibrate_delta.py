@@ -6,8 +6,8 @@ ln(Delta / N) (CoSA Sec. 3.3 Eq. (5); App. D.1).  This script runs the oracle's
 KAP and OSK over a seeded sample of (request, head, query block) items for each
 Delta of a grid and keeps the smallest Delta whose realised budget is at or under
 the target; if none is, it keeps the largest Delta of the grid below the shortest
-request length.  Workload 1 uses Delta = 2000, the paper's Qwen3-8B operating
-point (App. D.1), for its skip-on case.
+request length.  The 2K single-head workload uses Delta = 2000, the paper's
+Qwen3-8B operating point (App. D.1), for its skip-on case.
 
 Writes tests/golden/delta_calibration.json.  Calls only the oracle (and the
 seeded input generator).  Run:  python -m oracle.calibrate_delta
@@ -32,6 +32,7 @@ from oracle import cosa_oracle as orc  # noqa: E402
 GRID = [100, 200, 300, 500, 700, 1000, 1500, 2000, 3000, 4000, 5000, 6000, 7000, 8000, 10000,
         15000, 20000]
 PAPER_DELTA_QWEN = 2000.0
+PAPER_DELTA_WORKLOAD = "2k_d64_1head"   # the single-head 2K workload takes the paper's Delta
 SAMPLE_ITEMS = 384
 SAMPLE_SEED = 777
 
@@ -47,8 +48,8 @@ def sample_items(spec):
     return sorted(items[k] for k in pick), f"{SAMPLE_ITEMS} items drawn uniformly (seed {SAMPLE_SEED})"
 
 
-def calibrate(config: int, log=print) -> dict:
-    spec = synth.spec_for(config)
+def calibrate(name: str, log=print) -> dict:
+    spec = synth.spec_for(name)
     t0 = time.time()
     w = synth.make_workload(spec)
     items, how = sample_items(spec)
@@ -78,7 +79,7 @@ def calibrate(config: int, log=print) -> dict:
     target = spec.stage2_budget_ppm / 1e6
     ok = [d for d in grid if computed[d] / cand <= target]
     delta = float(min(ok)) if ok else float(max(grid))
-    log(f"config {config}: delta {delta} realized {curve[str(int(delta))]:.4f} target {target} "
+    log(f"{name}: delta {delta} realized {curve[str(int(delta))]:.4f} target {target} "
         f"({len(items)} items, {time.time() - t0:.0f}s)")
     return {"delta": delta, "realized_budget": curve[str(int(delta))], "target_budget": target,
             "target_met": bool(ok), "curve": curve, "sample": how, "num_items": len(items)}
@@ -89,18 +90,18 @@ def main():
         "what": "skip scale Delta per workload, calibrated on the float64 oracle (CoSA Eq. (5), App. D.1)",
         "script": "oracle/calibrate_delta.py",
         "grid": GRID,
-        "configs": {},
+        "workloads": {},
     }
-    configs = [int(a) for a in sys.argv[1:]] or [1, 2, 3, 4, 5]
+    names = sys.argv[1:] or list(synth.WORKLOADS)
     path = os.path.join(ROOT, "tests", "golden", "delta_calibration.json")
     if os.path.exists(path):
-        out["configs"].update(json.load(open(path)).get("configs", {}))
-    for c in configs:
-        if c == 1:
-            out["configs"]["1"] = {"delta": PAPER_DELTA_QWEN, "delta_off": -1.0,
+        out["workloads"].update(json.load(open(path)).get("workloads", {}))
+    for name in names:
+        if name == PAPER_DELTA_WORKLOAD:
+            out["workloads"][name] = {"delta": PAPER_DELTA_QWEN, "delta_off": -1.0,
                                    "source": "CoSA App. D.1: Delta = 2000 for Qwen3-8B; Delta = -1 disables the skip"}
             continue
-        out["configs"][str(c)] = calibrate(c)
+        out["workloads"][name] = calibrate(name)
     with open(path, "w") as f:
         json.dump(out, f, indent=1, sort_keys=True)
     print("wrote", path)

@@ -18,7 +18,7 @@ Co-Designed Sparse Attention", arXiv 2607.25291v1, and the PageWeaver notes):
     A_i = {t : floor(t/P) in S_i, 0 <= t < L_i, t <= c_i}; invalid IDs add no
     interaction, duplicate pages count once, empty support gives zero.
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
   * stride sampling keeps positions 0, s, 2s, ...; causality on the sampled grid is c <= r;
   * the softmax of Eq. (8) runs over the causal, valid sampled keys of the row;
     a row with no valid key contributes nothing;

@@ -29,7 +29,7 @@ from typing import Dict, List, Optional, Sequence
 import numpy as np
 
 __all__ = [
-    "WorkloadSpec", "Workload", "CONFIGS", "make_workload", "f32_to_bf16_bits",
+    "WorkloadSpec", "Workload", "WORKLOADS", "make_workload", "f32_to_bf16_bits",
     "bf16_bits_to_f32", "inject_mask_noise", "spec_for",
 ]
 
@@ -75,7 +75,7 @@ class WorkloadSpec:
     salient_bump: float = 6.0         # mean logit bump of salient keys
     local_pages: int = 4              # local window: keys less than this many pages behind
     local_bump: float = 6.0           # logit bump inside the local window
-    literal_config1: bool = False     # config 1: iid Q, salient keys shifted by 4*sqrt(d) toward mean Q
+    iid_queries: bool = False         # iid Q, salient keys shifted by 4*sqrt(d) toward the mean Q
     tail_garbage_std: float = 100.0   # value std of cache slots past L (must never be read)
     mask_noise_frac: float = 0.0      # fraction of mask rows given duplicate / invalid IDs
 
@@ -110,25 +110,23 @@ _GQA = dict(num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=128, page_s
 
 # The five workloads of the CoSA long-context study, shaped after Qwen3-8B attention
 # (32 q heads / 8 kv heads, d = 128) at 2K-128K tokens.
-CONFIGS: Dict[int, WorkloadSpec] = {
-    1: WorkloadSpec(name="c1_2k_d64_1head", lengths=(2048,), num_q_heads=1, num_kv_heads=1,
-                    head_dim=64, block_size=64, page_size=64, stride=8,
-                    budget_ppm=250_000, stage2_budget_ppm=250_000, seed=20261203,
-                    salient_pages=4, literal_config1=True),
-    2: WorkloadSpec(name="c2_8k_gqa", lengths=(8192,), budget_ppm=200_000,
-                    stage2_budget_ppm=100_000, seed=20261204, **_GQA),
-    3: WorkloadSpec(name="c3_32k_gqa_shuffled", lengths=(32768,), budget_ppm=150_000,
-                    stage2_budget_ppm=50_000, seed=20261205, shuffle_pages=True, **_GQA),
-    4: WorkloadSpec(name="c4_128k_gqa_student_t", lengths=(131072,), budget_ppm=100_000,
-                    stage2_budget_ppm=30_000, seed=20261206, key_dist="student_t3", **_GQA),
-    5: WorkloadSpec(name="c5_ragged4_gqa_noisy_masks", lengths=(16384, 49152, 98304, 131072),
-                    budget_ppm=100_000, stage2_budget_ppm=40_000, seed=20261207,
-                    shuffle_pages=True, mask_noise_frac=0.05, **_GQA),
-}
+WORKLOADS: Dict[str, WorkloadSpec] = {s.name: s for s in (
+    WorkloadSpec(name="2k_d64_1head", lengths=(2048,), num_q_heads=1, num_kv_heads=1, head_dim=64,
+                 block_size=64, page_size=64, stride=8, budget_ppm=250_000, stage2_budget_ppm=250_000,
+                 seed=20261203, salient_pages=4, iid_queries=True),
+    WorkloadSpec(name="8k_gqa", lengths=(8192,), budget_ppm=200_000, stage2_budget_ppm=100_000,
+                 seed=20261204, **_GQA),
+    WorkloadSpec(name="32k_gqa_shuffled", lengths=(32768,), budget_ppm=150_000, stage2_budget_ppm=50_000,
+                 seed=20261205, shuffle_pages=True, **_GQA),
+    WorkloadSpec(name="128k_gqa_student_t", lengths=(131072,), budget_ppm=100_000, stage2_budget_ppm=30_000,
+                 seed=20261206, key_dist="student_t3", **_GQA),
+    WorkloadSpec(name="ragged4_gqa_noisy_masks", lengths=(16384, 49152, 98304, 131072), budget_ppm=100_000,
+                 stage2_budget_ppm=40_000, seed=20261207, shuffle_pages=True, mask_noise_frac=0.05, **_GQA),
+)}
 
 
-def spec_for(config: int, **overrides) -> WorkloadSpec:
-    s = CONFIGS[config]
+def spec_for(name: str, **overrides) -> WorkloadSpec:
+    s = WORKLOADS[name]
     return s.with_(**overrides) if overrides else s
 
 
@@ -204,7 +202,7 @@ def make_workload(spec: WorkloadSpec, *, with_values: bool = True) -> Workload:
 
     # shared query direction per kv group (u_g) and local-window directions
     u = _unit_rows(gs, Hkv, d)                                      # [Hkv, d]
-    a_q = 0.0 if spec.literal_config1 else spec.query_mean_norm
+    a_q = 0.0 if spec.iid_queries else spec.query_mean_norm
 
     # ---------------- Q ----------------
     qf = _draw(s_q, T, (Hq, d), "normal", chunk_rows=4096)          # [T, Hq, d] float32
@@ -213,7 +211,7 @@ def make_workload(spec: WorkloadSpec, *, with_values: bool = True) -> Workload:
     # local window: q(t) += a_loc * (w(seg) + w(seg-1)) / sqrt(2), k(t) += a_loc * w(seg);
     # segments of half the window, so keys in the current or previous segment get the bump
     seg_len = max(1, spec.local_pages * P // 2)
-    a_loc = math.sqrt(spec.local_bump * sqrt_d * math.sqrt(2.0)) if (spec.local_bump and not spec.literal_config1) else 0.0
+    a_loc = math.sqrt(spec.local_bump * sqrt_d * math.sqrt(2.0)) if (spec.local_bump and not spec.iid_queries) else 0.0
     local_dirs = []
     for b in range(B):
         n_seg = -(-lengths[b] // seg_len) + 1
@@ -227,7 +225,7 @@ def make_workload(spec: WorkloadSpec, *, with_values: bool = True) -> Workload:
 
     q_bits = f32_to_bf16_bits(qf)
     qmean_dir = None
-    if spec.literal_config1:
+    if spec.iid_queries:
         # unit mean query of each kv group, from the bf16 queries themselves
         qd = bf16_bits_to_f32(q_bits).astype(np.float64)
         qmean_dir = np.zeros((Hkv, d), dtype=np.float32)
@@ -261,7 +259,7 @@ def make_workload(spec: WorkloadSpec, *, with_values: bool = True) -> Workload:
         npg = n_pages[b]
         Lp = npg * P
         kf = _draw(k_children[b], Lp, (Hkv, d), spec.key_dist, chunk_rows=8192)
-        if spec.literal_config1:
+        if spec.iid_queries:
             # keys of the salient pages shifted by 4*sqrt(d) toward the unit mean query
             sal = gs.choice(np.arange(1, npg), size=min(spec.salient_pages, npg - 1), replace=False)
             for g in range(Hkv):
@@ -305,7 +303,7 @@ def make_workload(spec: WorkloadSpec, *, with_values: bool = True) -> Workload:
 
 
 # --------------------------------------------------------------------------- #
-# mask noise (config 5): duplicates and invalid IDs, injected after selection
+# mask noise (the ragged batch): duplicates and invalid IDs, injected after selection
 # --------------------------------------------------------------------------- #
 def inject_mask_noise(mask: np.ndarray, mask_len: np.ndarray, lengths: Sequence[int], block_size: int,
                       frac: float, seed: int, rows=None) -> tuple:

@@ -57,9 +57,9 @@ def test_kap_ascending_small(name, ppm):
         assert np.array_equal(m1, mo) and np.array_equal(l1, lo)
 
 
-def test_kap_ascending_config3_all_rows():
+def test_kap_ascending_32k_all_rows():
     """32K tokens, 32 heads: every row of the ascending mask is the sorted computation-order row."""
-    sp = synth.spec_for(3)
+    sp = synth.spec_for("32k_gqa_shuffled")
     w = synth.make_workload(sp)
     dw = gh.to_device(w)
     pitch = gh.C.stage1_pitch(sp.budget_ppm, sp.max_seqlen, sp.block_size)
@@ -107,12 +107,12 @@ def _assert_flags_map(flags_b, l01, flags_a, ids, lens):
                 assert (fb[rest] == orc.IGNORED).all()
 
 
-def test_osk_binary_config3_sampled():
+def test_osk_binary_32k_sampled():
     """32K tokens, 32 heads, calibrated Delta: binary-mask visiting against the oracle on sampled
     rows, and bit-identical to the ascending ID lists on every row."""
     from tests.test_gpu_full import sampled_items
-    sp = synth.spec_for(3)
-    delta = json.load(open(GOLDEN))["configs"]["3"]["delta"]
+    sp = synth.spec_for("32k_gqa_shuffled")
+    delta = json.load(open(GOLDEN))["workloads"]["32k_gqa_shuffled"]["delta"]
     w = synth.make_workload(sp)
     dw = gh.to_device(w)
     pitch = gh.C.stage1_pitch(sp.budget_ppm, sp.max_seqlen, sp.block_size)

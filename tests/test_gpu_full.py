@@ -31,9 +31,9 @@ def sampled_items(spec, n, seed):
     return sorted(items)
 
 
-def run_full(config, n_items, seed):
-    sp = synth.spec_for(config)
-    delta = json.load(open(GOLDEN))["configs"][str(config)]["delta"]
+def run_full(name, n_items, seed):
+    sp = synth.spec_for(name)
+    delta = json.load(open(GOLDEN))["workloads"][name]["delta"]
     w = synth.make_workload(sp)
     prm = gh.oracle_params(sp, delta)
     pitch = gh.C.stage1_pitch(sp.budget_ppm, sp.max_seqlen, sp.block_size)
@@ -62,19 +62,19 @@ def run_full(config, n_items, seed):
     return rep, flags
 
 
-def test_full_config3():
+def test_full_32k_shuffled():
     """32K tokens, shuffled physical pages, budgets 15 % / 5 %."""
-    rep, flags = run_full(3, 48, seed=3)
+    rep, flags = run_full("32k_gqa_shuffled", 48, seed=3)
     assert (flags == orc.SKIPPED).any()
 
 
-def test_full_config4():
+def test_full_128k_student_t():
     """128K tokens, Student-t keys, budgets 10 % / 3 %: the benchmark workload."""
-    rep, flags = run_full(4, 64, seed=4)
+    rep, flags = run_full("128k_gqa_student_t", 64, seed=4)
     assert (flags == orc.SKIPPED).any()
 
 
-def test_full_config5():
+def test_full_ragged_batch():
     """Ragged batch {16K, 48K, 96K, 128K}, duplicate and invalid IDs in 5 % of the mask rows."""
-    rep, flags = run_full(5, 64, seed=5)
+    rep, flags = run_full("ragged4_gqa_noisy_masks", 64, seed=5)
     assert (flags == orc.IGNORED).sum() > 0

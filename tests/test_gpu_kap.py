@@ -44,13 +44,13 @@ def test_kap_budgets(ppm):
     _kap_check(w, budget_ppm=ppm)
 
 
-def test_kap_config1():
-    w = synth.make_workload(synth.spec_for(1))
+def test_kap_2k_single_head():
+    w = synth.make_workload(synth.spec_for("2k_d64_1head"))
     _kap_check(w)
 
 
-def test_kap_config2_all_heads():
-    w = synth.make_workload(synth.spec_for(2))
+def test_kap_8k_all_heads():
+    w = synth.make_workload(synth.spec_for("8k_gqa"))
     ties = _kap_check(w)
     assert len(ties) < 5
 

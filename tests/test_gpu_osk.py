@@ -63,9 +63,9 @@ def test_osk_small_edge_cases(name, delta):
 
 
 @pytest.mark.parametrize("delta", [-1.0, 2000.0])
-def test_osk_config1(delta):
+def test_osk_2k_single_head(delta):
     """1 head, d = 64, 2048 tokens, page/block 64, budget 25 %, skip off and on (Delta = 2000)."""
-    sp = synth.spec_for(1)
+    sp = synth.spec_for("2k_d64_1head")
     w = synth.make_workload(sp)
     prm = gh.oracle_params(sp, delta)
     pitch = gh.C.stage1_pitch(sp.budget_ppm, sp.max_seqlen, sp.block_size)
@@ -76,10 +76,10 @@ def test_osk_config1(delta):
     gh.assert_osk_ok(rep)
 
 
-def test_osk_config2_sampled_heads():
+def test_osk_8k_sampled_heads():
     """GQA 32/8, d = 128, 8K tokens; GPU runs every item, the oracle checks three heads."""
-    sp = synth.spec_for(2)
-    delta = json.load(open(GOLDEN))["configs"]["2"]["delta"]
+    sp = synth.spec_for("8k_gqa")
+    delta = json.load(open(GOLDEN))["workloads"]["8k_gqa"]["delta"]
     w = synth.make_workload(sp)
     prm = gh.oracle_params(sp, delta)
     pitch = gh.C.stage1_pitch(sp.budget_ppm, sp.max_seqlen, sp.block_size)

@@ -53,12 +53,12 @@ def test_top_p_small(name, ppm):
         assert (len_g[b, :, nqb:] == 0).all() and (mask_g[b, :, nqb:] == -1).all()
 
 
-def test_top_p_full_pipeline_config3():
+def test_top_p_full_pipeline_32k():
     """32K tokens, 32 heads, p = 0.95 and the workload's Delta: KAP + OSK through the C ABI, the oracle
     on sampled (head, query block) items."""
     from tests.test_gpu_full import sampled_items
-    sp = synth.spec_for(3)
-    delta = json.load(open(GOLDEN))["configs"]["3"]["delta"]
+    sp = synth.spec_for("32k_gqa_shuffled")
+    delta = json.load(open(GOLDEN))["workloads"]["32k_gqa_shuffled"]["delta"]
     w = synth.make_workload(sp)
     items = sampled_items(sp, 24, seed=95)
     dw, p, prm, mask_g, len_g, rows, cuts = _run(w, 950_000, delta=delta, items=items)

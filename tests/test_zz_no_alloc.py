@@ -22,7 +22,7 @@ def _specs():
     small = synth.WorkloadSpec(name="no_alloc_ragged", lengths=(1500, 300, 129), num_q_heads=4, num_kv_heads=2,
                                head_dim=128, block_size=128, page_size=64, stride=16, budget_ppm=300_000,
                                stage2_budget_ppm=0, seed=77, shuffle_pages=True, salient_pages=3)
-    return [small, synth.spec_for(2)]
+    return [small, synth.spec_for("8k_gqa")]
 
 
 @pytest.mark.parametrize("spec", _specs(), ids=lambda s: s.name)
@@ -50,7 +50,7 @@ def test_static_scratch_matches_workspace_entry_point(spec):
 
 def test_static_scratch_refuses_oversized_problem():
     # the 128K-token GQA workload needs far more than the fixed scratch; refused on the host
-    spec = synth.spec_for(4)
+    spec = synth.spec_for("128k_gqa_student_t")
     L = spec.max_seqlen
     p = C.make_params(num_reqs=1, num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=128, page_size=64,
                       stride=16, total_tokens=L, max_seqlen=L, num_pages=L // 64, max_pages_per_req=L // 64,
