@@ -1,6 +1,6 @@
 // Kernel-Aware Proxy (KAP): computation-order mask from stride-sampled queries and keys.
 //
-// CoSA (arXiv 2607.25291) Sec. 4.2, Eqs. (8)-(14), Algorithm A lines 2-5.  For each
+// CoSA (arXiv 2607.25291) Sec. 4.2, Eqs. (8)-(14), Algorithm A (proxy stage).  For each
 // request and query head, with sampled rows r (positions r*s) and keys c (positions c*s):
 //   logits  l[r,c] = q~_r . k~_c * scale for causal (c <= r), existing keys;
 //   Eq. (9)-(10) reduce, for the row softmax of Eq. (8), to

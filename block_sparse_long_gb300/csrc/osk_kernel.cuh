@@ -1,6 +1,6 @@
 // Ordered-Skipping Kernel (OSK): block-sparse prefill attention over a paged KV cache.
 //
-// CoSA (arXiv 2607.25291), Sec. 4.3 and Algorithm A lines 7-22.  A persistent CTA per SM walks the
+// CoSA (arXiv 2607.25291), Sec. 4.3 and Algorithm A (ordered-skipping stage).  A persistent CTA per SM walks the
 // work items with a grid stride; an item is a (request, query head, query block) with the 128-row
 // tile of its query block (block_size 64 is padded to 128 rows), its ordered list of key blocks (the
 // computation-order mask M_KAP) and the online-softmax state of its rows.
@@ -521,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float tau2 = use_skip ? log2f(static_cast<float>(a.skip_delta)) - log2f(static_cast<float>(L)) : 0.0f;
       const size_t row_base = ((static_cast<size_t>(it.b) * a.num_q_heads + it.h) * a.nqb_max + i);
       uint8_t* flags_row = FLAGS ? a.visit_flags + row_base * a.mask_pitch : nullptr;
-      float m_run = -INFINITY;   // running max (log2 units), Algorithm A line 13
+      float m_run = -INFINITY;   // running max (log2 units), Algorithm A (running-max update)
       float m_ref = -INFINITY;   // max the exponentials are taken against
       float l_part = 0.0f;       // this half's share of the row sum l
       int c_item = 0;            // computed visits of this item

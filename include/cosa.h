@@ -5,7 +5,7 @@
  *
  *   cosa_proxy_select   the Kernel-Aware Proxy (KAP).  CoSA: "Accelerating Long-Context
  *                       Inference via Proxy-Kernel Co-Designed Sparse Attention",
- *                       Sec. 4.2, Eqs. (8)-(14), Algorithm A lines 2-5.  Scores each
+ *                       Sec. 4.2, Eqs. (8)-(14), Algorithm A (proxy stage).  Scores each
  *                       (query block, key block) pair from stride-sampled queries and
  *                       keys, flags the blocks that hold a sampled row's maximum (HRM),
  *                       and writes the computation-order mask M_KAP: per query block,
@@ -13,7 +13,7 @@
  *                       the stage-1 budget.
  *
  *   cosa_sparse_prefill the Ordered-Skipping Kernel (OSK).  Same paper, Sec. 4.3 and
- *                       Algorithm A lines 7-22: per query block, visits the mask's blocks
+ *                       Algorithm A (ordered-skipping stage): per query block, visits the mask's blocks
  *                       in order through the page table, keeps the exact running row
  *                       maximum, skips a block when every row's local maximum is more
  *                       than ln(N/Delta) below its running maximum (Eq. (5)), and
@@ -182,7 +182,7 @@ int cosa_proxy_select_static(const cosa_params* p, const void* q, const int32_t*
                              void* stream);
 
 /*
- * OSK: ordered-skipping sparse prefill (CoSA Sec. 4.3; Algorithm A lines 7-22).
+ * OSK: ordered-skipping sparse prefill (CoSA Sec. 4.3; Algorithm A (ordered-skipping stage)).
  *
  *   mask, mask_len  the visiting order per (request, head, query block); rows may hold
  *                   any IDs (see the conventions above).  Entries k < mask_len are visited

@@ -10,8 +10,8 @@ Sources (paper "CoSA: Accelerating Long-Context Inference via Proxy-Kernel
 Co-Designed Sparse Attention", arXiv 2607.25291v1, and the PageWeaver notes):
 
   * KAP block ranking, Sec. 4.2, Eqs. (8)-(12); flag-grouped sort, Eq. (13);
-    computation-order mask, Eq. (14); Algorithm A lines 2-5 (causal candidates).
-  * OSK, Sec. 4.3 and Algorithm A lines 7-22: ordered visits through the page
+    computation-order mask, Eq. (14); Algorithm A (proxy stage) (causal candidates).
+  * OSK, Sec. 4.3 and Algorithm A (ordered-skipping stage): ordered visits through the page
     table, running row max (Eqs. (1)-(2)), the skip rule of Eq. (5) tested against
     the updated running max, online-softmax rescaling.
   * Per-query output semantics, PageWeaver Sec. 2.1 Eqs. (1)-(2): the token set
@@ -23,7 +23,7 @@ Readings taken where the pages are silent:
   * the softmax of Eq. (8) runs over the causal, valid sampled keys of the row;
     a row with no valid key contributes nothing;
   * ties in Eq. (13) are broken by ascending block index, inside each group;
-  * candidates of query block i are the blocks j <= i (Algorithm A line 5);
+  * candidates of query block i are the blocks j <= i (Algorithm A (causal candidates));
   * the stage-1 budget is a fraction: K_i = ceil(budget_ppm * J_i / 1e6), J_i = i + 1;
     with top-p, K_i is the shortest prefix of rho_i whose scores reach p of the row's total;
   * the skip threshold uses the request's own length: ln(delta / L); delta <= 0
@@ -109,7 +109,7 @@ def direct_output(q: np.ndarray, K: np.ndarray, V: np.ndarray, tokens: Sequence[
 
 
 # --------------------------------------------------------------------------- #
-# KAP: Eqs. (8)-(14), Algorithm A lines 2-5
+# KAP: Eqs. (8)-(14), Algorithm A (proxy stage)
 # --------------------------------------------------------------------------- #
 @dataclass
 class KapRow:
@@ -237,7 +237,7 @@ def kap_mask(q_bits, k_bits, page_table, cu_seqlens, num_q_heads, num_kv_heads, 
 
 
 # --------------------------------------------------------------------------- #
-# OSK: Algorithm A lines 7-22 with the PageWeaver token-set semantics
+# OSK: Algorithm A (ordered-skipping stage) with the PageWeaver token-set semantics
 # --------------------------------------------------------------------------- #
 @dataclass
 class OskResult:

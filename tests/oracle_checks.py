@@ -184,7 +184,7 @@ def check_direct_definition(orc):
 
 
 # --------------------------------------------------------------------------- #
-# skip rule (Eq. 5, Algorithm A lines 12-15): hand-built cases with closed forms
+# skip rule (Eq. 5, Algorithm A (the skip test)): hand-built cases with closed forms
 # --------------------------------------------------------------------------- #
 def _skip_case(orc, delta, order):
     # one row (position 7), b = P = s = 1, d = 1, scale 1: logit of token t is k_t

@@ -1,5 +1,5 @@
 """OSK parity on the GPU: cosa_sparse_prefill through the C ABI against the float64 oracle,
-with the oracle's own KAP masks as input (CoSA Sec. 4.3, Algorithm A lines 7-22; PageWeaver
+with the oracle's own KAP masks as input (CoSA Sec. 4.3, Algorithm A (ordered-skipping stage); PageWeaver
 Sec. 2.1 output semantics)."""
 import json
 import math
