@@ -552,10 +552,38 @@ __global__ void __launch_bounds__(128) kap_block_scores_kernel(KapArgs a) {
 // ---------------------------------------------------------------------------
 // exact row maxima (float64) of each sampled row whose argmax fp32 certifies; one warp per row
 // ---------------------------------------------------------------------------
+// Sums carried as three fp32 values hi + lo + c.  Knuth's two-sum is an error-free transformation
+// (s + e == a + b exactly); every addition is taken through two-sums into the pair (hi, lo) except
+// the small third term c, which gathers the pair's own rounding errors.  On sums of 128 bf16
+// products this is at least as accurate as a float64 running sum (checked against exact rational
+// sums, down to mixed magnitudes 2^-12 .. 2^12), on the FP32 pipe.  The intrinsics keep the
+// compiler from contracting or reordering the additions.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+// (hi, lo, c) += y
+__device__ __forceinline__ void sum3_add(float& hi, float& lo, float& c, float y) {
+  float s, e, t, et;
+  two_sum(hi, y, s, e);
+  two_sum(e, lo, t, et);
+  two_sum(s, t, hi, lo);
+  c = __fadd_rn(c, et);
+}
+// (hi, lo, c) += (yh, yl, yc)
+__device__ __forceinline__ void sum3_add(float& hi, float& lo, float& c, float yh, float yl, float yc) {
+  float s, e, t, et, t2, et2;
+  two_sum(hi, yh, s, e);
+  two_sum(e, lo, t, et);
+  two_sum(t, yl, t2, et2);
+  two_sum(s, t2, hi, lo);
+  c = __fadd_rn(__fadd_rn(c, yc), __fadd_rn(et, et2));
+}
+
 template <int HD>
 __global__ void __launch_bounds__(256) kap_exact_kernel(KapArgs a) {
-  // four rows per warp, eight lanes per row: the float64 work of the row's dot product (its cost on
-  // GB300's slow FP64 pipe sets this kernel's time) takes three shuffle rounds instead of five
+  // four rows per warp, eight lanes per row: the row's dot product takes three shuffle rounds
   constexpr int RPW = 4, LPR = 32 / RPW, PER = HD / LPR;
   const int lane = threadIdx.x & 31, sub = lane % LPR, grp = lane / LPR;
   const int64_t gw = (static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5)) * RPW + grp;
@@ -593,18 +621,24 @@ __global__ void __launch_bounds__(256) kap_exact_kernel(KapArgs a) {
   const bool empty = v1 == -INFINITY;
   const bool certain = !empty && v2 < v1 - 2.0f * e_r;
   const uint16_t* kr = certain ? key_ptr(a, ri, b, kvh, a.c1[rec]) + sub * PER : qr;
-  double acc = 0.0;
+  // products of two bf16 values are exact in fp32 (8-bit significands); their sum is kept as three
+  // fp32 terms on the FP32 pipe (GB300's FP64 pipe runs at a small fraction of that rate and had set
+  // this kernel's time when the sum was a float64)
+  float hi = 0.0f, lo = 0.0f, cc = 0.0f;
 #pragma unroll
   for (int e = 0; e < PER; e += 8) {
     float kf[8];
     load8_bf16(kr + e, kf);
 #pragma unroll
-    // products of two bf16 values are exact in fp32 (8-bit significands), so acc + (double)(x * y)
-    // rounds exactly like fma((double)x, (double)y, acc) with one float64 conversion instead of two
-    for (int q = 0; q < 8; ++q) acc += static_cast<double>(qf[e + q] * kf[q]);
+    for (int q = 0; q < 8; ++q) sum3_add(hi, lo, cc, __fmul_rn(qf[e + q], kf[q]));
   }
 #pragma unroll
-  for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  for (int o = LPR / 2; o > 0; o >>= 1) {
+    const float oh = __shfl_xor_sync(0xffffffffu, hi, o), ol = __shfl_xor_sync(0xffffffffu, lo, o);
+    const float oc = __shfl_xor_sync(0xffffffffu, cc, o);
+    sum3_add(hi, lo, cc, oh, ol, oc);
+  }
+  const double acc = (static_cast<double>(hi) + static_cast<double>(lo)) + static_cast<double>(cc);
   if (!live || sub != 0) return;
   a.qnorm[rec] = qn;
   a.err[rec] = e_r;
