@@ -142,9 +142,9 @@ const char* cosa_status_string(int status);
  *              its content on entry does not matter and is undefined on exit.
  *
  * Selections are exact: the fp32 tensor-core scores carry error bounds, and every
- * order or cut they cannot certify is settled with float64 logits, so the mask equals
- * the one computed from exact real-number scores except where two scores agree to
- * within float64 rounding.  The top-p length is the exception: it is decided on the fp32
+ * order or cut they cannot certify is settled with logits at float64 accuracy or
+ * better, so the mask equals the one computed from exact real-number scores except
+ * where two scores agree to within float64 rounding.  The top-p length is the exception: it is decided on the fp32
  * scores, so it can differ from the exact one where the prefix mass is within the scores'
  * error of p times the total.  Stride sampling keeps token positions 0, s, 2s, ...;
  * ties in score go to the lower block ID.
