@@ -550,7 +550,8 @@ __global__ void __launch_bounds__(128) kap_block_scores_kernel(KapArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// exact row maxima (float64) of each sampled row whose argmax fp32 certifies; one warp per row
+// exact row maxima of the sampled rows whose fp32 arg max is certain (kept as float64); four rows
+// per warp
 // ---------------------------------------------------------------------------
 // Sums carried as three fp32 values hi + lo + c.  Knuth's two-sum is an error-free transformation
 // (s + e == a + b exactly); every addition is taken through two-sums into the pair (hi, lo) except
