@@ -125,8 +125,9 @@ WORKLOADS: Dict[str, WorkloadSpec] = {s.name: s for s in (
 )}
 
 
-def spec_for(name: str, **overrides) -> WorkloadSpec:
-    s = WORKLOADS[name]
+def spec_for(workload: str, **overrides) -> WorkloadSpec:
+    """The named workload's spec, with fields (the name among them) replaced by ``overrides``."""
+    s = WORKLOADS[workload]
     return s.with_(**overrides) if overrides else s
 
 
