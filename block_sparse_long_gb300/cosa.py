@@ -6,7 +6,7 @@ missing the calls raise; there is no fallback.
 
 The functions carry the C names:
   cosa_proxy_select    KAP  (CoSA Sec. 4.2, Eqs. (8)-(14))      -> mask, mask_len
-  cosa_sparse_prefill  OSK  (CoSA Sec. 4.3, Algorithm A 7-22)   -> out (and visit flags)
+  cosa_sparse_prefill  OSK  (CoSA Sec. 4.3, Algorithm A)       -> out (and visit flags)
   cosa_proxy_workspace_size, cosa_prefill_workspace_size, cosa_status_string, cosa_version
 """
 from __future__ import annotations

@@ -129,7 +129,7 @@ int cosa_version(void);
 const char* cosa_status_string(int status);
 
 /*
- * KAP: write the computation-order mask (CoSA Sec. 4.2, Eqs. (8)-(14); Algorithm A l. 2-5).
+ * KAP: write the computation-order mask (CoSA Sec. 4.2, Eqs. (8)-(14); Algorithm A, proxy stage).
  *
  *   q, cu_seqlens, k_cache, page_table   inputs as above (V is not read)
  *   mask       out: for every request b, head h and query block i < ceil(L_b / b):
