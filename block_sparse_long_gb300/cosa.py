@@ -144,13 +144,37 @@ def _check(t: torch.Tensor, name: str, dtype: torch.dtype):
         raise ValueError(f"{name} must be contiguous")
 
 
+def required_numel(p: CosaParams) -> dict:
+    """Elements each buffer must hold at least, for the parameters ``p``, so that the library stays
+    inside it (the layouts of include/cosa.h: q and out [T, Hq, d], caches [num_pages, P, Hkv, d],
+    cu_seqlens [B + 1], page_table [B, max_pages_per_req], mask and visit_flags
+    [B, Hq, nqb_max, mask_pitch], mask_len [B, Hq, nqb_max], status [1])."""
+    nqb_max = -(-p.max_seqlen // p.block_size)
+    rows = p.num_reqs * p.num_q_heads * nqb_max
+    cache = p.num_pages * p.page_size * p.num_kv_heads * p.head_dim
+    tokens = p.total_tokens * p.num_q_heads * p.head_dim
+    return {"q": tokens, "out": tokens, "k_cache": cache, "v_cache": cache, "cu_seqlens": p.num_reqs + 1,
+            "page_table": p.num_reqs * p.max_pages_per_req, "mask": rows * p.mask_pitch,
+            "visit_flags": rows * p.mask_pitch, "mask_len": rows, "status": 1}
+
+
+def validate_buffers(p: CosaParams, **buffers: Optional[torch.Tensor]) -> None:
+    """Raise ValueError if a given buffer is smaller than the parameters say it is.  The library
+    reads and writes the sizes ``p`` implies and cannot see the tensors' own sizes."""
+    need = required_numel(p)
+    for name, t in buffers.items():
+        if t is not None and t.numel() < need[name]:
+            raise ValueError(f"{name} holds {t.numel()} elements; the parameters need at least {need[name]}")
+
+
 def params_for(q: torch.Tensor, k_cache: torch.Tensor, page_table: torch.Tensor, cu_seqlens: torch.Tensor, *,
                block_size: int, max_seqlen: int, stride: Optional[int] = None, budget_ppm: int = 1_000_000,
                mask_pitch: Optional[int] = None, skip_delta: float = -1.0,
                sm_scale: Optional[float] = None, flags: int = 0) -> CosaParams:
     T, Hq, d = q.shape
     num_pages, P, Hkv, d2 = k_cache.shape
-    assert d == d2
+    if d != d2:
+        raise ValueError(f"q has head dim {d}, k_cache {d2}")
     B = cu_seqlens.numel() - 1
     if mask_pitch is None:
         mask_pitch = stage1_pitch(budget_ppm, max_seqlen, block_size)
@@ -170,6 +194,11 @@ def cosa_proxy_select(p: CosaParams, q: torch.Tensor, cu_seqlens: torch.Tensor, 
     _check(k_cache, "k_cache", torch.bfloat16)
     _check(cu_seqlens, "cu_seqlens", torch.int32)
     _check(page_table, "page_table", torch.int32)
+    for t, n in ((mask, "mask"), (mask_len, "mask_len"), (status, "status")):
+        if t is not None:
+            _check(t, n, torch.int32)
+    validate_buffers(p, q=q, k_cache=k_cache, cu_seqlens=cu_seqlens, page_table=page_table, mask=mask,
+                     mask_len=mask_len, status=status)
     dev = q.device
     nqb_max = -(-p.max_seqlen // p.block_size)
     if mask is None:
@@ -180,7 +209,8 @@ def cosa_proxy_select(p: CosaParams, q: torch.Tensor, cu_seqlens: torch.Tensor, 
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     rc = library().cosa_proxy_select(ctypes.byref(p), _ptr(q), _ptr(cu_seqlens), _ptr(k_cache), _ptr(page_table),
-                                     _ptr(mask), _ptr(mask_len), _ptr(workspace), workspace.numel(),
+                                     _ptr(mask), _ptr(mask_len), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(),
                                      _ptr(status), _stream_handle(stream))
     if rc != COSA_OK:
         raise CosaError(rc, "cosa_proxy_select")
@@ -198,6 +228,10 @@ def cosa_proxy_select_static(p: CosaParams, q: torch.Tensor, cu_seqlens: torch.T
                      (cu_seqlens, "cu_seqlens", torch.int32), (page_table, "page_table", torch.int32),
                      (mask, "mask", torch.int32), (mask_len, "mask_len", torch.int32)):
         _check(t, n, dt)
+    if status is not None:
+        _check(status, "status", torch.int32)
+    validate_buffers(p, q=q, k_cache=k_cache, cu_seqlens=cu_seqlens, page_table=page_table, mask=mask,
+                     mask_len=mask_len, status=status)
     rc = library().cosa_proxy_select_static(ctypes.byref(p), _ptr(q), _ptr(cu_seqlens), _ptr(k_cache),
                                             _ptr(page_table), _ptr(mask), _ptr(mask_len), _ptr(status),
                                             _stream_handle(stream))
@@ -220,10 +254,15 @@ def cosa_sparse_prefill(p: CosaParams, q: torch.Tensor, cu_seqlens: torch.Tensor
         _check(t, n, dt)
     if out is None:
         out = torch.empty_like(q)
+    _check(out, "out", torch.bfloat16)
     if visit_flags is not None:
         _check(visit_flags, "visit_flags", torch.uint8)
+    if status is not None:
+        _check(status, "status", torch.int32)
+    validate_buffers(p, q=q, k_cache=k_cache, v_cache=v_cache, cu_seqlens=cu_seqlens, page_table=page_table,
+                     mask=mask, mask_len=mask_len, out=out, visit_flags=visit_flags, status=status)
     need = cosa_prefill_workspace_size(p)
-    ws_bytes = 0 if workspace is None else workspace.numel()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     if need > ws_bytes:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
         ws_bytes = need

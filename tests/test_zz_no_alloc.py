@@ -7,6 +7,8 @@ library.  This file checks, through the C ABI, that it produces exactly the mask
 cosa_proxy_select (which takes a workspace) on two calls in a row, and that a problem
 larger than the fixed scratch is refused.  It is named so that pytest collects it last.
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -58,6 +60,12 @@ def test_static_scratch_refuses_oversized_problem():
     assert C.cosa_proxy_workspace_size(p) > C.STATIC_SCRATCH_BYTES
     t = torch.zeros(16, dtype=torch.int32, device="cuda")
     q = torch.zeros(16, dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(C.CosaError) as e:
+    # the binding refuses buffers smaller than the parameters imply ...
+    with pytest.raises(ValueError):
         C.cosa_proxy_select_static(p, q, t, q, t, t, t)
-    assert e.value.code == C.COSA_ERR_WORKSPACE
+    # ... and the library refuses the problem itself, on the host, before it touches any buffer
+    vp = ctypes.c_void_p
+    rc = C.library().cosa_proxy_select_static(ctypes.byref(p), vp(q.data_ptr()), vp(t.data_ptr()), vp(q.data_ptr()),
+                                              vp(t.data_ptr()), vp(t.data_ptr()), vp(t.data_ptr()), None,
+                                              vp(torch.cuda.current_stream().cuda_stream))
+    assert rc == C.COSA_ERR_WORKSPACE
