@@ -13,10 +13,10 @@
  *                       the stage-1 budget.
  *
  *   cosa_sparse_prefill the Ordered-Skipping Kernel (OSK).  Same paper, Sec. 4.3 and
- *                       Algorithm A (ordered-skipping stage): per query block, visits the mask's blocks
- *                       in order through the page table, keeps the exact running row
- *                       maximum, skips a block when every row's local maximum is more
- *                       than ln(N/Delta) below its running maximum (Eq. (5)), and
+ *                       Algorithm A (ordered-skipping stage): per query block, visits the
+ *                       mask's blocks in order through the page table, keeps the exact
+ *                       running row maximum, skips a block when every row's local maximum
+ *                       is more than ln(N/Delta) below its running maximum (Eq. (5)), and
  *                       accumulates exact online softmax over the rest.  The output of
  *                       each query is the softmax-weighted sum over its token set as the
  *                       PageWeaver notes define it (Sec. 2.1, Eqs. (1)-(2)): tokens of
@@ -78,7 +78,7 @@ extern "C" {
 #define COSA_FLAG_TEST_STALL 1
 /* Ablation switch of cosa_proxy_select (ignored by cosa_sparse_prefill): write the same K_i selected
    blocks in ascending block order instead of the computation order rho_i of Eq. (14), i.e. visiting
-   without KV page remapping (the "w/o remap" arm of the paper's Sec. 5.4, Fig. 6 and App. D.4). */
+   without KV page remapping (the no-remapping arm of the paper's Sec. 5.4, Fig. 6 and App. D.4). */
 #define COSA_FLAG_ASCENDING_ORDER 2
 /* Ablation switch of cosa_sparse_prefill (ignored by cosa_proxy_select): read each mask row as the
    binary block mask M_01 of the paper's Eq. (3) instead of a list of block IDs.  Entry j != 0 selects
@@ -144,9 +144,9 @@ const char* cosa_status_string(int status);
  * Selections are exact: the fp32 tensor-core scores carry error bounds, and every
  * order or cut they cannot certify is settled with logits at float64 accuracy or
  * better, so the mask equals the one computed from exact real-number scores except
- * where two scores agree to within float64 rounding.  The top-p length is the exception: it is decided on the fp32
- * scores, so it can differ from the exact one where the prefix mass is within the scores'
- * error of p times the total.  Stride sampling keeps token positions 0, s, 2s, ...;
+ * where two scores agree to within float64 rounding.  The top-p length is the
+ * exception: it is decided on the fp32 scores, so it can differ from the exact one
+ * where the prefix mass is within the scores' error of p times the total.  Stride sampling keeps token positions 0, s, 2s, ...;
  * ties in score go to the lower block ID.
  */
 size_t cosa_proxy_workspace_size(const cosa_params* p);
