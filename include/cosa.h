@@ -146,8 +146,8 @@ const char* cosa_status_string(int status);
  * better, so the mask equals the one computed from exact real-number scores except
  * where two scores agree to within float64 rounding.  The top-p length is the
  * exception: it is decided on the fp32 scores, so it can differ from the exact one
- * where the prefix mass is within the scores' error of p times the total.  Stride sampling keeps token positions 0, s, 2s, ...;
- * ties in score go to the lower block ID.
+ * where the prefix mass is within the scores' error of p times the total.  Stride
+ * sampling keeps token positions 0, s, 2s, ...; ties in score go to the lower block ID.
  */
 size_t cosa_proxy_workspace_size(const cosa_params* p);
 int cosa_proxy_select(const cosa_params* p, const void* q, const int32_t* cu_seqlens, const void* k_cache,
