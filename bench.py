@@ -13,6 +13,11 @@ Work accounting (algorithmic FLOPs, the same for every implementation):
        computed block (P V), b = block size, d = head dim;
   KAP  2*d per causal (sampled row, sampled key) pair.
 Prints one JSON line (rank 0).
+
+Other modes (one JSON line per measurement, not the bench line): --sweep (CoSA against the dense
+endpoint of the same kernel, 4K to 128K tokens), --ablation remap|jump|topp|union (skip ratio
+against Delta with and without page remapping, physical jumps against logical skipping of a binary
+mask, the top-p stage-1 rule, GQA page reuse), --clocks-log PATH (keep the raw clock samples).
 """
 from __future__ import annotations
 
