@@ -56,6 +56,22 @@ int check_common(const cosa_params* p) {
   return COSA_OK;
 }
 
+// Checks of the KAP parameters (stride, budget, mask pitch), shared by the workspace-size query and
+// both select calls, so that no size is computed for a problem the calls would refuse.
+int check_kap(const cosa_params* p) {
+  const int rc = check_common(p);
+  if (rc != COSA_OK) return rc;
+  if (p->stride < 1 || p->block_size % p->stride != 0) return COSA_ERR_INVALID_ARG;
+  const int kb = p->block_size / p->stride;
+  if (kb != 4 && kb != 8 && kb != 16) return COSA_ERR_UNSUPPORTED;
+  if (p->budget_ppm < 1 || p->budget_ppm > 1000000) return COSA_ERR_INVALID_ARG;
+  const int64_t nqb_max = ceil_div(p->max_seqlen, p->block_size);
+  if (nqb_max > kMaxQueryBlocksKap) return COSA_ERR_UNSUPPORTED;
+  if (p->mask_pitch < ceil_div(static_cast<int64_t>(p->budget_ppm) * nqb_max, 1000000)) return COSA_ERR_INVALID_ARG;
+  if ((p->flags & COSA_FLAG_TOP_P) && p->mask_pitch < nqb_max) return COSA_ERR_INVALID_ARG;
+  return COSA_OK;
+}
+
 }  // namespace
 
 bool cosa::encode_tiled_bf16(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
@@ -94,7 +110,7 @@ const char* cosa_status_string(int status) {
 }
 
 size_t cosa_proxy_workspace_size(const cosa_params* p) {
-  if (check_common(p) != COSA_OK) return 0;
+  if (check_kap(p) != COSA_OK) return 0;
   return cosa::kap_workspace_bytes(p->num_reqs, p->num_q_heads, p->num_kv_heads, p->block_size, p->stride,
                                    p->total_tokens, p->max_seqlen);
 }
@@ -102,16 +118,8 @@ size_t cosa_proxy_workspace_size(const cosa_params* p) {
 int cosa_proxy_select(const cosa_params* p, const void* q, const int32_t* cu_seqlens, const void* k_cache,
                       const int32_t* page_table, int32_t* mask, int32_t* mask_len, void* workspace,
                       size_t workspace_bytes, int32_t* device_status, void* stream) {
-  int rc = check_common(p);
+  const int rc = check_kap(p);
   if (rc != COSA_OK) return rc;
-  if (p->stride < 1 || p->block_size % p->stride != 0) return COSA_ERR_INVALID_ARG;
-  const int kb = p->block_size / p->stride;
-  if (kb != 4 && kb != 8 && kb != 16) return COSA_ERR_UNSUPPORTED;
-  if (p->budget_ppm < 1 || p->budget_ppm > 1000000) return COSA_ERR_INVALID_ARG;
-  const int64_t nqb_max = ceil_div(p->max_seqlen, p->block_size);
-  if (nqb_max > kMaxQueryBlocksKap) return COSA_ERR_UNSUPPORTED;
-  if (p->mask_pitch < ceil_div(static_cast<int64_t>(p->budget_ppm) * nqb_max, 1000000)) return COSA_ERR_INVALID_ARG;
-  if ((p->flags & COSA_FLAG_TOP_P) && p->mask_pitch < nqb_max) return COSA_ERR_INVALID_ARG;
   if (!q || !cu_seqlens || !k_cache || !page_table || !mask || !mask_len || !workspace) return COSA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(cu_seqlens, 4) || !aligned(page_table, 4) ||
       !aligned(mask, 4) || !aligned(mask_len, 4))
@@ -150,10 +158,10 @@ int cosa_proxy_select(const cosa_params* p, const void* q, const int32_t* cu_seq
 int cosa_proxy_select_static(const cosa_params* p, const void* q, const int32_t* cu_seqlens, const void* k_cache,
                              const int32_t* page_table, int32_t* mask, int32_t* mask_len, int32_t* device_status,
                              void* stream) {
-  const int rc = check_common(p);
+  const int rc = check_kap(p);
   if (rc != COSA_OK) return rc;
   const size_t need = cosa_proxy_workspace_size(p);
-  if (need > cosa::kStaticScratchBytes) return COSA_ERR_WORKSPACE;
+  if (need == 0 || need > cosa::kStaticScratchBytes) return COSA_ERR_WORKSPACE;
   void* scratch = nullptr;
   if (cosa::kap_static_scratch(&scratch) != cudaSuccess) return COSA_ERR_CUDA;
   return cosa_proxy_select(p, q, cu_seqlens, k_cache, page_table, mask, mask_len, scratch, cosa::kStaticScratchBytes,

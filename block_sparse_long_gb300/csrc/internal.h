@@ -69,8 +69,8 @@ size_t kap_workspace_bytes(int num_reqs, int num_q_heads, int num_kv_heads, int 
 
 // Fixed device scratch of cosa_proxy_select_static (defined in kap.cu).
 constexpr size_t kStaticScratchBytes = size_t(64) << 20;
-constexpr int kMaxStaticDevices = 64;
-// Device address of that scratch on the current device (looked up on the first call per device).
+constexpr int kMaxStaticContexts = 64;
+// Device address of that scratch in the current context (looked up on the first call per context).
 cudaError_t kap_static_scratch(void** ptr);
 cudaError_t launch_kap(const KapLaunch& L, cudaStream_t stream);
 

@@ -12,26 +12,32 @@
 //   Eq. (14) M_KAP[i, 0:K_i] = rho_i[0:K_i], K_i = ceil(B1 * (i+1)).
 //
 // Exactness.  The logits run on tcgen05 tensor cores in fp32; every decision that fp32 could
-// get wrong is settled in float64:
-//   gather                       the sampled queries and keys are packed into contiguous arrays;
-//   pass 1 (kap_logits<ROWMAX>)  per row: largest fp32 logit, its key, and the largest over the
-//                                 other keys (branch-free);
-//   kap_exact                    per row: error bound e_r >= |fp32 logit - exact logit| for every
-//                                 key of the row (from ||q_r|| * max ||k|| and the accumulation
-//                                 length); if the runner-up is more than 2 e_r below the maximum
-//                                 the argmax key is certain and M_r is its float64 logit;
-//   kap_rescan                   rows where it is not: every key within 3 e_r of the largest is
-//                                 re-evaluated in float64; the HRM blocks of the row follow exactly;
-//   pass 2 (kap_logits<SCORES>)  per (query block, key block): fp32 score and a rigorous bound
-//                                 on its error, given the float64 M_r;
-//   kap_select                   flag-grouped sort of the fp32 scores; every adjacent pair whose
-//                                 order, and the budget cut, that the bounds cannot certify is
-//                                 recomputed with float64 logits and exp, and re-sorted.
+// get wrong is settled at float64 accuracy or better.  The kernels, in launch order:
+//   kap_setup                per-request offsets into the workspace, zeroed key norms;
+//   kap_gather               the sampled queries and keys packed into contiguous 128-row padded
+//                            arrays, a validity bit per key, the largest key norm per key block;
+//   kap_logits               one tensor-core pass over every causal (sampled row, sampled key) tile:
+//                            per row the largest fp32 logit, its key and the largest over the other
+//                            keys, and per (row, key block) the block maximum of Eq. (9), stored;
+//   kap_exact                per row: error bound e_r >= |fp32 logit - exact logit| for every key of
+//                            the row (from ||q_r|| * max ||k|| and the accumulation model of kKappa);
+//                            if the runner-up is more than 2 e_r below the maximum the argmax key is
+//                            certain and M_r is its exact logit (three-term fp32 sum);
+//   kap_rescan               rows where it is not: every key within 3 e_r of the largest is
+//                            re-evaluated in float64; the HRM blocks of the row follow exactly;
+//   kap_block_scores         per (query block, key block): fp32 score from the stored block maxima
+//                            and the exact M_r, with a rigorous bound on its error;
+//   kap_select_warp          a warp per mask row: top-K by radix select, sort, certification of
+//                            every adjacent pair and of the budget cut against the bounds, float64
+//                            repair of the uncertain positions; rows it cannot settle are listed;
+//   kap_select               a block per listed row: the same with a full sort (top-p, ascending
+//                            order, long rows, cuts the sentinel cannot certify).
 #include <cstdint>
 #include <mutex>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include "cosa.h"
 #include "internal.h"
@@ -1925,23 +1931,76 @@ size_t kap_workspace_bytes(int num_reqs, int num_q_heads, int num_kv_heads, int 
   return n + 256;
 }
 
+namespace {
+// Driver calls that identify the current context, reached through the runtime's entry-point query
+// (the library links no driver stub).
+struct CtxFns {
+  PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  PFN_cuCtxGetId_v12000 get_id = nullptr;
+};
+const CtxFns& ctx_fns() {
+  static CtxFns f;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      f.get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      f.get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+  });
+  return f;
+}
+
+// Identifier of the context current on this thread (unique for the life of the process), or 0 if
+// there is none or it cannot be read.
+unsigned long long current_ctx_id() {
+  const CtxFns& f = ctx_fns();
+  if (f.get_current == nullptr || f.get_id == nullptr) return 0;
+  CUcontext ctx = nullptr;
+  if (f.get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  unsigned long long id = 0;
+  if (f.get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+}  // namespace
+
 cudaError_t kap_static_scratch(void** ptr) {
-  // Host code cannot use the array's name as a device address: look the address up, once per
-  // device, with that device current.
+  // Host code cannot use the array's name as a device address: look the address up with the
+  // device current.  The array lives in the module loaded into a context, so the address is cached
+  // per context (a context created after cudaDeviceReset, or another context made current through
+  // the driver API, gets its own lookup).
   static std::mutex mu;
-  static void* addr[kMaxStaticDevices] = {};
+  static unsigned long long ids[kMaxStaticContexts] = {};
+  static void* addr[kMaxStaticContexts] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxStaticDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, cosa_kap_static_scratch);
-    if (e != cudaSuccess) return e;
-    addr[dev] = p;
+  unsigned long long id = current_ctx_id();
+  if (id != 0) {
+    for (int s = 0; s < kMaxStaticContexts; ++s)
+      if (ids[s] == id) {
+        *ptr = addr[s];
+        return cudaSuccess;
+      }
   }
-  *ptr = addr[dev];
+  // not cached: the lookup itself makes the device's primary context current if no context is
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, cosa_kap_static_scratch);
+  if (e != cudaSuccess) return e;
+  if (id == 0) id = current_ctx_id();
+  if (id != 0) {
+    int s = 0;
+    while (s < kMaxStaticContexts && ids[s] != 0) ++s;
+    if (s == kMaxStaticContexts) s = static_cast<int>(id % kMaxStaticContexts);   // table full: replace one
+    ids[s] = id;
+    addr[s] = p;
+  }
+  *ptr = p;
   return cudaSuccess;
 }
 

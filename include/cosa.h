@@ -149,6 +149,7 @@ const char* cosa_status_string(int status);
  * where the prefix mass is within the scores' error of p times the total.  Stride
  * sampling keeps token positions 0, s, 2s, ...; ties in score go to the lower block ID.
  */
+/* Bytes of workspace cosa_proxy_select needs for `p`; 0 if cosa_proxy_select would refuse `p`. */
 size_t cosa_proxy_workspace_size(const cosa_params* p);
 int cosa_proxy_select(const cosa_params* p, const void* q, const int32_t* cu_seqlens, const void* k_cache,
                       const int32_t* page_table, int32_t* mask, int32_t* mask_len, void* workspace,
@@ -169,9 +170,12 @@ int cosa_proxy_select(const cosa_params* p, const void* q, const int32_t* cu_seq
  *
  *   - Size limit: a problem whose cosa_proxy_workspace_size(p) exceeds COSA_STATIC_SCRATCH_BYTES
  *     is rejected with COSA_ERR_WORKSPACE before anything is enqueued.
- *   - The first call on a device looks up the array's device address with that device
- *     current (a runtime call that does not allocate); make that first call before any stream
- *     capture begins on that device.
+ *   - The first call in a CUDA context (normally the device's primary context) looks up the
+ *     array's device address with that device current (a runtime call that does not allocate)
+ *     and keeps it for that context; make that first call before any stream capture begins on
+ *     that device.  A context created later (after cudaDeviceReset, or another context made
+ *     current through the driver API) gets its own lookup on its first call.
+ *   - Invalid parameters are refused exactly as cosa_proxy_select refuses them.
  *   - Every call shares the one array and leaves its contents behind; the kernels initialise
  *     everything they read.  Calls whose work overlaps on the GPU (different streams, or
  *     several host threads on one device) race on the array: order them on one stream.

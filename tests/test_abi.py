@@ -91,6 +91,24 @@ def test_host_validation(lib):
     assert osk(_params(lib, total_tokens=0)) == lib.COSA_OK                 # nothing to do
 
 
+def test_kap_stride_validation(lib):
+    """A stride of 0, or one that does not divide the block, is refused by the workspace query and
+    by both select calls before any size is computed (no division by the stride on the host)."""
+    L = lib.library()
+    fake = ctypes.c_void_p(4096)
+    for stride, code in ((0, lib.COSA_ERR_INVALID_ARG), (3, lib.COSA_ERR_INVALID_ARG),
+                         (-16, lib.COSA_ERR_INVALID_ARG), (64, lib.COSA_ERR_UNSUPPORTED)):
+        p = _params(lib, stride=stride)
+        assert lib.cosa_proxy_workspace_size(p) == 0, stride
+        rc = L.cosa_proxy_select(ctypes.byref(p), fake, fake, fake, fake, fake, fake, fake, 1 << 30, None, None)
+        assert rc == code, (stride, rc)
+        rc = L.cosa_proxy_select_static(ctypes.byref(p), fake, fake, fake, fake, fake, fake, None, None)
+        assert rc == code, (stride, rc)
+    # a budget or mask pitch the select calls refuse gives no workspace size either
+    assert lib.cosa_proxy_workspace_size(_params(lib, budget_ppm=0)) == 0
+    assert lib.cosa_proxy_workspace_size(_params(lib, mask_pitch=3)) == 0
+
+
 def test_workspace_sizes(lib):
     p = _params(lib)
     n = lib.cosa_proxy_workspace_size(p)
