@@ -5,6 +5,6 @@ package.  It shares no code with the CUDA path.
 """
 from .cosa_oracle import *  # noqa: F401,F403
 from .cosa_oracle import (COMPUTED, SKIPPED, IGNORED, Params, decode_bf16, token_set, direct_output,
-                          kap_request_head, kap_mask, osk_qblock, osk_all, realized_budget,
+                          kap_request_head, kap_mask, osk_qblock, osk_all,
                           stage1_count, flag_grouped_order, request_keys, request_queries,
-                          computed_tokens, kap_pbar_rows, kap_sampled)
+                          kap_pbar_rows, kap_sampled)

@@ -345,14 +345,6 @@ def osk_qblock_binary(Q: np.ndarray, K: np.ndarray, V: np.ndarray, exists: np.nd
     return OskResult(out=r.out, flags=flags, margins=margins, row_max=r.row_max, row_sum=r.row_sum)
 
 
-def computed_tokens(flags: np.ndarray, mask_row: Sequence[int], L: int, b: int, exists: np.ndarray,
-                    row_pos: int) -> List[int]:
-    """Token set of one query row: PageWeaver Eq. (1) over the blocks the OSK computed."""
-    blocks = [int(mask_row[k]) for k in range(len(flags)) if flags[k] == COMPUTED]
-    toks = token_set(blocks, b, L, row_pos)
-    return [t for t in toks if exists[t]]
-
-
 def osk_all(q_bits, k_bits, v_bits, page_table, cu_seqlens, num_q_heads, num_kv_heads, prm: Params,
             mask, mask_len, items: Optional[Sequence[Tuple[int, int, int]]] = None, force=None,
             binary: bool = False):
@@ -420,13 +412,3 @@ def ordered_shared_loads(orders: Sequence[Sequence[int]]) -> int:
                 pos[h] += 1
         loads += 1
     return loads
-
-
-def realized_budget(results: dict, lengths: Sequence[int], b: int, num_heads: int,
-                    items: Optional[Sequence[Tuple[int, int, int]]] = None) -> float:
-    """Computed blocks over causal candidate blocks (sum of J_i = i + 1) for the given items."""
-    if items is None:
-        items = list(results.keys())
-    num = sum(int((results[it].flags == COMPUTED).sum()) for it in items)
-    den = sum(it[2] + 1 for it in items)
-    return num / den if den else 0.0

@@ -25,3 +25,15 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """The parity record of the GPU tests: per workload, skip-decision agreement with every
+    disagreement and its oracle margin, output errors, mask rows compared and float64 ties."""
+    gh = sys.modules.get("tests.gpu_helpers")
+    lines = gh.parity_summary_lines() if gh is not None else []
+    if not lines:
+        return
+    terminalreporter.write_sep("=", "parity record: GPU path against the float64 oracle")
+    for line in lines:
+        terminalreporter.write_line(line)

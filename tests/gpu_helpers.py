@@ -3,6 +3,7 @@ the C ABI, and comparisons against the float64 oracle."""
 from __future__ import annotations
 
 import math
+import os
 from dataclasses import dataclass
 from typing import Dict, List, Optional, Tuple
 
@@ -21,6 +22,19 @@ SKIP_AGREE = 0.999
 SKIP_MARGIN_TOL = 1e-3
 # two oracle scores closer than this (relative) are a float64 tie: either order is valid
 SCORE_TIE_RTOL = 1e-12
+
+# The parity record: every comparison against the oracle appends an entry here, and the terminal
+# summary of tests/conftest.py prints them grouped by workload (skip agreement with each
+# disagreement's oracle margin, output errors, mask rows and accepted float64 ties).
+PARITY_LOG: List[dict] = []
+
+
+def _current_test() -> str:
+    return os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0]
+
+
+def record(kind: str, workload: str, **fields) -> None:
+    PARITY_LOG.append(dict(kind=kind, workload=workload, test=_current_test(), **fields))
 
 
 def bf16_tensor(bits: np.ndarray, dev) -> torch.Tensor:
@@ -165,8 +179,11 @@ def compare_osk(w: synth.Workload, prm: orc.Params, mask, mask_len, out_gpu, fla
         got = out_gpu[t0:t0 + r.out.shape[0], h, :]
         errs.append(np.abs(got - r.out).ravel())
     e = np.concatenate(errs) if errs else np.zeros(1)
-    return OskReport(len(ref), n_tested, len(dis), max([abs(x[2]) for x in dis], default=0.0),
-                     float(e.max()), float(e.mean()), dis)
+    rep = OskReport(len(ref), n_tested, len(dis), max([abs(x[2]) for x in dis], default=0.0),
+                    float(e.max()), float(e.mean()), dis)
+    record("osk", sp.name, items=rep.n_items, tested=rep.n_tested, disagree=rep.n_disagree,
+           disagreements=list(dis), max_abs=rep.max_abs, mean_abs=rep.mean_abs, binary=binary)
+    return rep
 
 
 def assert_osk_ok(rep: OskReport):
@@ -183,7 +200,7 @@ def assert_osk_ok(rep: OskReport):
 TOP_P_RTOL = 1e-3
 
 
-def compare_masks_top_p(mask_gpu, len_gpu, rows: Dict, p_ppm: int) -> Tuple[List, List]:
+def compare_masks_top_p(mask_gpu, len_gpu, rows: Dict, p_ppm: int, workload: str = "") -> Tuple[List, List]:
     """Top-p masks: the GPU row must be a prefix of the oracle's rho_i (float64 ties accepted as in
     compare_masks) whose length is the oracle's K_i, or differs from it only across cuts the fp32
     scores cannot tell apart (oracle prefix mass within TOP_P_RTOL * total of p * total).
@@ -201,19 +218,31 @@ def compare_masks_top_p(mask_gpu, len_gpu, rows: Dict, p_ppm: int) -> Tuple[List
                 assert abs(csum[k - 1] - p * T) <= TOP_P_RTOL * T, (key, kg, ko, k, csum[k - 1] / T)
             cuts.append((key, kg, ko))
         sub = type(row)(scores=row.scores, hrm=row.hrm, order=row.order, K=kg, pbar=row.pbar)
-        ties += compare_masks_rows(mask_gpu, len_gpu, {key: sub})
+        ties += _compare_mask_rows(mask_gpu, len_gpu, {key: sub})
+    record("top_p", workload, rows=len(rows), p_ppm=p_ppm, cuts=list(cuts), ties=len(ties))
     return cuts, ties
 
 
-def compare_masks_rows(mask_gpu, len_gpu, rows: Dict) -> List:
+def compare_masks_rows(mask_gpu, len_gpu, rows: Dict, workload: str = "") -> List:
     """compare_masks restricted to the oracle's rows (no check of absent query blocks)."""
-    return compare_masks(mask_gpu, len_gpu, rows, None, None)
+    return compare_masks(mask_gpu, len_gpu, rows, None, None, workload=workload)
 
 
-def compare_masks(mask_gpu, len_gpu, rows: Dict, lengths, block_size) -> List:
+def compare_masks(mask_gpu, len_gpu, rows: Dict, lengths, block_size, workload: str = "") -> List:
     """Bit-exact comparison of M_KAP rows; a difference is accepted only between blocks whose
     oracle keys (HRM flag, score) are equal within a float64 tie.  Returns accepted ties;
     raises on a real mismatch."""
+    ties = _compare_mask_rows(mask_gpu, len_gpu, rows)
+    # absent query blocks
+    for b, L in enumerate(lengths or []):
+        nqb = -(-L // block_size)
+        assert (len_gpu[b, :, nqb:] == 0).all()
+        assert (mask_gpu[b, :, nqb:, :] == -1).all()
+    record("mask", workload, rows=len(rows), entries=int(sum(r.K for r in rows.values())), ties=list(ties))
+    return ties
+
+
+def _compare_mask_rows(mask_gpu, len_gpu, rows: Dict) -> List:
     ties = []
     for (b, h, i), row in rows.items():
         K = row.K
@@ -237,9 +266,55 @@ def compare_masks(mask_gpu, len_gpu, rows: Dict, lengths, block_size) -> List:
             ties.append(((b, h, i), p, a, c, float(sc[a]), float(sc[c])))
         assert len(set(g.tolist())) == K
         assert (mask_gpu[b, h, i, K:] == -1).all()
-    # absent query blocks
-    for b, L in enumerate(lengths or []):
-        nqb = -(-L // block_size)
-        assert (len_gpu[b, :, nqb:] == 0).all()
-        assert (mask_gpu[b, :, nqb:, :] == -1).all()
     return ties
+
+
+# --------------------------------------------------------------------------- #
+# the parity record, as printed after the test run
+# --------------------------------------------------------------------------- #
+def parity_summary_lines() -> List[str]:
+    """One line per (kind, workload), then one line per skip disagreement with its oracle margin.
+    Workloads are printed in the order they were first compared."""
+    order, groups = [], {}
+    for e in PARITY_LOG:
+        key = (e["kind"], e["workload"])
+        if key not in groups:
+            order.append(key)
+            groups[key] = []
+        groups[key].append(e)
+    lines = []
+    for kind, wl in order:
+        es = groups[(kind, wl)]
+        name = wl or "?"
+        if kind == "osk":
+            items = sum(e["items"] for e in es)
+            tested = sum(e["tested"] for e in es)
+            dis = [d for e in es for d in e["disagreements"]]
+            agree = 100.0 * (1.0 - len(dis) / tested) if tested else 100.0
+            lines.append(f"skip parity {name}: {len(es)} run(s), {items} items, {tested} tested visits, "
+                         f"{len(dis)} disagree ({agree:.4f}% agree); O max-abs {max(e['max_abs'] for e in es):.2e}, "
+                         f"mean-abs {max(e['mean_abs'] for e in es):.2e}")
+            for (it, k, margin) in dis:
+                lines.append(f"    disagreement {name} item {it} entry {k}: oracle margin {margin:+.3e} nats")
+        elif kind == "mask":
+            rows = sum(e["rows"] for e in es)
+            ents = sum(e["entries"] for e in es)
+            ties = [t for e in es for t in e["ties"]]
+            lines.append(f"mask parity {name}: {rows} rows, {ents} entries bit-exact except {len(ties)} "
+                         f"float64 tie(s)")
+        elif kind == "top_p":
+            rows = sum(e["rows"] for e in es)
+            cuts = [c for e in es for c in e["cuts"]]
+            lines.append(f"top-p parity {name}: {rows} rows, {len(cuts)} cut(s) differ from the oracle's"
+                         + (f": {cuts[:4]}" if cuts else ""))
+        elif kind == "kappa":
+            wn = max(es, key=lambda e: e["r_norm"])
+            wa = max(es, key=lambda e: e["r_abs"])
+            lines.append(f"kappa bound {name}: {len(es)} cases, {sum(e['logits'] for e in es)} logits; worst "
+                         f"|err|/(|q||k|) {wn['r_norm'] / 2.0 ** -24:.2f}*2^-24 ({wn['case']}; limit 32*2^-24), "
+                         f"worst |err|/sum|q_i k_i| {wa['r_abs'] / 2.0 ** -24:.2f}*2^-24 ({wa['case']}; model 48*2^-24)")
+        else:
+            for e in es:
+                extra = {k: v for k, v in e.items() if k not in ("kind", "workload", "test")}
+                lines.append(f"{kind} {name}: " + ", ".join(f"{k} {v}" for k, v in extra.items()))
+    return lines

@@ -52,7 +52,7 @@ def test_kap_ascending_small(name, ppm):
     prm = gh.oracle_params(sp, -1.0, budget_ppm=ppm)
     mo, lo, rows = orc.kap_mask(w.q, w.k_cache, w.page_table, w.cu_seqlens, sp.num_q_heads, sp.num_kv_heads,
                                 prm, pitch, ascending=True)
-    ties = gh.compare_masks(m0, l0, rows, sp.lengths, sp.block_size)
+    ties = gh.compare_masks(m0, l0, rows, sp.lengths, sp.block_size, workload=sp.name)
     if not ties:
         assert np.array_equal(m1, mo) and np.array_equal(l1, lo)
 

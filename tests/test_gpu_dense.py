@@ -1,6 +1,8 @@
-"""Dense endpoint of the OSK (every causal block, ascending order, skipping off) against PyTorch's
-fp32 causal attention on the same GPU: with B1 = 100 % and Delta <= 0, CoSA's Algorithm A reduces to
-exact causal softmax attention (CoSA Sec. 4.3; the oracle pins the same reduction in float64)."""
+"""Dense endpoint of the OSK (every causal block, ascending order, skipping off: B1 = 100 %, Delta = -1,
+the stage-1-only endpoint of CoSA App. D.1) against the float64 oracle's Algorithm A on the same masks,
+every item compared, and against PyTorch's fp32 causal attention on the same GPU: with B1 = 100 % and
+Delta <= 0, CoSA's Algorithm A reduces to exact causal softmax attention (CoSA Sec. 4.3; the oracle
+pins the same reduction in float64)."""
 import math
 
 import numpy as np
@@ -40,7 +42,7 @@ def paged_to_dense(w, dev):
 
 @pytest.mark.parametrize("block_size,page_size,head_dim", [(128, 64, 128), (64, 32, 64)])
 def test_dense_endpoint_matches_torch_causal_attention(block_size, page_size, head_dim):
-    sp = synth.WorkloadSpec(name="dense", lengths=(2048, 1500, 77), num_q_heads=4, num_kv_heads=2,
+    sp = synth.WorkloadSpec(name=f"dense_b{block_size}_P{page_size}_d{head_dim}", lengths=(2048, 1500, 77), num_q_heads=4, num_kv_heads=2,
                             head_dim=head_dim, block_size=block_size, page_size=page_size,
                             stride=block_size // 8, budget_ppm=1_000_000, stage2_budget_ppm=0, seed=31,
                             shuffle_pages=True, salient_pages=3)
@@ -54,6 +56,12 @@ def test_dense_endpoint_matches_torch_causal_attention(block_size, page_size, he
     for b, L in enumerate(sp.lengths):
         n = -(-L // sp.block_size)
         assert (flags[b, :, :n, :][np.arange(nqb)[None, None, :] < ml[b, :, :n, None]] == 0).all()
+
+    # the oracle's Algorithm A over the same dense masks, every (request, head, query block)
+    prm = gh.oracle_params(sp, -1.0, budget_ppm=1_000_000)
+    rep = gh.compare_osk(w, prm, mask, ml, out, flags, gh.items_of(sp))
+    gh.assert_osk_ok(rep)
+    assert rep.n_disagree == 0 and rep.n_items == sum(sp.num_q_heads * -(-L // sp.block_size) for L in sp.lengths)
 
     q = torch.from_numpy(synth.bf16_bits_to_f32(w.q)).to(dev)
     g = sp.num_q_heads // sp.num_kv_heads

@@ -47,7 +47,7 @@ def run_full(name, n_items, seed):
         by.setdefault((b, h), []).append(i)
     mask_o, len_o, rows = orc.kap_mask(w.q, w.k_cache, w.page_table, w.cu_seqlens, sp.num_q_heads,
                                        sp.num_kv_heads, prm, p.mask_pitch, qblocks=by)
-    ties = gh.compare_masks_rows(mask_g, len_g, rows)
+    ties = gh.compare_masks_rows(mask_g, len_g, rows, workload=sp.name)
     if sp.mask_noise_frac:
         mask_g, len_g = synth.inject_mask_noise(mask_g, len_g, sp.lengths, sp.block_size, sp.mask_noise_frac,
                                                 seed=sp.seed)
@@ -78,3 +78,14 @@ def test_full_ragged_batch():
     """Ragged batch {16K, 48K, 96K, 128K}, duplicate and invalid IDs in 5 % of the mask rows."""
     rep, flags = run_full("ragged4_gqa_noisy_masks", 64, seed=5)
     assert (flags == orc.IGNORED).sum() > 0
+
+
+def test_full_32k_iid_queries():
+    """The literal reading of the GQA workloads' "N(0,1) Q": iid queries, salient pages shifted toward
+    the unit mean query, 32K tokens, shuffled pages, stage-1 budget 15 %.  Calibrated on the oracle, the
+    skip rule meets no stage-2 budget on this input (every Delta of the grid below N computes every
+    selected block: the rows of a query block have independent maxima, so some row always wants a
+    block), so the parity here is of the masks (flat, near-tied scores) and the outputs, with the
+    largest Delta of the grid."""
+    rep, flags = run_full("32k_gqa_shuffled_iidq", 48, seed=6)
+    assert rep.n_tested > 0

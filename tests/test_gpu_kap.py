@@ -25,7 +25,7 @@ def _kap_check(w, budget_ppm=None, heads=None, missing_pages=False):
     mask_g, len_g = gh.run_kap(dw, gh.cosa_params(dw, delta=-1.0, mask_pitch=pitch, budget_ppm=ppm))
     _, _, rows = orc.kap_mask(w.q, w.k_cache, w.page_table, w.cu_seqlens, sp.num_q_heads, sp.num_kv_heads,
                               prm, pitch, heads=heads)
-    ties = gh.compare_masks(mask_g, len_g, rows, sp.lengths, sp.block_size)
+    ties = gh.compare_masks(mask_g, len_g, rows, sp.lengths, sp.block_size, workload=sp.name)
     return ties
 
 
@@ -80,7 +80,7 @@ def test_kap_long_rows_both_select_paths():
     by = {(0, h): rows for h in range(sp.num_q_heads)}
     _, _, orows = orc.kap_mask(w.q, w.k_cache, w.page_table, w.cu_seqlens, sp.num_q_heads, sp.num_kv_heads,
                                prm, pitch, qblocks=by)
-    gh.compare_masks_rows(mask_g, len_g, orows)
+    gh.compare_masks_rows(mask_g, len_g, orows, workload=sp.name)
     nqb = -(-70000 // 64)
     want = np.maximum(1, -(-200_000 * np.arange(1, nqb + 1) // 1_000_000))
     assert (len_g[0, :, :nqb] == want[None, :]).all()

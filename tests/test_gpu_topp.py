@@ -35,7 +35,7 @@ def _run(w, ppm, delta=-1.0, items=None):
             by.setdefault((b, h), []).append(i)
     _, len_o, rows = orc.kap_mask(w.q, w.k_cache, w.page_table, w.cu_seqlens, sp.num_q_heads, sp.num_kv_heads,
                                   prm, nqb, qblocks=by)
-    cuts, ties = gh.compare_masks_top_p(mask_g, len_g, rows, ppm)
+    cuts, ties = gh.compare_masks_top_p(mask_g, len_g, rows, ppm, workload=sp.name)
     return dw, p, prm, mask_g, len_g, rows, cuts
 
 
