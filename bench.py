@@ -483,7 +483,10 @@ def run_cosa(args, spec, workload_name, delta):
         "dense_equiv_tflops": dense_equiv_flops(spec) / (osk_avg * 1e-3) / 1e12,
         "visits": visited, "computed": computed, "realized_stage1": visited / causal,
         "realized_stage2": computed / causal,
-        "roofline": {"bound": "tensor", "kernel": "osk_kernel<128,128,false>", "achieved": achieved, "peak": peak,
+        "roofline": {"bound": "tensor",
+                     "kernel": f"osk_kernel<{spec.block_size},{spec.head_dim},{spec.page_size},false,"
+                               f"{'true' if delta > 0 else 'false'},false>",
+                     "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"bf16_tflops ({pk_src}, burst)"},
         "e2e": {"value": job_tflops(world, step_flops, e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,

@@ -122,6 +122,11 @@ WORKLOADS: Dict[str, WorkloadSpec] = {s.name: s for s in (
                  seed=20261206, key_dist="student_t3", **_GQA),
     WorkloadSpec(name="ragged4_gqa_noisy_masks", lengths=(16384, 49152, 98304, 131072), budget_ppm=100_000,
                  stage2_budget_ppm=40_000, seed=20261207, shuffle_pages=True, mask_noise_frac=0.05, **_GQA),
+    # the literal reading of "N(0,1) Q/K/V" for the GQA shapes: iid queries, the 16 salient pages per kv
+    # head shifted by 4*sqrt(d) toward the unit mean query (no sink or window: with iid queries no key
+    # direction raises every query's logit, and nothing ties a query to its neighbours)
+    WorkloadSpec(name="32k_gqa_shuffled_iidq", lengths=(32768,), budget_ppm=150_000, stage2_budget_ppm=50_000,
+                 seed=20261208, shuffle_pages=True, iid_queries=True, **_GQA),
 )}
 
 
