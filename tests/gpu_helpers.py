@@ -273,48 +273,48 @@ def _compare_mask_rows(mask_gpu, len_gpu, rows: Dict) -> List:
 # the parity record, as printed after the test run
 # --------------------------------------------------------------------------- #
 def parity_summary_lines() -> List[str]:
-    """One line per (kind, workload), then one line per skip disagreement with its oracle margin.
-    Workloads are printed in the order they were first compared."""
-    order, groups = [], {}
+    """One line per workload (masks, top-p cuts, skip decisions, outputs), the named workloads of
+    synth.WORKLOADS last in registry order, each skip disagreement on its own line with its oracle
+    margin, and the tensor-core error bound at the end."""
+    by = {}
     for e in PARITY_LOG:
-        key = (e["kind"], e["workload"])
-        if key not in groups:
-            order.append(key)
-            groups[key] = []
-        groups[key].append(e)
+        by.setdefault(e["workload"] or "?", []).append(e)
+    named = [n for n in synth.WORKLOADS if n in by]
+    others = [n for n in by if n not in synth.WORKLOADS and n != "tensor-core logits"]
     lines = []
-    for kind, wl in order:
-        es = groups[(kind, wl)]
-        name = wl or "?"
-        if kind == "osk":
-            items = sum(e["items"] for e in es)
-            tested = sum(e["tested"] for e in es)
-            dis = [d for e in es for d in e["disagreements"]]
-            agree = 100.0 * (1.0 - len(dis) / tested) if tested else 100.0
-            lines.append(f"skip parity {name}: {len(es)} run(s), {items} items, {tested} tested visits, "
-                         f"{len(dis)} disagree ({agree:.4f}% agree); O max-abs {max(e['max_abs'] for e in es):.2e}, "
-                         f"mean-abs {max(e['mean_abs'] for e in es):.2e}")
-            for (it, k, margin) in dis:
-                lines.append(f"    disagreement {name} item {it} entry {k}: oracle margin {margin:+.3e} nats")
-        elif kind == "mask":
-            rows = sum(e["rows"] for e in es)
-            ents = sum(e["entries"] for e in es)
-            ties = [t for e in es for t in e["ties"]]
-            lines.append(f"mask parity {name}: {rows} rows, {ents} entries bit-exact except {len(ties)} "
-                         f"float64 tie(s)")
-        elif kind == "top_p":
-            rows = sum(e["rows"] for e in es)
-            cuts = [c for e in es for c in e["cuts"]]
-            lines.append(f"top-p parity {name}: {rows} rows, {len(cuts)} cut(s) differ from the oracle's"
-                         + (f": {cuts[:4]}" if cuts else ""))
-        elif kind == "kappa":
-            wn = max(es, key=lambda e: e["r_norm"])
-            wa = max(es, key=lambda e: e["r_abs"])
-            lines.append(f"kappa bound {name}: {len(es)} cases, {sum(e['logits'] for e in es)} logits; worst "
-                         f"|err|/(|q||k|) {wn['r_norm'] / 2.0 ** -24:.2f}*2^-24 ({wn['case']}; limit 32*2^-24), "
-                         f"worst |err|/sum|q_i k_i| {wa['r_abs'] / 2.0 ** -24:.2f}*2^-24 ({wa['case']}; model 48*2^-24)")
-        else:
-            for e in es:
-                extra = {k: v for k, v in e.items() if k not in ("kind", "workload", "test")}
-                lines.append(f"{kind} {name}: " + ", ".join(f"{k} {v}" for k, v in extra.items()))
+    small = [e for n in others for e in by[n]]
+    if small:
+        lines += _summary_of(f"small and edge cases ({len(others)} shapes)", small)
+    for n in named:
+        lines += _summary_of(n, by[n])
+    kap = by.get("tensor-core logits", [])
+    if kap:
+        wn = max(kap, key=lambda e: e["r_norm"])
+        wa = max(kap, key=lambda e: e["r_abs"])
+        lines.append(f"kappa bound: {len(kap)} cases, {sum(e['logits'] for e in kap)} tensor-core logits; worst "
+                     f"|err|/(|q||k|) {wn['r_norm'] / 2.0 ** -24:.2f}*2^-24 ({wn['case']}; limit 32*2^-24), worst "
+                     f"|err|/sum|q_i k_i| {wa['r_abs'] / 2.0 ** -24:.2f}*2^-24 ({wa['case']}; model 48*2^-24)")
     return lines
+
+
+def _summary_of(name: str, es: List[dict]) -> List[str]:
+    parts, extra = [], []
+    ms = [e for e in es if e["kind"] == "mask"]
+    if ms:
+        ties = sum(len(e["ties"]) for e in ms)
+        parts.append(f"masks {sum(e['rows'] for e in ms)} rows / {sum(e['entries'] for e in ms)} entries exact "
+                     f"({ties} float64 ties)")
+    tp = [e for e in es if e["kind"] == "top_p"]
+    if tp:
+        cuts = [c for e in tp for c in e["cuts"]]
+        parts.append(f"top-p {sum(e['rows'] for e in tp)} rows, {len(cuts)} cuts differ")
+    os_ = [e for e in es if e["kind"] == "osk"]
+    if os_:
+        tested = sum(e["tested"] for e in os_)
+        dis = [d for e in os_ for d in e["disagreements"]]
+        agree = 100.0 * (1.0 - len(dis) / tested) if tested else 100.0
+        parts.append(f"skip {tested} visits of {sum(e['items'] for e in os_)} items, {len(dis)} disagree "
+                     f"({agree:.3f}% agree); O max-abs {max(e['max_abs'] for e in os_):.1e} mean-abs "
+                     f"{max(e['mean_abs'] for e in os_):.1e}")
+        extra = [f"    disagreement {name} item {it} entry {k}: oracle margin {m:+.3e} nats" for (it, k, m) in dis]
+    return [f"{name}: " + "; ".join(parts)] + extra
