@@ -23,8 +23,9 @@
 //                            the row (from ||q_r|| * max ||k|| and the accumulation model of kKappa);
 //                            if the runner-up is more than 2 e_r below the maximum the argmax key is
 //                            certain and M_r is its exact logit (three-term fp32 sum);
-//   kap_rescan               rows where it is not: every key within 3 e_r of the largest is
-//                            re-evaluated in float64; the HRM blocks of the row follow exactly;
+//   kap_rescan               rows where it is not: every key of the blocks whose stored fp32 block
+//                            maximum is within 3 e_r of the largest logit is re-evaluated in float64;
+//                            the HRM blocks of the row follow exactly;
 //   kap_block_scores         per (query block, key block): fp32 score from the stored block maxima
 //                            and the exact M_r, with a rigorous bound on its error;
 //   kap_select_warp          a warp per mask row: top-K by radix select, sort, certification of
@@ -34,6 +35,7 @@
 //                            order, long rows, cuts the sentinel cannot certify).
 #include <cstdint>
 #include <mutex>
+#include <type_traits>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -201,10 +203,14 @@ __global__ void kap_setup_kernel(KapArgs a) {
 
 // Gather the stride-sampled queries and keys of every (request, head) into contiguous, 128-row
 // padded arrays (absent keys and padding rows are zero), record which keys exist, and the largest
-// key norm per (request, kv head) and per key block.  One warp per 32 rows; grid.y walks the
-// requests' q heads then kv heads.
+// key norm per (request, kv head) and per key block.  One warp per 32 rows, eight rows in flight;
+// each lane moves HD / 32 consecutive elements of a row with one vector load and store.  grid.y
+// walks the requests' q heads then kv heads.
 template <int HD>
 __global__ void __launch_bounds__(256) kap_gather_kernel(KapArgs a) {
+  constexpr int PER = HD / 32;  // bf16 per lane per row
+  static_assert(PER == 4 || PER == 2, "d = 128 or 64");
+  using Vec = typename std::conditional<PER == 4, uint2, uint32_t>::type;
   const int nh = a.num_q_heads + a.num_kv_heads;
   const int b = blockIdx.y / nh, hh = blockIdx.y % nh;
   const bool is_key = hh >= a.num_q_heads;
@@ -216,38 +222,55 @@ __global__ void __launch_bounds__(256) kap_gather_kernel(KapArgs a) {
   const int head = is_key ? hh - a.num_q_heads : hh;
   const int64_t base = is_key ? a.ks_off[b] + static_cast<int64_t>(head) * rp : a.qs_off[b] + static_cast<int64_t>(head) * rp;
   uint16_t* dst_base = (is_key ? a.ks : a.qs) + base * HD;
-  constexpr int PER = HD / 32;  // bf16 per lane per row
+  constexpr int U = 8;          // rows in flight
   uint32_t valid_bits = 0;
   float blk_norm = 0.0f;        // running max over the rows of the current key block
-  for (int rr = 0; rr < 32; ++rr) {
-    const int r = r0 + rr;
-    const uint16_t* src = nullptr;
-    if (r < ri.R) src = is_key ? key_ptr(a, ri, b, head, r) : query_ptr(a, ri, head, r);
-    uint16_t v[PER];
-    float s2 = 0.0f;
+  for (int rr0 = 0; rr0 < 32; rr0 += U) {
+    Vec val[U];
+    bool have[U];
 #pragma unroll
-    for (int e = 0; e < PER; ++e) {
-      v[e] = src ? src[lane * PER + e] : static_cast<uint16_t>(0);
-      const float x = bf16_to_f32(v[e]);
-      s2 = fmaf(x, x, s2);
+    for (int u = 0; u < U; ++u) {
+      const int r = r0 + rr0 + u;
+      const uint16_t* src = nullptr;
+      if (r < ri.R) src = is_key ? key_ptr(a, ri, b, head, r) : query_ptr(a, ri, head, r);
+      have[u] = src != nullptr;
+      if (src) val[u] = *reinterpret_cast<const Vec*>(src + lane * PER);
+      else val[u] = Vec{};
     }
-    uint16_t* dst = dst_base + static_cast<int64_t>(r) * HD + lane * PER;
 #pragma unroll
-    for (int e = 0; e < PER; ++e) dst[e] = v[e];
-    if (is_key) {
+    for (int u = 0; u < U; ++u) {
+      const int rr = rr0 + u;
+      const int r = r0 + rr;
+      *reinterpret_cast<Vec*>(dst_base + static_cast<int64_t>(r) * HD + lane * PER) = val[u];
+      if (is_key) {
+        uint32_t w[2];
+        if constexpr (PER == 4) {
+          w[0] = val[u].x;
+          w[1] = val[u].y;
+        } else {
+          w[0] = val[u];
+          w[1] = 0u;
+        }
+        float s2 = 0.0f;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
-      const float n = src ? sqrtf(s2) * (1.0f + 1.0f / 65536.0f) : 0.0f;
-      if (src) valid_bits |= 1u << rr;
-      blk_norm = fmaxf(blk_norm, n);
-      const int j = (r * a.stride) / a.block_size;
-      const bool last_of_block = (rr == 31) || (((r + 1) * a.stride) / a.block_size != j);
-      if (last_of_block && lane == 0 && blk_norm > 0.0f) {
-        atomicMax(reinterpret_cast<int*>(&a.kbnorm[(static_cast<size_t>(b) * a.num_kv_heads + head) * a.nqb_max + j]),
-                  __float_as_int(blk_norm));
-        atomicMax(reinterpret_cast<int*>(&a.knorm[b * a.num_kv_heads + head]), __float_as_int(blk_norm));
+        for (int e = 0; e < PER; ++e) {
+          const float x = __uint_as_float((e & 1) ? (w[e >> 1] & 0xffff0000u) : (w[e >> 1] << 16));
+          s2 = fmaf(x, x, s2);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+        const float nrm = have[u] ? sqrtf(s2) * (1.0f + 1.0f / 65536.0f) : 0.0f;
+        if (have[u]) valid_bits |= 1u << rr;
+        blk_norm = fmaxf(blk_norm, nrm);
+        const int j = (r * a.stride) / a.block_size;
+        const bool last_of_block = (rr == 31) || (((r + 1) * a.stride) / a.block_size != j);
+        if (last_of_block && lane == 0 && blk_norm > 0.0f) {
+          atomicMax(reinterpret_cast<int*>(&a.kbnorm[(static_cast<size_t>(b) * a.num_kv_heads + head) * a.nqb_max + j]),
+                    __float_as_int(blk_norm));
+          atomicMax(reinterpret_cast<int*>(&a.knorm[b * a.num_kv_heads + head]), __float_as_int(blk_norm));
+        }
+        if (last_of_block) blk_norm = 0.0f;
       }
-      if (last_of_block) blk_norm = 0.0f;
     }
   }
   if (is_key && lane == 0) a.kvalid[(base + r0) >> 5] = valid_bits;
@@ -664,21 +687,39 @@ __global__ void __launch_bounds__(256) kap_exact_kernel(KapArgs a) {
   }
 }
 
-// Rows whose maximum fp32 cannot certify: one CTA per row (grid-stride over the queue).  Every
-// thread takes keys c = tid, tid + 256, ... of the row from the gathered arrays, screens them with an
-// fp32 dot (within 3 e_r of v1), re-evaluates the survivors in float64, and the CTA flags the blocks
-// of the keys that attain the exact maximum.
-template <int HD>
-__global__ void __launch_bounds__(512) kap_rescan_kernel(KapArgs a) {
-  constexpr int kCand = 256;
-  __shared__ float qf[HD];
-  __shared__ double cval[kCand];
-  __shared__ int ckey[kCand];
-  __shared__ int ncand;
-  __shared__ double red[32];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+// q . k over d = 32 * PER elements, the warp's lanes holding PER each, summed as three fp32 terms
+// (bf16 products are exact in fp32) and returned in float64 to every lane (lane 0's sum).
+template <int PER>
+__device__ __forceinline__ double warp_dot3(const float (&qf)[PER], const float (&kf)[PER]) {
+  float hi = 0.0f, lo = 0.0f, cc = 0.0f;
+#pragma unroll
+  for (int e = 0; e < PER; ++e) sum3_add(hi, lo, cc, __fmul_rn(qf[e], kf[e]));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float oh = __shfl_xor_sync(0xffffffffu, hi, o), ol = __shfl_xor_sync(0xffffffffu, lo, o);
+    const float oc = __shfl_xor_sync(0xffffffffu, cc, o);
+    sum3_add(hi, lo, cc, oh, ol, oc);
+  }
+  const double v = (static_cast<double>(hi) + static_cast<double>(lo)) + static_cast<double>(cc);
+  return __shfl_sync(0xffffffffu, v, 0);
+}
+
+// Rows whose maximum fp32 cannot certify: a warp per row (warp-stride over the queue).  A key can
+// hold the exact maximum only if its fp32 logit is at least v1 - 2 e_r (its exact logit is within
+// e_r of its fp32 one, and the exact maximum is at least the fp32 argmax's exact logit, v1 - e_r),
+// so only the key blocks whose stored fp32 block maximum (the logits pass) reaches v1 - 3 e_r are
+// examined: every visible key of those blocks is evaluated in float64 (lanes split d, butterfly sum:
+// every lane holds the same value), the row maximum is the largest, and the row's HRM bitmap flags
+// the blocks of the keys that attain it.
+template <int HD, int KB>
+__global__ void __launch_bounds__(256) kap_rescan_kernel(KapArgs a) {
+  constexpr int PER = HD / 32;   // d elements per lane
+  const int lane = threadIdx.x & 31;
+  const long long wid = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
+  const long long nw = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
   const long long n = a.amb[0];
-  for (long long qi = blockIdx.x; qi < n; qi += gridDim.x) {
+  const float sc = static_cast<float>(a.sm_scale);
+  for (long long qi = wid; qi < n; qi += nw) {
     const int64_t gw = a.amb[1 + qi];
     int b = 0;
     while (b + 1 < a.num_reqs && a.row_off[b + 1] <= gw) ++b;
@@ -688,83 +729,94 @@ __global__ void __launch_bounds__(512) kap_rescan_kernel(KapArgs a) {
     const int r = static_cast<int>(local % ri.R);
     const int kvh = h / (a.num_q_heads / a.num_kv_heads);
     const int rp = (ri.R + kRowTile - 1) / kRowTile * kRowTile;
-    const uint16_t* qrow = a.qs + (a.qs_off[b] + static_cast<int64_t>(h) * rp + r) * HD;
-    const int64_t krow0 = a.ks_off[b] + static_cast<int64_t>(kvh) * rp;
-    for (int e = tid; e < HD; e += blockDim.x) qf[e] = bf16_to_f32(qrow[e]);
-    if (tid == 0) ncand = 0;
-    __syncthreads();
+    const int qblk = r / KB;
+    const float* bm_row = a.bm + a.bm_off[b] + static_cast<int64_t>(h) * bm_block_base(ri.nqb, KB) +
+                          bm_block_base(qblk, KB) + static_cast<int64_t>(r - qblk * KB) * bm_pitch(qblk, KB);
     const float thr = a.v1[gw] - 3.0f * a.err[gw];
-    const float sc = static_cast<float>(a.sm_scale);
-    double best = -INFINITY;
-    bool overflow = false;
-    for (int c = tid; c <= r; c += blockDim.x) {
-      if (!((a.kvalid[(krow0 + c) >> 5] >> ((krow0 + c) & 31)) & 1u)) continue;
-      const uint16_t* kr = a.ks + (krow0 + c) * HD;
-      // four interleaved partial sums: rounding depth HD/4 + 2 stays within the fp32 bound e_r
-      float p4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll 4
-      for (int e = 0; e < HD; e += 8) {
-        float kf[8];
-        load8_bf16(kr + e, kf);
+    float qf[PER];
+    {
+      const uint16_t* qrow = a.qs + (a.qs_off[b] + static_cast<int64_t>(h) * rp + r) * HD + lane * PER;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) p4[i & 3] = fmaf(qf[e + i], kf[i], p4[i & 3]);
-      }
-      const float acc = (p4[0] + p4[1]) + (p4[2] + p4[3]);
-      if (acc * sc < thr) continue;
-      double dacc = 0.0;
-      for (int e = 0; e < HD; e += 8) {
-        float kf[8];
-        load8_bf16(kr + e, kf);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) dacc += static_cast<double>(qf[e + i] * kf[i]);
-      }
-      const double lx = dacc * a.sm_scale;
-      best = fmax(best, lx);
-      const int slot = atomicAdd(&ncand, 1);
-      if (slot < kCand) { cval[slot] = lx; ckey[slot] = c; } else { overflow = true; }
+      for (int e = 0; e < PER; ++e) qf[e] = bf16_to_f32(qrow[e]);
     }
-    // CTA maximum of the float64 logits
-    for (int o = 16; o > 0; o >>= 1) best = fmax(best, __shfl_xor_sync(0xffffffffu, best, o));
-    if (lane == 0) red[warp] = best;
+    const int64_t krow0 = a.ks_off[b] + static_cast<int64_t>(kvh) * rp;
     uint32_t* bits = a.hrm_bits + gw * a.words_per_row;
-    for (int w = tid; w < a.words_per_row; w += blockDim.x) bits[w] = 0u;
-    const int any_overflow = __syncthreads_or(overflow);
-    double M = red[0];
-    for (int w = 1; w < static_cast<int>(blockDim.x / 32); ++w) M = fmax(M, red[w]);
-    const int nc = min(ncand, kCand);
-    if (!any_overflow) {
-      for (int x = tid; x < nc; x += blockDim.x)
-        if (cval[x] == M) {
-          const int j = (ckey[x] * a.stride) / a.block_size;
-          atomicOr(&bits[j >> 5], 1u << (j & 31));
-        }
-    } else {
-      // more survivors than the candidate list holds: evaluate them again
-      for (int c = tid; c <= r; c += blockDim.x) {
-        if (!((a.kvalid[(krow0 + c) >> 5] >> ((krow0 + c) & 31)) & 1u)) continue;
-        const uint16_t* kr = a.ks + (krow0 + c) * HD;
-        float p4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        for (int e = 0; e < HD; e += 8) {
-          float kf[8];
-          load8_bf16(kr + e, kf);
-          for (int i = 0; i < 8; ++i) p4[i & 3] = fmaf(qf[e + i], kf[i], p4[i & 3]);
-        }
-        const float acc = (p4[0] + p4[1]) + (p4[2] + p4[3]);
-        if (acc * sc < thr) continue;
-        double dacc = 0.0;
-        for (int e = 0; e < HD; e += 8) {
-          float kf[8];
-          load8_bf16(kr + e, kf);
-          for (int i = 0; i < 8; ++i) dacc += static_cast<double>(qf[e + i] * kf[i]);
-        }
-        if (dacc * a.sm_scale == M) {
-          const int j = (c * a.stride) / a.block_size;
-          atomicOr(&bits[j >> 5], 1u << (j & 31));
+    for (int w = lane; w < a.words_per_row; w += 32) bits[w] = 0u;
+    __syncwarp();
+    // candidate blocks, 32 per ballot, all block maxima of a group of 1024 blocks loaded at once;
+    // one pass over their keys keeps each candidate block's largest exact logit (lane k holds the
+    // k-th candidate's), a second pass is taken only when there are more than 32 candidates
+    double M = -INFINITY;
+    double bmx_lane = -INFINITY;
+    int bj_lane = -1, ncand = 0;
+    for (int g0 = 0; g0 <= qblk; g0 += 1024) {
+      uint32_t cmk[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const int j = g0 + c * 32 + lane;
+        const float bmj = (j <= qblk) ? bm_row[j] : -INFINITY;
+        cmk[c] = __ballot_sync(0xffffffffu, bmj != -INFINITY && bmj * sc >= thr);
+      }
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        uint32_t cm = cmk[c];
+        while (cm) {
+          const int jj = g0 + c * 32 + __ffs(cm) - 1;
+          cm &= cm - 1;
+          float kf[KB][PER];
+          bool vis[KB];
+#pragma unroll
+          for (int q = 0; q < KB; ++q) {
+            const int kc = jj * KB + q;
+            vis[q] = kc <= r && ((a.kvalid[(krow0 + kc) >> 5] >> ((krow0 + kc) & 31)) & 1u);
+            const uint16_t* kr = a.ks + (krow0 + (vis[q] ? kc : 0)) * HD + lane * PER;
+#pragma unroll
+            for (int e = 0; e < PER; ++e) kf[q][e] = bf16_to_f32(kr[e]);
+          }
+          double bx = -INFINITY;
+#pragma unroll
+          for (int q = 0; q < KB; ++q) {
+            double part = 0.0;
+#pragma unroll
+            for (int e = 0; e < PER; ++e) part += static_cast<double>(qf[e] * kf[q][e]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+            if (vis[q]) bx = fmax(bx, part * a.sm_scale);
+          }
+          if (lane == (ncand & 31) && ncand < 32) { bmx_lane = bx; bj_lane = jj; }
+          ++ncand;
+          M = fmax(M, bx);
         }
       }
     }
-    if (tid == 0) a.M[gw] = M;
-    __syncthreads();
+    if (ncand <= 32) {
+      if (bj_lane >= 0 && bmx_lane == M) atomicOr(&bits[bj_lane >> 5], 1u << (bj_lane & 31));
+    } else {
+      for (int j0 = 0; j0 <= qblk; j0 += 32) {
+        const int j = j0 + lane;
+        const float bmj = (j <= qblk) ? bm_row[j] : -INFINITY;
+        unsigned cm = __ballot_sync(0xffffffffu, bmj != -INFINITY && bmj * sc >= thr);
+        while (cm) {
+          const int jj = j0 + __ffs(cm) - 1;
+          cm &= cm - 1;
+          bool hit = false;
+          for (int q = 0; q < KB; ++q) {
+            const int kc = jj * KB + q;
+            if (kc > r) break;
+            if (!((a.kvalid[(krow0 + kc) >> 5] >> ((krow0 + kc) & 31)) & 1u)) continue;
+            const uint16_t* kr = a.ks + (krow0 + kc) * HD + lane * PER;
+            double part = 0.0;
+#pragma unroll
+            for (int e = 0; e < PER; ++e) part += static_cast<double>(qf[e] * bf16_to_f32(kr[e]));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+            hit = hit || (part * a.sm_scale == M);
+          }
+          if (hit && lane == 0) atomicOr(&bits[jj >> 5], 1u << (jj & 31));
+        }
+      }
+    }
+    if (lane == 0) a.M[gw] = M;
   }
 }
 
@@ -1267,21 +1319,17 @@ __device__ void kap_select_row(const KapArgs& a, int cap, int row) {
             uint32_t cmask = __ballot_sync(0xffffffffu, cand && sub == 0);
             double dv = -INFINITY;
             const uint16_t* qrow = qbase + static_cast<int64_t>(r) * HD;
+            float qf[HD / 32];
+#pragma unroll
+            for (int e = 0; e < HD / 32; ++e) qf[e] = bf16_to_f32(qrow[lane * (HD / 32) + e]);
             while (cmask) {
               const int g = (__ffs(cmask) - 1) / LPK;   // key group of the candidate
               cmask &= cmask - 1;
               const uint16_t* krow = a.ks + (krow0 + j * KB + g) * HD;
-              double dp = 0.0;
+              float kf[HD / 32];
 #pragma unroll
-              for (int e = lane * (HD / 32); e < (lane + 1) * (HD / 32); e += 2) {
-                const uint32_t qw = *reinterpret_cast<const uint32_t*>(qrow + e);
-                const uint32_t kw = *reinterpret_cast<const uint32_t*>(krow + e);
-                dp += static_cast<double>(__uint_as_float(qw << 16) * __uint_as_float(kw << 16));
-                dp += static_cast<double>(__uint_as_float(qw & 0xffff0000u) * __uint_as_float(kw & 0xffff0000u));
-              }
-#pragma unroll
-              for (int o = 16; o > 0; o >>= 1) dp += __shfl_xor_sync(0xffffffffu, dp, o);
-              dv = fmax(dv, dp * a.sm_scale);
+              for (int e = 0; e < HD / 32; ++e) kf[e] = bf16_to_f32(krow[lane * (HD / 32) + e]);
+              dv = fmax(dv, warp_dot3<HD / 32>(qf, kf) * a.sm_scale);   // float64 accuracy, FP32 pipe
             }
             term = dv - Mr;   // exponent; exp is taken below, one item per thread
           } else {
@@ -1387,10 +1435,13 @@ constexpr int kWarpSelMaxK = 128;
 constexpr int kWarpRepMax = 16;
 constexpr int kWarpSelWarps = 4;
 
+constexpr int kWarpCand = 64;            // float64 candidates of a row's repairs (more: block kernel)
+
 struct WarpSelSmem {
   unsigned long long key[kWarpSelMaxK];   // selected keys, sorted descending
   double rep_val[kWarpRepMax];
-  double terms[kWarpRepMax * 16];         // (repaired position, sampled row) exponents, then terms
+  double terms[kWarpRepMax * 16];         // (repaired position, sampled row): block maxima, then terms
+  uint32_t cand[kWarpCand];               // float64 candidates: (item << 16) | key
   uint32_t hist[256];
   int32_t rep_pos[kWarpRepMax];
   uint8_t hrm[kWarpSelMaxJ];
@@ -1713,37 +1764,52 @@ __global__ void __launch_bounds__(kWarpSelWarps * 32, 8) kap_select_warp_kernel(
         if (mk[e]) sm.rep_pos[pos++] = lane * E3 + e;
     }
     __syncwarp();
-    // exact scores s_ij = sum over rows r (ascending) of exp(bm[r,j] - M_r) with float64 logits, as
-    // in kap_select_kernel: lane group kgrp holds key j*KB + kgrp, its LPK lanes split d
-    constexpr int LPK = 32 / KB;
-    constexpr int SL = HD / LPK;
-    const int kgrp = lane / LPK, sub = lane % LPK;
+    // exact scores s_ij = sum over rows r (ascending) of exp(bm[r,j] - M_r), bm[r, j] the largest
+    // float64 logit of block j for row r.  Items are (repaired position, sampled row) pairs: (1) the
+    // fp32 logits of every item's keys; only keys within 2 e_r of their item's fp32 maximum can attain
+    // the exact block maximum and are listed; (2) the listed candidates get float64 logits, four lanes
+    // each, eight candidates at a time; (3) per item the largest is bm[r, j].
     const int nrows = r1 - r0;
+    const int n_items = n_rep * nrows;
     const int rp = (ri.R + kRowTile - 1) / kRowTile * kRowTile;
     const uint16_t* qbase = a.qs + (a.qs_off[b] + static_cast<int64_t>(h) * rp) * HD;
     const int64_t krow0 = a.ks_off[b] + static_cast<int64_t>(kvh) * rp;
     const float scl = static_cast<float>(a.sm_scale);
-#pragma unroll 1
-    for (int item = 0; item < n_rep * nrows; ++item) {
-      const int m = item / nrows, r = r0 + item % nrows;
-      const int j = key_block(sm.key[sm.rep_pos[m]]);
-      const double Mr = a.M[rbase + r];
-      double term = -INFINITY;
-      if (Mr != -INFINITY) {
-        const int kc = j * KB + kgrp;
-        const bool vis = kc <= r && ((a.kvalid[(krow0 + kc) >> 5] >> ((krow0 + kc) & 31)) & 1u);
-        const uint16_t* qr = qbase + static_cast<int64_t>(r) * HD + sub * SL;
-        const uint16_t* kr = vis ? a.ks + (krow0 + kc) * HD + sub * SL : qr;
-        float p0 = 0.0f, p1 = 0.0f;
-#pragma unroll 4
-        for (int e = 0; e < SL; e += 8) {
-          float qv[8], kv[8];
-          load8_bf16(qr + e, qv);
-          load8_bf16(kr + e, kv);
+    // (1) per repaired position, the fp32 logits of the query block's sampled rows against the block's
+    // sampled keys: lane group kq (LPK lanes splitting d) keeps key j*KB + kq in registers and takes
+    // the rows one after another (two interleaved partial sums: rounding depth SL/2 + 1 + log2(LPK),
+    // within e_r); each key row is loaded once per position, the query rows are shared through L1
+    constexpr int LPK = 32 / KB;
+    constexpr int SL = HD / LPK;
+    const int kq = lane / LPK, sub = lane % LPK;
+    int ncand = 0;
+    for (int m = 0; m < n_rep; ++m) {
+      const int kc = key_block(sm.key[sm.rep_pos[m]]) * KB + kq;
+      const bool kvis = (a.kvalid[(krow0 + kc) >> 5] >> ((krow0 + kc) & 31)) & 1u;
+      float kf[SL];
+      {
+        const uint16_t* kr = a.ks + (krow0 + kc) * HD + sub * SL;   // padded rows: always in the array
 #pragma unroll
-          for (int q = 0; q < 8; q += 2) {
-            p0 = fmaf(qv[q], kv[q], p0);
-            p1 = fmaf(qv[q + 1], kv[q + 1], p1);
+        for (int e = 0; e < SL; e += 8) {
+          float t8[8];
+          load8_bf16(kr + e, t8);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) kf[e + u] = t8[u];
+        }
+      }
+      for (int rr = 0; rr < nrows; ++rr) {
+        const int r = r0 + rr, item = m * nrows + rr;
+        const bool vis = kvis && kc <= r && a.M[rbase + r] != -INFINITY;
+        const uint16_t* qr = qbase + static_cast<int64_t>(r) * HD + sub * SL;
+        float p0 = 0.0f, p1 = 0.0f;
+#pragma unroll
+        for (int e = 0; e < SL; e += 8) {
+          float qv[8];
+          load8_bf16(qr + e, qv);
+#pragma unroll
+          for (int u = 0; u < 8; u += 2) {
+            p0 = fmaf(qv[u], kf[e + u], p0);
+            p1 = fmaf(qv[u + 1], kf[e + u + 1], p1);
           }
         }
         float part = p0 + p1;
@@ -1753,31 +1819,54 @@ __global__ void __launch_bounds__(kWarpSelWarps * 32, 8) kap_select_warp_kernel(
         float mx = x;
 #pragma unroll
         for (int o = LPK; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        if (mx != -INFINITY) {
-          const bool cand = vis && x >= mx - 2.0f * a.err[rbase + r];
-          uint32_t cmask = __ballot_sync(0xffffffffu, cand && sub == 0);
-          double dv = -INFINITY;
-          const uint16_t* qrow = qbase + static_cast<int64_t>(r) * HD;
-          while (cmask) {
-            const int gk = (__ffs(cmask) - 1) / LPK;
-            cmask &= cmask - 1;
-            const uint16_t* krow = a.ks + (krow0 + j * KB + gk) * HD;
-            double dp = 0.0;
-#pragma unroll
-            for (int e = lane * (HD / 32); e < (lane + 1) * (HD / 32); e += 2) {
-              const uint32_t qw = *reinterpret_cast<const uint32_t*>(qrow + e);
-              const uint32_t kw = *reinterpret_cast<const uint32_t*>(krow + e);
-              dp += static_cast<double>(__uint_as_float(qw << 16) * __uint_as_float(kw << 16));
-              dp += static_cast<double>(__uint_as_float(qw & 0xffff0000u) * __uint_as_float(kw & 0xffff0000u));
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) dp += __shfl_xor_sync(0xffffffffu, dp, o);
-            dv = fmax(dv, dp * a.sm_scale);
-          }
-          term = dv - Mr;
+        const bool cand = vis && sub == 0 && x >= mx - 2.0f * a.err[rbase + r];
+        if (lane == 0) sm.terms[item] = -INFINITY;
+        const unsigned cb = __ballot_sync(0xffffffffu, cand);
+        const int slot = ncand + __popc(cb & ((1u << lane) - 1u));
+        if (cand && slot < kWarpCand) sm.cand[slot] = (static_cast<uint32_t>(item) << 16) | static_cast<uint32_t>(kc);
+        ncand += __popc(cb);
+      }
+    }
+    if (ncand > kWarpCand) {   // a row with many tied keys: the block kernel settles it
+      defer();
+      return;
+    }
+    __syncwarp();
+    for (int c0 = 0; c0 < ncand; c0 += 8) {
+      const int ci = c0 + lane / 4, sub = lane % 4;
+      int item = -1;
+      double dp = 0.0;
+      if (ci < ncand) {
+        const uint32_t cw = sm.cand[ci];
+        item = static_cast<int>(cw >> 16);
+        const int r = r0 + item % nrows;
+        const int kc = static_cast<int>(cw & 0xffffu);
+        const uint16_t* qrow = qbase + static_cast<int64_t>(r) * HD + sub * (HD / 4);
+        const uint16_t* krow = a.ks + (krow0 + kc) * HD + sub * (HD / 4);
+#pragma unroll 4
+        for (int e = 0; e < HD / 4; e += 2) {
+          const uint32_t qw = *reinterpret_cast<const uint32_t*>(qrow + e);
+          const uint32_t kw = *reinterpret_cast<const uint32_t*>(krow + e);
+          dp += static_cast<double>(__uint_as_float(qw << 16) * __uint_as_float(kw << 16));
+          dp += static_cast<double>(__uint_as_float(qw & 0xffff0000u) * __uint_as_float(kw & 0xffff0000u));
         }
       }
-      if (lane == 0) sm.terms[item] = term;
+      dp += __shfl_xor_sync(0xffffffffu, dp, 1);
+      dp += __shfl_xor_sync(0xffffffffu, dp, 2);
+      const double lx = dp * a.sm_scale;
+      // fold the round's candidates into their items' maxima, one after another
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const double v = __shfl_sync(0xffffffffu, lx, 4 * t);
+        const int it = __shfl_sync(0xffffffffu, item, 4 * t);
+        if (lane == 0 && it >= 0) sm.terms[it] = fmax(sm.terms[it], v);
+      }
+    }
+    __syncwarp();
+    for (int item = lane; item < n_items; item += 32) {
+      const double Mr = a.M[rbase + r0 + item % nrows];
+      const double bmx = sm.terms[item];
+      sm.terms[item] = (Mr == -INFINITY || bmx == -INFINITY) ? -INFINITY : bmx - Mr;
     }
     __syncwarp();
     for (int item = lane; item < n_rep * nrows; item += 32) sm.terms[item] = exp(sm.terms[item]);
@@ -1882,7 +1971,7 @@ cudaError_t launch_kap_t(KapArgs a, size_t qs_rows, size_t ks_rows, cudaStream_t
     const size_t rows = static_cast<size_t>(a.num_q_heads) * (static_cast<size_t>(a.total_tokens) / a.stride + a.num_reqs);
     const unsigned blocks = static_cast<unsigned>((rows + 31) / 32);   // 8 warps of 4 rows
     kap_exact_kernel<HD><<<blocks, 256, 0, stream>>>(a);
-    kap_rescan_kernel<HD><<<1024, 512, 0, stream>>>(a);
+    kap_rescan_kernel<HD, KB><<<512, 256, 0, stream>>>(a);
   }
   kap_block_scores_kernel<KB><<<dim3(a.nqb_max, a.num_q_heads, a.num_reqs), 128, 0, stream>>>(a);
   int cap = kSelectThreads;   // the sort works on at least one key per thread
