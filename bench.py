@@ -262,6 +262,30 @@ def job_tflops(world: int, flops_per_rank_step: float, ms_per_step: float) -> fl
     return world * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
 
 
+def sum_over_ranks(x: float, world: int, device) -> float:
+    """The sum of a per-rank figure over the ranks (the work of the whole job); the value itself on one rank."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def shard_workload(w, rank: int, world: int):
+    """The kv heads of ``rank`` (and their query heads) of workload ``w``, as a workload of their own
+    (contiguous host arrays; the page table and request lengths are shared)."""
+    from block_sparse_long_gb300 import shard
+    sp = w.spec
+    G = sp.num_q_heads // sp.num_kv_heads
+    kv0, kv1 = shard.kv_head_range(rank, world, sp.num_kv_heads)
+    q, k, v = shard.shard_heads(w.q, w.k_cache, w.v_cache, kv0, kv1, G)
+    spec = sp.with_(num_q_heads=(kv1 - kv0) * G, num_kv_heads=kv1 - kv0)
+    return synth.Workload(spec=spec, q=q, k_cache=k, v_cache=v, page_table=w.page_table, cu_seqlens=w.cu_seqlens), \
+        (kv0, kv1)
+
+
 # --------------------------------------------------------------------------- #
 # reference arm: the oracle, as it stands, on the host cores
 # --------------------------------------------------------------------------- #
@@ -301,6 +325,8 @@ def run_reference(args, spec, workload_name, delta):
 def run_cosa(args, spec, workload_name, delta):
     world, rank, local = dist_env()
     w = synth.make_workload(spec)
+    w_full = w
+    by_heads = world > 1 and args.shard == "heads"
     # CPU baseline first: the oracle pool is forked before this process touches CUDA
     cpu = None
     if rank == 0 and world >= 1 and not args.no_cpu_baseline:
@@ -318,6 +344,11 @@ def run_cosa(args, spec, workload_name, delta):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    kv_range = (0, spec.num_kv_heads)
+    if by_heads:
+        # this rank's kv heads and their query heads: the step computes only those (strong scaling)
+        w, kv_range = shard_workload(w_full, rank, world)
+        spec = w.spec
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
@@ -389,7 +420,8 @@ def run_cosa(args, spec, workload_name, delta):
     if int(status.item()) != 0:
         raise RuntimeError(C.cosa_status_string(int(status.item())))
     ms_step = total_ms / args.steps
-    value = job_tflops(world, step_flops, ms_step)
+    job_flops = sum_over_ranks(step_flops, world, dev)      # the work of every rank's step
+    value = job_flops / (ms_step * 1e-3) / 1e12
 
     # end to end through the public API with host buffers (pinned), copies inside the timed region.
     # Two sets of device inputs and outputs, pipelined across steps: step s's host-to-device copies
@@ -455,6 +487,17 @@ def run_cosa(args, spec, workload_name, delta):
     if not np.array_equal(houts[(args.steps - 1) % 2].numpy(), out.view(torch.int16).cpu().numpy()):
         raise RuntimeError("end-to-end output differs from the device-resident run")
     e2e_ms = max_over_ranks(e_start.elapsed_time(e_stop) / args.steps, world, dev)
+    gathered = None
+    if by_heads and args.gather_out:
+        # the optional exchange of the head split: O of every head on every rank (outside the timed region)
+        from block_sparse_long_gb300 import shard
+        G = w_full.spec.num_q_heads // w_full.spec.num_kv_heads
+        torch.cuda.synchronize()
+        g0 = time.perf_counter()
+        full = shard.gather_heads(out, world, w_full.spec.num_kv_heads, G)
+        torch.cuda.synchronize()
+        gathered = {"ms": 1e3 * (time.perf_counter() - g0), "bytes_per_rank": full.numel() * full.element_size(),
+                    "heads": int(full.shape[1])}
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hpt, hcu))
     d2h = hout.numel() * hout.element_size()
 
@@ -470,14 +513,17 @@ def run_cosa(args, spec, workload_name, delta):
     cl = clk.summary()
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "strong" if by_heads else "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_name, "num_reqs": spec.num_reqs, "seq_lens": list(spec.lengths),
-                   "num_q_heads": spec.num_q_heads, "num_kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim,
+                   "num_q_heads": w_full.spec.num_q_heads, "num_kv_heads": w_full.spec.num_kv_heads,
+                   "head_dim": spec.head_dim,
                    "block_size": spec.block_size, "page_size": spec.page_size, "stride": spec.stride,
                    "stage1_budget": spec.budget_ppm / 1e6, "skip_delta": delta,
                    "l2": "inputs larger than L2 (q, k, v = %.2f GiB)" % ((q.numel() + k.numel() + v.numel()) * 2 / 2**30),
-                   "parallelism": f"independent replicas per GPU x{world}"},
+                   "parallelism": (f"kv heads [{kv_range[0]}, {kv_range[1]}) of {w_full.spec.num_kv_heads} on rank 0, "
+                                   f"{world} ranks" if by_heads else f"independent replicas per GPU x{world}")},
         "osk_ms": osk_avg, "kap_ms": statistics.mean(kap_ms),
         "osk_tflops": achieved, "osk_pct_bf16_peak": 100.0 * achieved / peak,
         "dense_equiv_tflops": dense_equiv_flops(spec) / (osk_avg * 1e-3) / 1e12,
@@ -489,7 +535,7 @@ def run_cosa(args, spec, workload_name, delta):
                      "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"bf16_tflops ({pk_src}, burst)"},
-        "e2e": {"value": job_tflops(world, step_flops, e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,
+        "e2e": {"value": job_flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
                 "pipelined": "two device input/output sets; step s's host-to-device copy and step s-1's "
                              "device-to-host read overlap the kernels",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -498,6 +544,8 @@ def run_cosa(args, spec, workload_name, delta):
     }
     if cpu is not None:
         line["cpu_baseline"] = cpu
+    if gathered is not None:
+        line["gather_out"] = gathered
     print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -782,6 +830,11 @@ def main():
     ap.add_argument("--workload", default="128k_gqa_student_t", choices=sorted(synth.WORKLOADS),
                     help="workload name (default: one 128K-token request, 32 q / 8 kv heads)")
     ap.add_argument("--impl", choices=["cosa", "reference"], default="cosa")
+    ap.add_argument("--shard", choices=["heads", "replicas"], default="heads",
+                    help="with N > 1 ranks: split the workload's kv heads (and their query heads) across the ranks "
+                         "(one job, strong scaling), or run a replica of the whole workload on every rank (weak)")
+    ap.add_argument("--gather-out", action="store_true",
+                    help="with --shard heads: all-gather O over heads after the timed region (reported apart)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--clocks-log", default=None, help="also write the raw nvidia-smi clock samples here")
     ap.add_argument("--sweep", action="store_true",
