@@ -273,13 +273,16 @@ def sum_over_ranks(x: float, world: int, device) -> float:
     return float(t.item())
 
 
-def shard_workload(w, rank: int, world: int):
+def shard_workload(w, rank: int, world: int, kv_range=None):
     """The kv heads of ``rank`` (and their query heads) of workload ``w``, as a workload of their own
-    (contiguous host arrays; the page table and request lengths are shared)."""
+    (contiguous host arrays; the page table and request lengths are shared).  ``kv_range`` (kv0, kv1)
+    names the kv heads directly instead."""
     from block_sparse_long_gb300 import shard
     sp = w.spec
     G = sp.num_q_heads // sp.num_kv_heads
-    kv0, kv1 = shard.kv_head_range(rank, world, sp.num_kv_heads)
+    kv0, kv1 = kv_range if kv_range is not None else shard.kv_head_range(rank, world, sp.num_kv_heads)
+    if not 0 <= kv0 < kv1 <= sp.num_kv_heads:
+        raise ValueError(f"kv heads [{kv0}, {kv1}) of {sp.num_kv_heads}")
     q, k, v = shard.shard_heads(w.q, w.k_cache, w.v_cache, kv0, kv1, G)
     spec = sp.with_(num_q_heads=(kv1 - kv0) * G, num_kv_heads=kv1 - kv0)
     return synth.Workload(spec=spec, q=q, k_cache=k, v_cache=v, page_table=w.page_table, cu_seqlens=w.cu_seqlens), \
@@ -325,6 +328,12 @@ def run_reference(args, spec, workload_name, delta):
 def run_cosa(args, spec, workload_name, delta):
     world, rank, local = dist_env()
     w = synth.make_workload(spec)
+    if args.kv_slice:
+        # a slice of the workload at full length: kv heads [a, b) and their query heads (for profiling)
+        a_, b_ = (int(x) for x in args.kv_slice.split(":"))
+        w, _ = shard_workload(w, 0, 1, kv_range=(a_, b_))
+        spec = w.spec
+        workload_name = f"{workload_name} kv heads [{a_}, {b_})"
     w_full = w
     by_heads = world > 1 and args.shard == "heads"
     # CPU baseline first: the oracle pool is forked before this process touches CUDA
@@ -833,6 +842,9 @@ def main():
     ap.add_argument("--shard", choices=["heads", "replicas"], default="heads",
                     help="with N > 1 ranks: split the workload's kv heads (and their query heads) across the ranks "
                          "(one job, strong scaling), or run a replica of the whole workload on every rank (weak)")
+    ap.add_argument("--kv-slice", default=None, metavar="A:B",
+                    help="run only kv heads [A, B) of the workload and their query heads (a full-length slice, "
+                         "for profiling); not a bench line of the whole workload")
     ap.add_argument("--gather-out", action="store_true",
                     help="with --shard heads: all-gather O over heads after the timed region (reported apart)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
