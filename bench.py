@@ -17,7 +17,8 @@ Prints one JSON line (rank 0).
 Other modes (one JSON line per measurement, not the bench line): --sweep (CoSA against the dense
 endpoint of the same kernel, 4K to 128K tokens), --ablation remap|jump|topp|union (skip ratio
 against Delta with and without page remapping, physical jumps against logical skipping of a binary
-mask, the top-p stage-1 rule, GQA page reuse), --clocks-log PATH (keep the raw clock samples).
+mask, the top-p stage-1 rule, GQA page reuse), --ablation union-kernel (the GQA page-union OSK against
+the default OSK on the same masks), --clocks-log PATH (keep the raw clock samples).
 """
 from __future__ import annotations
 
@@ -748,6 +749,44 @@ def run_ablation(args):
             del t
             torch.cuda.empty_cache()
         return 0
+    if args.ablation == "union-kernel":
+        # the GQA page-union OSK (COSA_FLAG_GQA_UNION) against the default OSK on the same KAP masks
+        for wl in ("32k_gqa_shuffled", "128k_gqa_student_t", "ragged4_gqa_noisy_masks"):
+            spec = synth.spec_for(wl)
+            w = synth.make_workload(spec)
+            delta = delta_for(wl)
+            t = dict(q=bf(w.q), k=bf(w.k_cache), v=bf(w.v_cache), pt=torch.from_numpy(w.page_table).to(dev),
+                     cu=torch.from_numpy(w.cu_seqlens).to(dev))
+            pitch = C.stage1_pitch(spec.budget_ppm, spec.max_seqlen, spec.block_size) + (4 if spec.mask_noise_frac else 0)
+            p = params(spec, t, spec.budget_ppm, pitch, delta)
+            mask, ml = C.cosa_proxy_select(p, t["q"], t["cu"], t["k"], t["pt"])
+            if spec.mask_noise_frac:
+                m_np, l_np = synth.inject_mask_noise(mask.cpu().numpy(), ml.cpu().numpy(), spec.lengths,
+                                                     spec.block_size, spec.mask_noise_frac, seed=spec.seed)
+                mask, ml = torch.from_numpy(m_np).to(dev), torch.from_numpy(l_np).to(dev)
+            out = torch.empty_like(t["q"])
+            pu = params(spec, t, spec.budget_ppm, pitch, delta, C.COSA_FLAG_GQA_UNION)
+            rec = {"ablation": "union-kernel", "workload": spec.name, "skip_delta": delta}
+            flags = {}
+            for name, pp in (("per_head", p), ("union", pu)):
+                rec[f"{name}_osk_ms"] = timed(lambda: C.cosa_sparse_prefill(pp, t["q"], t["cu"], t["k"], t["v"], t["pt"],
+                                                                            mask, ml, out=out), 5)
+                # rows of absent query blocks (shorter requests) are not written: 255 marks them
+                f = torch.full(mask.shape, 255, dtype=torch.uint8, device=dev)
+                C.cosa_sparse_prefill(pp, t["q"], t["cu"], t["k"], t["v"], t["pt"], mask, ml, out=out, visit_flags=f)
+                flags[name] = f.cpu().numpy()
+            live = flags["per_head"] != 255
+            visits = int((live & ((flags["per_head"] & 3) != C.VISIT_IGNORED)).sum())
+            shared = int((live & ((flags["union"] & C.VISIT_SHARED_LOAD) != 0)).sum())
+            rec.update({"visits": visits, "computed": int((flags["per_head"] == C.VISIT_COMPUTED).sum()),
+                        "per_head_k_loads": visits, "union_k_loads": visits - shared // 2,
+                        "k_loads_saved": (shared // 2) / max(1, visits),
+                        "decisions_equal": bool(np.array_equal(np.where(live, flags["union"] & 3, 255),
+                                                               flags["per_head"]))})
+            print(json.dumps(rec), flush=True)
+            del t, mask, ml, out, flags
+            torch.cuda.empty_cache()
+        return 0
     if args.ablation == "topp":
         n_tok = args.ablation_tokens
         spec, t = setup(n_tok)
@@ -851,10 +890,10 @@ def main():
     ap.add_argument("--clocks-log", default=None, help="also write the raw nvidia-smi clock samples here")
     ap.add_argument("--sweep", action="store_true",
                     help="time CoSA against the dense endpoint of the same kernel from 4K to 128K tokens")
-    ap.add_argument("--ablation", choices=["remap", "jump", "topp", "union"],
+    ap.add_argument("--ablation", choices=["remap", "jump", "topp", "union", "union-kernel"],
                     help="remap: skip ratio vs Delta with and without remapping over stage-1 budgets; "
                          "jump: physical jumps vs logical skipping of a binary mask; topp: the top-p stage-1 rule; "
-                         "union: GQA page reuse rates")
+                         "union: GQA page reuse rates; union-kernel: the GQA page-union OSK against the default OSK")
     ap.add_argument("--ablation-tokens", type=int, default=131072, help="context length of --ablation remap/topp")
     args = ap.parse_args()
     if args.sweep:

@@ -20,8 +20,9 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libcosa.so")
-SOURCES = ["api.cu", "osk.cu", "osk_p16.cu", "osk_p32.cu", "osk_p64.cu", "osk_p128.cu", "kap.cu"]
-HEADERS = ["ptx.cuh", "internal.h", "osk_kernel.cuh"]
+SOURCES = ["api.cu", "osk.cu", "osk_p16.cu", "osk_p32.cu", "osk_p64.cu", "osk_p128.cu", "osk_union_d64.cu",
+           "osk_union_d128.cu", "kap.cu"]
+HEADERS = ["ptx.cuh", "internal.h", "osk_kernel.cuh", "osk_union_kernel.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall", "--expt-relaxed-constexpr"]
 

@@ -97,6 +97,8 @@ COSA_FLAG_TEST_STALL = 1   # test hook of cosa_sparse_prefill: every in-kernel w
 COSA_FLAG_ASCENDING_ORDER = 2   # cosa_proxy_select writes the selected blocks in ascending order
 COSA_FLAG_BINARY_MASK = 4       # cosa_sparse_prefill reads mask rows as binary block masks
 COSA_FLAG_TOP_P = 8             # cosa_proxy_select: budget_ppm is the top-p threshold p
+COSA_FLAG_GQA_UNION = 16        # cosa_sparse_prefill: two query heads of a kv group share one K stream
+VISIT_SHARED_LOAD = 4           # visit-flag bit under COSA_FLAG_GQA_UNION: K loaded once for both heads
 
 
 def make_params(*, num_reqs, num_q_heads, num_kv_heads, head_dim, block_size, page_size, stride=None,

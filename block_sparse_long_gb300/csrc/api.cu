@@ -46,7 +46,8 @@ int check_common(const cosa_params* p) {
   if (p->total_tokens < 0 || p->max_seqlen < 1 || p->num_pages < 1 || p->max_pages_per_req < 1) return COSA_ERR_INVALID_ARG;
   if (p->mask_pitch < 1) return COSA_ERR_INVALID_ARG;
   if (!(p->sm_scale > 0.0) || !std::isfinite(p->sm_scale) || std::isnan(p->skip_delta)) return COSA_ERR_INVALID_ARG;
-  if ((p->flags & ~(COSA_FLAG_TEST_STALL | COSA_FLAG_ASCENDING_ORDER | COSA_FLAG_BINARY_MASK | COSA_FLAG_TOP_P)) != 0)
+  if ((p->flags & ~(COSA_FLAG_TEST_STALL | COSA_FLAG_ASCENDING_ORDER | COSA_FLAG_BINARY_MASK | COSA_FLAG_TOP_P |
+                    COSA_FLAG_GQA_UNION)) != 0)
     return COSA_ERR_INVALID_ARG;
   if (p->head_dim != 64 && p->head_dim != 128) return COSA_ERR_UNSUPPORTED;
   if (p->block_size != 64 && p->block_size != 128) return COSA_ERR_UNSUPPORTED;
@@ -183,6 +184,8 @@ int cosa_sparse_prefill(const cosa_params* p, const void* q, const int32_t* cu_s
   if (rc != COSA_OK) return rc;
   const int64_t nqb_max = ceil_div(p->max_seqlen, p->block_size);
   if (nqb_max > kMaxQueryBlocksOsk) return COSA_ERR_UNSUPPORTED;
+  if ((p->flags & COSA_FLAG_GQA_UNION) && (p->block_size != 128 || (p->flags & COSA_FLAG_BINARY_MASK)))
+    return COSA_ERR_UNSUPPORTED;
   if (!q || !cu_seqlens || !k_cache || !v_cache || !page_table || !mask || !mask_len || !out) return COSA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
       !aligned(cu_seqlens, 4) || !aligned(page_table, 4) || !aligned(mask, 4) || !aligned(mask_len, 4))

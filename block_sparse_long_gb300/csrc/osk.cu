@@ -1,5 +1,6 @@
 // Ordered-Skipping Kernel (OSK): shared-memory sizes and the dispatch of a call to the instances
-// of its page size (the kernel itself is in osk_kernel.cuh).
+// of its page size (the kernel itself is in osk_kernel.cuh), or to the GQA page-union kernel
+// (osk_union_kernel.cuh) under COSA_FLAG_GQA_UNION.
 #include "osk_kernel.cuh"
 
 namespace cosa {
@@ -11,7 +12,14 @@ size_t osk_smem_bytes(int block_size, int head_dim) {
   return sizeof(OskSmem<64, 64>) + 1024;
 }
 
+cudaError_t launch_osk_union_d64(const OskLaunch& L, cudaStream_t stream);
+cudaError_t launch_osk_union_d128(const OskLaunch& L, cudaStream_t stream);
+
 cudaError_t launch_osk(const OskLaunch& L, cudaStream_t stream) {
+  if (L.flags & COSA_FLAG_GQA_UNION) {
+    if (L.block_size != 128) return cudaErrorInvalidValue;
+    return L.head_dim == 128 ? launch_osk_union_d128(L, stream) : launch_osk_union_d64(L, stream);
+  }
   switch (L.page_size) {
     case 16: return launch_osk_p16(L, stream);
     case 32: return launch_osk_p32(L, stream);

@@ -94,11 +94,25 @@ extern "C" {
    cut is taken on the kernel's fp32 scores (summed in float64); mask_pitch must be >= ceil(max_seqlen /
    block_size), since K_i can reach i + 1. */
 #define COSA_FLAG_TOP_P 8
+/* GQA page union (cosa_sparse_prefill; ignored by cosa_proxy_select).  PageWeaver notes, Sec. 2.2: the
+   query heads of a kv group select largely the same pages, so one K load can serve several of them
+   (the union U_G with a membership mask per head).  Under this flag one CTA serves two query heads
+   2x, 2x+1 of a kv group (the last head alone when Hq/Hkv is odd) for one query block, from one
+   stream of K tiles: the two heads' de-duplicated valid block lists, each in its own mask order, are
+   merged by taking at every step the block that is next for both heads if they agree, else the
+   lower of the two next block IDs (which serves only the head it is next for).  Each head still
+   visits exactly its own blocks in its own order with its own running maximum and skip vote, so
+   out and the visit decisions equal those of the default kernel bit for bit; visit_flags entries
+   whose K tile was loaded once for both heads carry COSA_VISIT_SHARED_LOAD in addition.  Requires
+   block_size 128; not combinable with COSA_FLAG_BINARY_MASK. */
+#define COSA_FLAG_GQA_UNION 16
 
 /* values written to visit_flags (one per mask entry) */
 #define COSA_VISIT_COMPUTED 0 /* softmax and P.V accumulated (pattern 3 of the paper's Fig. 4) */
 #define COSA_VISIT_SKIPPED 1  /* Q.K^T computed, in-kernel skip rule fired (pattern 2)         */
 #define COSA_VISIT_IGNORED 2  /* invalid, repeated, or past mask_len: never loaded            */
+#define COSA_VISIT_SHARED_LOAD 4 /* bit OR-ed onto COMPUTED / SKIPPED under COSA_FLAG_GQA_UNION:
+                                    the block's K tile was gathered once for both heads of a pair */
 
 typedef struct cosa_params {
   int32_t num_reqs;          /* B >= 1                                                        */

@@ -392,23 +392,48 @@ def reuse_rate(groups: Sequence[Sequence[Sequence[int]]]) -> float:
     return num / den if den else 0.0
 
 
-def ordered_shared_loads(orders: Sequence[Sequence[int]]) -> int:
-    """Loads of a traversal shared by a group of heads that each keep their own visiting order (the
-    GQA union for CoSA's ordered visits): each load serves every head whose next pending block it
-    is.  Greedy: load the block that is next for the most heads (ties: lowest block ID).  An upper
-    bound on the shortest common supersequence of the orders; equal to sum |S_i| when no two heads
-    ever wait for the same block, and to |U_G| when all heads share one order."""
+def kept_visits(mask_row: Sequence[int], n: int, i: int, nblk: int) -> List[Tuple[int, int]]:
+    """The blocks Algorithm A visits for query block i from the mask entries 0..n-1, as (k, j) pairs
+    in mask order: entries with 0 <= j <= i and j < nblk, each block at its first occurrence (the
+    entries osk_qblock does not flag IGNORED)."""
+    seen = set()
+    out = []
+    for k in range(n):
+        j = int(mask_row[k])
+        if not (0 <= j <= i and j < nblk) or j in seen:
+            continue
+        seen.add(j)
+        out.append((k, j))
+    return out
+
+
+def union_traversal(orders: Sequence[Sequence[int]]) -> List[Tuple[int, Tuple[int, ...]]]:
+    """One K stream for a group of heads that each keep their own visiting order: PageWeaver Sec. 2.2
+    (a shared traversal of the group's pages with a membership mask per head) applied to CoSA's ordered
+    visits (Sec. 4.3).  Returns the loads in order as (block, members): the heads (indices into
+    ``orders``) whose next pending block it is; each of them moves past it.  Greedy: load the block that
+    is next for the most heads, ties to the lowest block ID.  Repeats inside an order count once (first
+    occurrence).  Each head's blocks, read off the loads it is a member of, are its own order."""
     seqs = [list(dict.fromkeys(int(x) for x in o)) for o in orders]   # first occurrence of each ID
     pos = [0] * len(seqs)
-    loads = 0
+    loads = []
     while any(p < len(q) for p, q in zip(pos, seqs)):
         cand = {}
         for p, q in zip(pos, seqs):
             if p < len(q):
                 cand[q[p]] = cand.get(q[p], 0) + 1
         blk = min(cand, key=lambda b: (-cand[b], b))
+        members = []
         for h, q in enumerate(seqs):
             if pos[h] < len(q) and q[pos[h]] == blk:
+                members.append(h)
                 pos[h] += 1
-        loads += 1
+        loads.append((blk, tuple(members)))
     return loads
+
+
+def ordered_shared_loads(orders: Sequence[Sequence[int]]) -> int:
+    """Loads of union_traversal: an upper bound on the shortest common supersequence of the orders;
+    equal to sum |S_i| when no two heads ever wait for the same block, and to |U_G| when all heads
+    share one order."""
+    return len(union_traversal(orders))

@@ -472,6 +472,57 @@ def check_query_union(orc):
         assert len(orc.query_union(G)[0]) <= n <= sum(len(S) for S in G)
 
 
+def check_union_traversal(orc):
+    # by hand: heads wait for 5 and 3 -> the lower ID (3) serves head 1 alone; then both wait for 5;
+    # then 3 for head 0; then both wait for 7
+    assert orc.union_traversal([[5, 3, 7], [3, 5, 7]]) == [(3, (1,)), (5, (0, 1)), (3, (0,)), (7, (0, 1))]
+    assert orc.union_traversal([[1, 2], [3, 4]]) == [(1, (0,)), (2, (0,)), (3, (1,)), (4, (1,))]
+    assert orc.union_traversal([[4, 4, 9], [], [9]]) == [(4, (0,)), (9, (0, 2))]      # repeats once
+    assert orc.union_traversal([[2, 8], [8, 2], [8]]) == [(8, (1, 2)), (2, (0, 1)), (8, (0,))]  # most heads first
+    assert orc.union_traversal([[], []]) == []
+    rng = np.random.default_rng(5)
+    for _ in range(100):
+        H = int(rng.integers(1, 5))
+        G = [list(rng.integers(0, 12, size=int(rng.integers(0, 9)))) for _ in range(H)]
+        loads = orc.union_traversal(G)
+        assert len(loads) == orc.ordered_shared_loads(G)
+        pos = [0] * H
+        seqs = [list(dict.fromkeys(int(x) for x in o)) for o in G]
+        for blk, members in loads:
+            assert members and list(members) == sorted(set(members))
+            # exactly the heads whose next pending block this is, and as many as any candidate has
+            nxt = [q[p] if p < len(q) else None for p, q in zip(pos, seqs)]
+            assert [h for h in range(H) if nxt[h] == blk] == list(members)
+            counts = {b: nxt.count(b) for b in nxt if b is not None}
+            assert len(members) == max(counts.values())
+            assert blk == min(b for b, c in counts.items() if c == len(members))
+            for h in members:
+                pos[h] += 1
+        # every head saw its own order, in order, once
+        assert pos == [len(q) for q in seqs]
+        for h in range(H):
+            assert [b for b, m in loads if h in m] == seqs[h]
+
+
+def check_kept_visits(orc):
+    # row of query block 3 (4 blocks exist): -1 and 5 are invalid, the second 2 repeats the first
+    assert orc.kept_visits([2, -1, 2, 0, 5, 1, 3], 7, 3, 4) == [(0, 2), (3, 0), (5, 1), (6, 3)]
+    assert orc.kept_visits([2, -1, 2, 0, 5, 1, 3], 5, 3, 4) == [(0, 2), (3, 0)]   # entries past n unread
+    assert orc.kept_visits([0, 1, 2], 3, 2, 2) == [(0, 0), (1, 1)]               # block 2 does not exist
+    # the same entries as osk_qblock visits (those it does not flag IGNORED)
+    rng = np.random.default_rng(6)
+    for _ in range(40):
+        i, nblk = int(rng.integers(0, 6)), int(rng.integers(1, 7))
+        row = rng.integers(-2, 8, size=9)
+        n = int(rng.integers(0, 10))
+        L, d = 4 * nblk, 4
+        Q = rng.standard_normal((L, d))
+        r = orc.osk_qblock(Q, Q, Q, np.ones(L, bool), min(i, nblk - 1), row, min(n, 9),
+                           orc.Params(4, 4, 1, 1_000_000, 0.5, -1.0))
+        kept = orc.kept_visits(row, min(n, 9), min(i, nblk - 1), nblk)
+        assert [k for k, _ in kept] == [k for k in range(min(n, 9)) if r.flags[k] != orc.IGNORED]
+
+
 # --------------------------------------------------------------------------- #
 # ablation modes: ascending-order visiting (no remap) and binary-mask visiting
 # --------------------------------------------------------------------------- #
@@ -560,5 +611,5 @@ ALL_CHECKS = [
     check_direct_definition, check_skip_hand_cases, check_skip_bucket_case, check_skip_invariants,
     check_stage1_count, check_kap_hand_cases, check_kap_brute_force, check_kap_invariants,
     check_kap_mask_layout, check_ascending_mask, check_binary_mask_visiting, check_top_p_count,
-    check_query_union,
+    check_query_union, check_union_traversal, check_kept_visits,
 ]

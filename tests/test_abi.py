@@ -89,6 +89,10 @@ def test_host_validation(lib):
     assert kap(_params(lib, flags=1 << 5)) == lib.COSA_ERR_INVALID_ARG
     assert kap(_params(lib, flags=lib.COSA_FLAG_TOP_P, mask_pitch=7)) == lib.COSA_ERR_INVALID_ARG   # K_i up to 8
     assert osk(_params(lib, total_tokens=0)) == lib.COSA_OK                 # nothing to do
+    # the GQA page-union kernel serves 128-token blocks of ID-list masks only
+    assert osk(_params(lib, flags=lib.COSA_FLAG_GQA_UNION, block_size=64, stride=8)) == lib.COSA_ERR_UNSUPPORTED
+    assert osk(_params(lib, flags=lib.COSA_FLAG_GQA_UNION | lib.COSA_FLAG_BINARY_MASK)) == lib.COSA_ERR_UNSUPPORTED
+    assert osk(_params(lib, flags=lib.COSA_FLAG_GQA_UNION, total_tokens=0)) == lib.COSA_OK
 
 
 def test_kap_stride_validation(lib):

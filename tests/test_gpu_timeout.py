@@ -22,7 +22,10 @@ def _small():
     return sp, synth.make_workload(sp)
 
 
-def test_stalled_producer_times_out_and_context_survives():
+@pytest.mark.parametrize("union", [False, True])
+def test_stalled_producer_times_out_and_context_survives(union):
+    """Both OSK kernels: the default one and the GQA page-union one (COSA_FLAG_GQA_UNION)."""
+    extra = gh.C.COSA_FLAG_GQA_UNION if union else 0
     sp, w = _small()
     prm = gh.oracle_params(sp, 40.0)
     pitch = gh.C.stage1_pitch(sp.budget_ppm, sp.max_seqlen, sp.block_size)
@@ -35,7 +38,7 @@ def test_stalled_producer_times_out_and_context_survives():
 
     # stalled: every wait runs out (2 s budget), the kernel stops and reports it
     p = gh.cosa_params(dw, delta=40.0, mask_pitch=pitch)
-    p.flags = gh.C.COSA_FLAG_TEST_STALL
+    p.flags = gh.C.COSA_FLAG_TEST_STALL | extra
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     out = torch.zeros_like(dw.q)
     t0 = time.perf_counter()
@@ -46,9 +49,9 @@ def test_stalled_producer_times_out_and_context_survives():
     assert elapsed < 30.0, elapsed
 
     # the context is still good: the same call without the hook succeeds and matches the oracle
-    p.flags = 0
+    p.flags = extra
     out2, flags2 = gh.run_osk(dw, p, mask, ml)
-    rep = gh.compare_osk(w, prm, mask, ml, out2, flags2, gh.items_of(sp))
+    rep = gh.compare_osk(w, prm, mask, ml, out2, flags2 & 3, gh.items_of(sp))
     gh.assert_osk_ok(rep)
 
 

@@ -63,6 +63,10 @@ MUTATIONS = {
     "reuse_rate_counts_repeats": ("num = sum(len(set(int(x) for x in S)) for G in groups for S in G)",
                                   "num = sum(len(S) for G in groups for S in G)"),
     "shared_load_serves_one_head": ("                pos[h] += 1\n", "                pos[h] += 1\n                break\n"),
+    "union_tie_to_highest_id": ("blk = min(cand, key=lambda b: (-cand[b], b))", "blk = min(cand, key=lambda b: (-cand[b], -b))"),
+    "union_fewest_heads_first": ("blk = min(cand, key=lambda b: (-cand[b], b))", "blk = min(cand, key=lambda b: (cand[b], b))"),
+    "kept_visits_keeps_future": ("if not (0 <= j <= i and j < nblk) or j in seen:", "if not (0 <= j and j < nblk) or j in seen:"),
+    "kept_visits_keeps_repeats": ("if not (0 <= j <= i and j < nblk) or j in seen:", "if not (0 <= j <= i and j < nblk):"),
 }
 
 
