@@ -512,9 +512,22 @@ __global__ void __launch_bounds__(kLogitsThreads, 2)
 
 // ---------------------------------------------------------------------------
 // block scores (Eqs. (9)-(11)): s_ij = sum over the sampled rows r of query block i of
-// Pbar[r, j] = exp(bm[r, j] * scale - M_r), with the float64 row maxima M_r (rounded to fp32), and a
-// bound on |s_ij - exact|.  A block per (request, head, query block), a thread per key block j <= i.
+// Pbar[r, j] = exp(bm[r, j] * scale - M_r), with the float64 row maxima M_r, and a bound on
+// |s_ij - exact|.  A block per (request, head, query block), a thread per key block j <= i.
+//
+// Each term is taken in base 2: x = 2^u, u = bm * (scale log2 e) - M_r log2 e, by the hardware
+// exponential, whose relative error is at most kEx2Rel (a test measures it over every input).  The
+// first factor is rounded once to fp32; the second three times (M_r to fp32, the fp32 log2 e, their
+// product); the fmaf once.  With |bm * scale log2 e| <= |u| + |M_r log2 e| and U the exact exponent,
+//   |u - U| <= log2 e * dl * ||k||max_j + 2^-23 |u| + 2^-22 |M_r log2 e|,
+// dl = kKappa * scale * ||q_r|| the logit error per unit key norm; and |2^D - 1| <= 1.02 ln 2 |D|
+// for |D| <= 0.04.  Hence
+//   |x - 2^U| <= x (1 + 2^-19) (kEx2Rel + 1.02 dl ||k||max_j + 1.7e-7 |M_r log2 e| + 8.5e-8 |u|),
+// plus 2^-125 for a result the instruction flushes to zero (u < -126: the exact value is below
+// 2^-125 too).  Blocks outside that expansion's range take a looser bound through expm1f.
 // ---------------------------------------------------------------------------
+constexpr float kEx2Rel = 8.0f / 16777216.0f;   // 2^-21: the relative error assumed of ex2.approx.ftz.f32
+
 template <int KB>
 __global__ void __launch_bounds__(128) kap_block_scores_kernel(KapArgs a) {
   const int i = a.nqb_max - 1 - static_cast<int>(blockIdx.x);   // heaviest query blocks first
@@ -524,57 +537,87 @@ __global__ void __launch_bounds__(128) kap_block_scores_kernel(KapArgs a) {
   const int nqb = ri.nqb;
   const int kvh = h / (a.num_q_heads / a.num_kv_heads);
   const float scale = static_cast<float>(a.sm_scale);
+  const float sl2 = static_cast<float>(a.sm_scale * 1.4426950408889634);
   const int64_t rbase = a.row_off[b] + static_cast<int64_t>(h) * ri.R;
   const float* bm_blk = a.bm + a.bm_off[b] + static_cast<int64_t>(h) * bm_block_base(nqb, KB) + bm_block_base(i, KB);
   const int64_t pitch = bm_pitch(i, KB);
   const float* kbn = a.kbnorm + (static_cast<size_t>(b) * a.num_kv_heads + kvh) * a.nqb_max;
   const int64_t sbase = a.sc_off[b] + static_cast<int64_t>(h) * nqb * nqb + static_cast<int64_t>(i) * nqb;
-  // the query block's sampled rows: rounded row maximum and the logit error scale
-  float M32[KB], ebase[KB];
+  constexpr float kGrow = 1.0f + 1.0f / 524288.0f;   // 1 + 2^-19
+  constexpr float kRnd = 8.5e-8f;                    // >= 1.02 ln 2 2^-23 (|u|)
+  constexpr float kRndM = 1.7e-7f;                   // >= 1.02 ln 2 2^-22 (|M_r log2 e|)
+  // per sampled row of the query block, computed once per block (float64 is slow here): M_r log2 e
+  // and the bound's parts.  A row without a visible key (M_r = -inf) gets +inf, which makes every u
+  // -inf and its terms 0.
+  __shared__ float s_ml2[KB], s_a[KB], s_b[KB], s_dl[KB];
+  if (threadIdx.x < KB) {
+    const int q = threadIdx.x, r = i * KB + q;
+    float ml2 = INFINITY, av = 0.0f, bv = 0.0f, dl = 0.0f;
+    if (r < ri.R) {
+      const float M = static_cast<float>(a.M[rbase + r]);
+      if (M != -INFINITY) {
+        ml2 = M * 1.44269504f;
+        dl = kKappa * scale * a.qnorm[rbase + r] * 1.001f;
+        av = kGrow * (kEx2Rel + kRndM * fabsf(ml2));
+        bv = kGrow * 1.02f * dl;
+      }
+    }
+    s_ml2[q] = ml2;
+    s_a[q] = av;
+    s_b[q] = bv;
+    s_dl[q] = dl;
+  }
+  __syncthreads();
+  float Ml2[KB], A[KB], B[KB];
+  float dl_max = 0.0f, ml_max = 0.0f;
 #pragma unroll
   for (int q = 0; q < KB; ++q) {
-    const int r = i * KB + q;
-    M32[q] = -INFINITY;
-    ebase[q] = 0.0f;
-    if (r < ri.R) {
-      M32[q] = static_cast<float>(a.M[rbase + r]);
-      ebase[q] = kKappa * scale * a.qnorm[rbase + r] * 1.001f;
-    }
+    Ml2[q] = s_ml2[q];
+    A[q] = s_a[q];
+    B[q] = s_b[q];
+    dl_max = fmaxf(dl_max, s_dl[q]);
+    if (A[q] != 0.0f) ml_max = fmaxf(ml_max, fabsf(Ml2[q]));
   }
+  const float C = kGrow * kRnd;
   for (int j = threadIdx.x; j <= i; j += blockDim.x) {
     const float kbv = __ldg(kbn + j);
     // every row's block maximum is requested before any is used
     float bmv[KB];
 #pragma unroll
     for (int q = 0; q < KB; ++q) bmv[q] = (i * KB + q < ri.R) ? __ldcs(bm_blk + q * pitch + j) : -INFINITY;
-    float x[KB], xe[KB];
+    float x[KB];
+    float xe = 0.0f;
+    if (dl_max * kbv <= 0.013f && ml_max <= 1.0e5f) {
 #pragma unroll
-    for (int q = 0; q < KB; ++q) {
-      x[q] = 0.0f;
-      xe[q] = 0.0f;
-      const float bm = bmv[q];
-      if (bm != -INFINITY && M32[q] != -INFINITY) {
-        const float u = fmaf(bm, scale, -M32[q]);
-        x[q] = expf(u);
-        // |u - exact| <= kappa * scale * ||q|| * (largest ||k|| of block j) plus the rounding of the
-        // scaled logit, of M_r and of the subtraction; expf adds at most 2 ulp; exp(du) - 1 <=
-        // 1.02 du for du <= 0.03; a value below exp(-80) is only bounded absolutely
-        const float du = ebase[q] * kbv + 1.2e-7f * (2.0f * fabsf(M32[q]) + fabsf(u) + 1.0f);
-        const float rel = (du <= 0.03f) ? 1.02f * du : expm1f(du) * 1.01f;
-        xe[q] = x[q] * (rel + 3.0e-7f) + ((u < -80.0f) ? 2.0e-35f : 0.0f);
+      for (int q = 0; q < KB; ++q) {
+        const float u = fmaf(bmv[q], sl2, -Ml2[q]);
+        x[q] = ex2_approx(u);
+        const float t = fmaf(C, fminf(fabsf(u), 1024.0f), fmaf(B[q], kbv, A[q]));
+        xe = fmaf(x[q], t, xe);
+      }
+    } else {
+      // far outside the usual range: D may exceed 0.04, take |2^D - 1| <= expm1(ln 2 |D|) directly
+#pragma unroll
+      for (int q = 0; q < KB; ++q) {
+        x[q] = 0.0f;
+        if (A[q] == 0.0f) continue;   // a row without a visible key
+        const float u = fmaf(bmv[q], sl2, -Ml2[q]);
+        x[q] = ex2_approx(u);
+        const float D = 1.4426950408889634f * B[q] / (kGrow * 1.02f) * kbv +
+                        1.2e-7f * (2.0f * fabsf(Ml2[q]) + fminf(fabsf(u), 1.0e30f));
+        const float rel = expm1f(0.6931472f * D) * 1.01f + kEx2Rel * 1.01f;
+        xe = fmaf(x[q], kGrow * rel, xe);
       }
     }
     // pairwise sum over the rows (log2 KB levels)
 #pragma unroll
     for (int o = KB / 2; o > 0; o >>= 1) {
 #pragma unroll
-      for (int q = 0; q < o; ++q) {
-        x[q] += x[q + o];
-        xe[q] += xe[q + o];
-      }
+      for (int q = 0; q < o; ++q) x[q] += x[q + o];
     }
     a.score[sbase + j] = x[0];
-    a.score_err[sbase + j] = xe[0] + x[0] * (4.0f * 6.0e-8f);   // rounding of the kb-term sum
+    // the fmaf chain's own roundings, the pairwise sum's, and the flushed results
+    a.score_err[sbase + j] = xe * kGrow + x[0] * (4.0f * 6.0e-8f) + KB * 2.36e-38f;
   }
 }
 
@@ -825,8 +868,13 @@ __global__ void __launch_bounds__(256) kap_rescan_kernel(KapArgs a) {
 // ---------------------------------------------------------------------------
 // dynamic shared memory of kap_select for `cap` candidates (a power of two)
 constexpr int kRepChunk = 64;            // repaired positions per round of the float64 repair
+// per warp of the select kernel: one key block staged for the bulk exact scores, rows padded by 16 bytes
+// (the rows of a block then start in different banks); sized for 16 keys of d = 128
+constexpr int kBulkRowPitch = 128 + 8;    // bf16 elements
+constexpr size_t kBulkSlabBytes = static_cast<size_t>(kSelectThreads / 32) * 16 * kBulkRowPitch * 2;
 __host__ __device__ inline size_t select_smem_bytes(int cap) {
-  return static_cast<size_t>(cap) * (8 + 4 + 4 + 4 + 4 + 8 + 1 + 1) + 64 + kRepChunk * 16 * sizeof(double) + 64;
+  return static_cast<size_t>(cap) * (8 + 4 + 4 + 4 + 4 + 8 + 1 + 1) + 64 + kRepChunk * 16 * sizeof(double) + 64 +
+         kBulkSlabBytes;
 }
 
 __device__ __forceinline__ unsigned long long sort_key(bool hrm, float s, int j) {
@@ -1004,52 +1052,268 @@ __device__ void select_top_keys(unsigned long long* key, const uint8_t* hrm, con
   sort_keys_desc<1>(s1, key, kSelectThreads);
 }
 
-// Top-p length: the shortest prefix of the sorted candidates key[0..J) whose fp32 scores (summed in
-// float64) reach p = ppm / 1e6 of the total; at least 1.  Thread t scans positions t*E .. t*E+E-1.
-__device__ int top_p_count(const unsigned long long* key, const float* score, int J, int ppm, double* warp_sum,
-                           int& first_s) {
+// Top-p length (the shortest prefix of rho_i whose scores reach p of the row's total), bracketed by
+// the score intervals [s - e, s + e] (s clamped at 0) of the sorted candidates key[0..J).  With
+//   f(k) = (1 - p) sum_{x<k} s_x - p sum_{x>=k} s_x,
+// non-decreasing in k, the exact length is the least k with f(k) >= 0: it is at least K_lo, the least
+// k whose upper bound of f reaches 0, and at most K_hi, the least k whose lower bound does.  Sums in
+// float64; a margin of 1e-12 of the total covers their rounding.  K_lo == K_hi certifies the length.
+__device__ int2 top_p_range(const unsigned long long* key, const float* score, const float* serr, int J, int ppm,
+                            double* ws_lo, double* ws_hi, int* kr) {
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int E = (J + kSelectThreads - 1) / kSelectThreads;
-  double part = 0.0;
-  for (int e = 0; e < E; ++e) {
-    const int x = tid * E + e;
-    if (x < J) part += static_cast<double>(fmaxf(score[key_block(key[x])], 0.0f));
-  }
-  double incl = part;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const double y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) warp_sum[w] = incl;
-  if (tid == 0) first_s = J;
-  __syncthreads();
-  double before = incl - part, total = 0.0;
-  for (int q = 0; q < kSelectThreads / 32; ++q) {
-    if (q < w) before += warp_sum[q];
-    total += warp_sum[q];
-  }
-  const double thr = static_cast<double>(ppm) / 1e6 * total;
-  double run = before;
+  double plo = 0.0, phi = 0.0;
   for (int e = 0; e < E; ++e) {
     const int x = tid * E + e;
     if (x >= J) break;
-    run += static_cast<double>(fmaxf(score[key_block(key[x])], 0.0f));
-    if (run >= thr) {
-      atomicMin(&first_s, x);
+    const int j = key_block(key[x]);
+    const float sv = fmaxf(score[j], 0.0f);
+    plo += static_cast<double>(fmaxf(sv - serr[j], 0.0f));
+    phi += static_cast<double>(sv) + static_cast<double>(serr[j]);
+  }
+  double ilo = plo, ihi = phi;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double ylo = __shfl_up_sync(0xffffffffu, ilo, o);
+    const double yhi = __shfl_up_sync(0xffffffffu, ihi, o);
+    if (lane >= o) {
+      ilo += ylo;
+      ihi += yhi;
+    }
+  }
+  if (lane == 31) {
+    ws_lo[w] = ilo;
+    ws_hi[w] = ihi;
+  }
+  if (tid == 0) kr[0] = kr[1] = J;
+  __syncthreads();
+  double run_lo = ilo - plo, run_hi = ihi - phi, TL = 0.0, TH = 0.0;
+  for (int q = 0; q < kSelectThreads / 32; ++q) {
+    if (q < w) {
+      run_lo += ws_lo[q];
+      run_hi += ws_hi[q];
+    }
+    TL += ws_lo[q];
+    TH += ws_hi[q];
+  }
+  const double p = static_cast<double>(ppm) / 1e6, eps = 1e-12 * TH;
+  // both tests are monotone in x: each thread reports only its first position passing each
+  bool got_lo = false;
+  for (int e = 0; e < E; ++e) {
+    const int x = tid * E + e;
+    if (x >= J) break;
+    const int j = key_block(key[x]);
+    const float sv = fmaxf(score[j], 0.0f);
+    run_lo += static_cast<double>(fmaxf(sv - serr[j], 0.0f));
+    run_hi += static_cast<double>(sv) + static_cast<double>(serr[j]);
+    // prefix of length x + 1: upper bound of f >= 0 possible, lower bound of f >= 0 certain
+    if (!got_lo && (1.0 - p) * run_hi + p * run_lo >= p * TL - eps) {
+      atomicMin(&kr[0], x + 1);
+      got_lo = true;
+    }
+    if (got_lo && (1.0 - p) * run_lo + p * run_hi >= p * TH + eps) {
+      atomicMin(&kr[1], x + 1);
       break;
     }
   }
   __syncthreads();
-  const int k = first_s + 1;
+  int2 r = make_int2(kr[0], kr[1]);
   __syncthreads();
-  return k < 1 ? 1 : (k > J ? J : k);
+  r.x = r.x < 1 ? 1 : (r.x > J ? J : r.x);
+  r.y = r.y < r.x ? r.x : (r.y > J ? J : r.y);
+  return r;
 }
 
 template <int E>
 __device__ void select_top_dispatch(unsigned long long* key, const uint8_t* hrm, const float* score,
                                     const float* serr, int J, int K, TopkShared& sh) {
   select_top_keys<E>(key, hrm, score, serr, J, K, sh);
+}
+
+// Exact scores s_ij = sum over the query block's sampled rows r (ascending) of exp(bm[r,j] - M_r) with
+// float64-accurate logits, for the blocks at positions pos[0..n) of the sorted keys, into val[0..n).
+// A warp per (position, row): lane group kgrp holds key j*KB + kgrp of the block, its LPK lanes split
+// d; the keys whose fp32 logit lies within 2 e_r of the block's fp32 maximum get the float64 dot.
+// Ends with the block synchronised.
+template <int HD, int KB>
+__device__ void exact_scores(const KapArgs& a, const unsigned long long* key, const int32_t* pos, int n, double* val,
+                             double* terms, int b, int h, int kvh, int r0, int r1, int R, int64_t rbase) {
+  constexpr int LPK = 32 / KB;
+  constexpr int SL = HD / LPK;
+  const int tid = threadIdx.x;
+  const int warps = blockDim.x / 32, w = tid >> 5, lane = tid & 31;
+  const int kgrp = lane / LPK, sub = lane % LPK;
+  const int nrows = r1 - r0;
+  const int rp = (R + kRowTile - 1) / kRowTile * kRowTile;
+  const uint16_t* qbase = a.qs + (a.qs_off[b] + static_cast<int64_t>(h) * rp) * HD;
+  const int64_t krow0 = a.ks_off[b] + static_cast<int64_t>(kvh) * rp;
+  const float sc = static_cast<float>(a.sm_scale);
+  for (int base = 0; base < n; base += kRepChunk) {
+    const int nm = min(kRepChunk, n - base);
+    for (int item = w; item < nm * nrows; item += warps) {
+      const int m = base + item / nrows, r = r0 + item % nrows;
+      const int j = key_block(key[pos[m]]);
+      const double Mr = a.M[rbase + r];
+      double term = 0.0;
+      if (Mr != -INFINITY) {
+        const int kc = j * KB + kgrp;
+        const bool vis = kc <= r && ((a.kvalid[(krow0 + kc) >> 5] >> ((krow0 + kc) & 31)) & 1u);
+        const uint16_t* qr = qbase + static_cast<int64_t>(r) * HD + sub * SL;
+        // keys past the row (or past the request) are not read: their lanes use the query row
+        const uint16_t* kr = vis ? a.ks + (krow0 + kc) * HD + sub * SL : qr;
+        // two interleaved partial sums: rounding depth SL/2 + 1 + log2(LPK) stays within e_r
+        float p0 = 0.0f, p1 = 0.0f;
+#pragma unroll 1
+        for (int e = 0; e < SL; e += 8) {
+          float qv[8], kv[8];
+          load8_bf16(qr + e, qv);
+          load8_bf16(kr + e, kv);
+#pragma unroll
+          for (int i = 0; i < 8; i += 2) {
+            p0 = fmaf(qv[i], kv[i], p0);
+            p1 = fmaf(qv[i + 1], kv[i + 1], p1);
+          }
+        }
+        float part = p0 + p1;
+#pragma unroll
+        for (int o = LPK / 2; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        const float x = vis ? part * sc : -INFINITY;
+        float mx = x;
+#pragma unroll
+        for (int o = LPK; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (mx != -INFINITY) {
+          // candidates: keys whose fp32 logit is within 2 e_r of the row's block maximum; each
+          // candidate's float64 logit is taken by the whole warp (four elements per lane)
+          const bool cand = vis && x >= mx - 2.0f * a.err[rbase + r];
+          uint32_t cmask = __ballot_sync(0xffffffffu, cand && sub == 0);
+          double dv = -INFINITY;
+          const uint16_t* qrow = qbase + static_cast<int64_t>(r) * HD;
+          float qf[HD / 32];
+#pragma unroll
+          for (int e = 0; e < HD / 32; ++e) qf[e] = bf16_to_f32(qrow[lane * (HD / 32) + e]);
+          while (cmask) {
+            const int g = (__ffs(cmask) - 1) / LPK;   // key group of the candidate
+            cmask &= cmask - 1;
+            const uint16_t* krow = a.ks + (krow0 + j * KB + g) * HD;
+            float kf[HD / 32];
+#pragma unroll
+            for (int e = 0; e < HD / 32; ++e) kf[e] = bf16_to_f32(krow[lane * (HD / 32) + e]);
+            dv = fmax(dv, warp_dot3<HD / 32>(qf, kf) * a.sm_scale);   // float64 accuracy, FP32 pipe
+          }
+          term = dv - Mr;   // exponent; exp is taken below, one item per thread
+        } else {
+          term = -INFINITY;
+        }
+      } else {
+        term = -INFINITY;
+      }
+      if (lane == 0) terms[item] = term;
+    }
+    __syncthreads();
+    for (int item = tid; item < nm * nrows; item += blockDim.x) terms[item] = exp(terms[item]);
+    __syncthreads();
+    for (int m = tid; m < nm; m += blockDim.x) {
+      double sum = 0.0;
+      for (int rr = 0; rr < nrows; ++rr) sum += terms[m * nrows + rr];
+      val[base + m] = sum;
+    }
+    __syncthreads();
+  }
+}
+
+// The same exact scores for the positions [x0, x1) at once (the top-p length's exact path, which can
+// need a whole row): a warp per position and every (sampled row, key) pair of its block in the warp,
+// lane = (row q = lane / L, keys sub, sub + L, ...) with L = 32 / KB lanes per row.  fp32 dots with
+// eight partial sums (rounding depth HD / 8 + 3 <= 19, within e_r), the row's maximum across its L
+// lanes, the keys within 2 e_r of it summed as three fp32 terms by their own lanes (float64
+// accuracy), rows summed in ascending order.  qrows: the query block's sampled rows, bf16, staged in
+// shared memory by the caller.  Ends with the block synchronised.
+template <int HD, int KB>
+__device__ void exact_scores_bulk(const KapArgs& a, const unsigned long long* key, int x0, int x1, double* val,
+                                  const uint16_t* qrows, uint16_t* slab, int b, int kvh, int r0, int r1, int R,
+                                  int64_t rbase) {
+  constexpr int L = 32 / KB;                     // lanes per sampled row
+  constexpr int KPL = (KB + L - 1) / L;          // keys per lane
+  constexpr int CH = HD / 8;                     // 16-byte chunks per key row
+  static_assert(KB <= 16 && HD + 8 <= kBulkRowPitch, "the slab holds 16 keys of d = 128");
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, warps = blockDim.x >> 5;
+  uint16_t* kb_s = slab + static_cast<size_t>(w) * 16 * kBulkRowPitch;
+  const int q = lane / L, sub = lane % L;
+  const int r = r0 + q;
+  const bool row_ok = r < r1;
+  const double Mr = row_ok ? a.M[rbase + r] : -INFINITY;
+  const float er = row_ok ? a.err[rbase + r] : 0.0f;
+  const int rp = (R + kRowTile - 1) / kRowTile * kRowTile;
+  const int64_t krow0 = a.ks_off[b] + static_cast<int64_t>(kvh) * rp;
+  const uint16_t* qrow = qrows + q * HD;
+  const float sc = static_cast<float>(a.sm_scale);
+  for (int x = x0 + w; x < x1; x += warps) {
+    const int j = key_block(key[x]);
+    // the block's KB key rows (contiguous in the gathered keys; padding rows past the request are
+    // loaded but never used), one coalesced pass of the warp
+    __syncwarp();
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(a.ks + (krow0 + static_cast<int64_t>(j) * KB) * HD);
+#pragma unroll
+      for (int e = lane; e < KB * CH; e += 32)
+        *reinterpret_cast<uint4*>(kb_s + (e / CH) * kBulkRowPitch + (e % CH) * 8) = src[e];
+    }
+    __syncwarp();
+    float lg[KPL];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int t = 0; t < KPL; ++t) {
+      const int kk = sub + L * t, kc = j * KB + kk;
+      const bool vis = row_ok && kk < KB && kc <= r && ((a.kvalid[(krow0 + kc) >> 5] >> ((krow0 + kc) & 31)) & 1u);
+      lg[t] = -INFINITY;
+      if (vis) {
+        const uint16_t* krow = kb_s + kk * kBulkRowPitch;
+        float acc[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 4
+        for (int e = 0; e < HD; e += 8) {
+          float qv[8], kv[8];
+          load8_bf16(qrow + e, qv);
+          load8_bf16(krow + e, kv);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] = fmaf(qv[i], kv[i], acc[i]);
+        }
+        lg[t] = (((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]))) * sc;
+        mx = fmaxf(mx, lg[t]);
+      }
+    }
+#pragma unroll
+    for (int o = 1; o < L; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    double dv = -INFINITY;
+#pragma unroll
+    for (int t = 0; t < KPL; ++t) {
+      if (lg[t] != -INFINITY && lg[t] >= mx - 2.0f * er) {
+        const uint16_t* krow = kb_s + (sub + L * t) * kBulkRowPitch;
+        float hi = 0.0f, lo = 0.0f, cc = 0.0f;
+#pragma unroll 2
+        for (int e = 0; e < HD; e += 8) {
+          float qv[8], kv[8];
+          load8_bf16(qrow + e, qv);
+          load8_bf16(krow + e, kv);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) sum3_add(hi, lo, cc, __fmul_rn(qv[i], kv[i]));
+        }
+        const double d = (static_cast<double>(hi) + static_cast<double>(lo)) + static_cast<double>(cc);
+        dv = fmax(dv, d * a.sm_scale);
+      }
+    }
+#pragma unroll
+    for (int o = 1; o < L; o <<= 1) dv = fmax(dv, __shfl_xor_sync(0xffffffffu, dv, o));
+    double term = 0.0;
+    if (sub == 0 && Mr != -INFINITY && dv != -INFINITY) term = exp(dv - Mr);
+    double sum = 0.0;
+#pragma unroll
+    for (int qq = 0; qq < KB; ++qq) {
+      const double tq = __shfl_sync(0xffffffffu, term, qq * L);
+      if (r0 + qq < r1) sum += tq;
+    }
+    if (lane == 0) val[x] = sum;
+  }
+  __syncthreads();
 }
 
 // Selection of mask row `row` by the whole block (the rows kap_select_warp_kernel leaves).
@@ -1067,7 +1331,8 @@ __device__ void kap_select_row(const KapArgs& a, int cap, int row) {
       (reinterpret_cast<uintptr_t>(hrm + 2 * cap) + 15) & ~uintptr_t(15));     // [kRepChunk * KB] row terms
   uint8_t* cutf = hrm + cap;                                                   // [cap] certain-cut flags
   __shared__ int32_t n_rep_s, n_hrm_s, cstar_s[2], warp_cnt_s[kSelectThreads / 32], sentinel_marked_s, topk_s;
-  __shared__ double warp_sum_s[kSelectThreads / 32];
+  __shared__ int32_t krange_s[2], klo_s;
+  __shared__ double warp_sum_s[kSelectThreads / 32], warp_sum2_s[kSelectThreads / 32];
   __shared__ TopkShared topk;
 
   const int tid = threadIdx.x;
@@ -1125,6 +1390,7 @@ __device__ void kap_select_row(const KapArgs& a, int cap, int row) {
   // certified against the sentinel, the full path runs instead.
   int Jl = J, nh = nh_all, n2 = 1, Nl = kSelectThreads;
   bool sentinel = false;
+  bool topp_exact = false;   // the top-p length is not certified by the bounds: exact scores below
   float sentinel_hi = -INFINITY;
   for (int attempt = (!a.top_p && K <= kTopFast && K < J) ? 0 : 1; attempt < 2; ++attempt) {
     int N2 = 1;
@@ -1151,7 +1417,13 @@ __device__ void kap_select_row(const KapArgs& a, int cap, int row) {
         case 8: sort_block_keys<8>(key, hrm, sc, J, N); break;
         default: sort_block_keys<16>(key, hrm, sc, J, N); break;
       }
-      if (a.top_p) K = top_p_count(key, sc, J, a.budget_ppm, warp_sum_s, topk_s);
+      if (a.top_p) {
+        // a certified length, or every position's exact score decides it below
+        const int2 kr = top_p_range(key, sc, se, J, a.budget_ppm, warp_sum_s, warp_sum2_s, krange_s);
+        K = kr.y;
+        topp_exact = kr.x != kr.y;
+        if (tid == 0) klo_s = kr.x;
+      }
       sentinel = false;
       Jl = J;
       nh = nh_all;
@@ -1268,88 +1540,7 @@ __device__ void kap_select_row(const KapArgs& a, int cap, int row) {
   __syncthreads();
   const int n_rep = n_rep_s;
   if (n_rep > 0) {
-    // exact scores s_ij = sum over rows r (ascending) of exp(bm[r,j] - M_r) with float64 logits.
-    // Warp per (position, row); lane group kgrp holds key j*KB + kgrp, its LPK lanes split d.
-    constexpr int LPK = 32 / KB;
-    constexpr int SL = HD / LPK;
-    const int warps = blockDim.x / 32, w = tid >> 5, lane = tid & 31;
-    const int kgrp = lane / LPK, sub = lane % LPK;
-    const int nrows = r1 - r0;
-    const int rp = (ri.R + kRowTile - 1) / kRowTile * kRowTile;
-    const uint16_t* qbase = a.qs + (a.qs_off[b] + static_cast<int64_t>(h) * rp) * HD;
-    const int64_t krow0 = a.ks_off[b] + static_cast<int64_t>(kvh) * rp;
-    const float sc = static_cast<float>(a.sm_scale);
-    for (int base = 0; base < n_rep; base += kRepChunk) {
-      const int nm = min(kRepChunk, n_rep - base);
-      for (int item = w; item < nm * nrows; item += warps) {
-        const int m = base + item / nrows, r = r0 + item % nrows;
-        const int j = key_block(key[rep_pos[m]]);
-        const double Mr = a.M[rbase + r];
-        double term = 0.0;
-        if (Mr != -INFINITY) {
-          const int kc = j * KB + kgrp;
-          const bool vis = kc <= r && ((a.kvalid[(krow0 + kc) >> 5] >> ((krow0 + kc) & 31)) & 1u);
-          const uint16_t* qr = qbase + static_cast<int64_t>(r) * HD + sub * SL;
-          // keys past the row (or past the request) are not read: their lanes use the query row
-          const uint16_t* kr = vis ? a.ks + (krow0 + kc) * HD + sub * SL : qr;
-          // two interleaved partial sums: rounding depth SL/2 + 1 + log2(LPK) stays within e_r
-          float p0 = 0.0f, p1 = 0.0f;
-#pragma unroll 1
-          for (int e = 0; e < SL; e += 8) {
-            float qv[8], kv[8];
-            load8_bf16(qr + e, qv);
-            load8_bf16(kr + e, kv);
-#pragma unroll
-            for (int i = 0; i < 8; i += 2) {
-              p0 = fmaf(qv[i], kv[i], p0);
-              p1 = fmaf(qv[i + 1], kv[i + 1], p1);
-            }
-          }
-          float part = p0 + p1;
-#pragma unroll
-          for (int o = LPK / 2; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-          const float x = vis ? part * sc : -INFINITY;
-          float mx = x;
-#pragma unroll
-          for (int o = LPK; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-          if (mx != -INFINITY) {
-            // candidates: keys whose fp32 logit is within 2 e_r of the row's block maximum; each
-            // candidate's float64 logit is taken by the whole warp (four elements per lane)
-            const bool cand = vis && x >= mx - 2.0f * a.err[rbase + r];
-            uint32_t cmask = __ballot_sync(0xffffffffu, cand && sub == 0);
-            double dv = -INFINITY;
-            const uint16_t* qrow = qbase + static_cast<int64_t>(r) * HD;
-            float qf[HD / 32];
-#pragma unroll
-            for (int e = 0; e < HD / 32; ++e) qf[e] = bf16_to_f32(qrow[lane * (HD / 32) + e]);
-            while (cmask) {
-              const int g = (__ffs(cmask) - 1) / LPK;   // key group of the candidate
-              cmask &= cmask - 1;
-              const uint16_t* krow = a.ks + (krow0 + j * KB + g) * HD;
-              float kf[HD / 32];
-#pragma unroll
-              for (int e = 0; e < HD / 32; ++e) kf[e] = bf16_to_f32(krow[lane * (HD / 32) + e]);
-              dv = fmax(dv, warp_dot3<HD / 32>(qf, kf) * a.sm_scale);   // float64 accuracy, FP32 pipe
-            }
-            term = dv - Mr;   // exponent; exp is taken below, one item per thread
-          } else {
-            term = -INFINITY;
-          }
-        } else {
-          term = -INFINITY;
-        }
-        if (lane == 0) terms[item] = term;
-      }
-      __syncthreads();
-      for (int item = tid; item < nm * nrows; item += blockDim.x) terms[item] = exp(terms[item]);
-      __syncthreads();
-      for (int m = tid; m < nm; m += blockDim.x) {
-        double sum = 0.0;
-        for (int rr = 0; rr < nrows; ++rr) sum += terms[m * nrows + rr];
-        rep_val[base + m] = sum;
-      }
-      __syncthreads();
-    }
+    exact_scores<HD, KB>(a, key, rep_pos, n_rep, rep_val, terms, b, h, kvh, r0, r1, ri.R, rbase);
     // re-sort the repaired runs by (exact score desc, block asc); a run never crosses the
     // HRM / rest boundary
     if (tid == 0) {
@@ -1376,6 +1567,91 @@ __device__ void kap_select_row(const KapArgs& a, int cap, int row) {
         m0 = m1 + 1;
       }
     }
+    __syncthreads();
+  }
+  if (topp_exact) {
+    // The score bounds leave the top-p length between klo and K (= the upper end, whose cut and the
+    // order before it are certified above).  Exact scores for a prefix of the positions (which holds
+    // most of the row's mass, hence most of the bounds' width), bounds for the rest: f(k) is then known
+    // to within p times the rest's width.  While that leaves the sign of f open somewhere in
+    // [klo, K], the exact prefix grows (K + 16 positions, then four times as many, then the row);
+    // with the whole row exact, the length is the oracle's: exact scores summed in order.
+    // the query block's sampled rows, bf16, in the (here unused) repair term buffer; the key slabs after it
+    uint16_t* qrows = reinterpret_cast<uint16_t*>(terms);
+    uint16_t* slab = reinterpret_cast<uint16_t*>(terms + kRepChunk * 16);
+    {
+      const int rp = (ri.R + kRowTile - 1) / kRowTile * kRowTile;
+      const uint4* src = reinterpret_cast<const uint4*>(a.qs + (a.qs_off[b] + static_cast<int64_t>(h) * rp +
+                                                                static_cast<int64_t>(r0)) * HD);
+      for (int e = tid; e < (r1 - r0) * HD / 8; e += blockDim.x) reinterpret_cast<uint4*>(qrows)[e] = src[e];
+    }
+    __syncthreads();
+    const double p = static_cast<double>(a.budget_ppm) / 1e6;
+    int done = 0;   // exact scores of positions [0, done)
+    int want = min(J, K + 16);
+    while (true) {
+      exact_scores_bulk<HD, KB>(a, key, done, want, rep_val, qrows, slab, b, kvh, r0, r1, ri.R, rbase);
+      done = want;
+      double tlo = 0.0, thi = 0.0;
+      for (int x = done + tid; x < J; x += blockDim.x) {
+        const int j = key_block(key[x]);
+        const float sv = fmaxf(sc[j], 0.0f);
+        tlo += static_cast<double>(fmaxf(sv - se[j], 0.0f));
+        thi += static_cast<double>(sv) + static_cast<double>(se[j]);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        tlo += __shfl_xor_sync(0xffffffffu, tlo, o);
+        thi += __shfl_xor_sync(0xffffffffu, thi, o);
+      }
+      if ((tid & 31) == 0) {
+        warp_sum_s[tid >> 5] = tlo;
+        warp_sum2_s[tid >> 5] = thi;
+      }
+      __syncthreads();
+      if (tid == 0) {
+        if (done == J) {
+          // every score exact: summed in order, as the scores of Eq. (11) are summed for the cut
+          double tot = 0.0;
+          for (int x = 0; x < J; ++x) tot += rep_val[x];
+          const double thr = p * tot;
+          double run = 0.0;
+          int k = J;
+          for (int x = 0; x < J; ++x) {
+            run += rep_val[x];
+            if (run >= thr) {
+              k = x + 1;
+              break;
+            }
+          }
+          topk_s = k < K ? k : K;
+        } else {
+          double TLo = 0.0, THi = 0.0, pre = 0.0;
+          for (int q = 0; q < kSelectThreads / 32; ++q) {
+            TLo += warp_sum_s[q];
+            THi += warp_sum2_s[q];
+          }
+          for (int x = 0; x < done; ++x) pre += rep_val[x];
+          const double eps = 1e-12 * (pre + THi);
+          int kstar = -1;
+          double E = 0.0;
+          for (int x = 0; x < klo_s - 1; ++x) E += rep_val[x];
+          for (int k = klo_s; k <= K; ++k) {
+            E += rep_val[k - 1];                        // sum of the first k exact scores
+            const double Rp = pre - E;                   // exact scores of positions [k, done)
+            if ((1.0 - p) * E - p * (Rp + TLo) < -eps) continue;   // f(k) < 0 for sure
+            if ((1.0 - p) * E - p * (Rp + THi) >= eps) kstar = k;  // f(k) >= 0 for sure
+            break;
+          }
+          topk_s = kstar;
+        }
+      }
+      __syncthreads();
+      if (topk_s >= 0) break;
+      want = (done * 4 < J) ? done * 4 : J;
+      __syncthreads();
+    }
+    K = topk_s;
     __syncthreads();
   }
   if (a.ascending) {

@@ -72,6 +72,7 @@ struct alignas(1024) UnionSmem {
   KInfo stage[2][32];           // the producer's kept entries of each head, in mask order
   uint32_t tmem_base;
   int32_t abort_flag;
+  alignas(4) uint8_t stopf[2][2][4];   // [head][visit & 1][softmax warp]: 0 go on, 1 stop, 2 a wait ran out
   uint32_t seen[2][kMaxBlocksPerReq / 32];
 };
 
@@ -461,10 +462,14 @@ __global__ void __launch_bounds__(kUThreads, 1)
           const bool w1 = (p1 != -INFINITY) && (p1 - fmaxf(m_run, p1) >= tau2);
           want = row_valid && (w0 || w1);
         }
+        // each warp's stop code goes to shared memory before the vote and is read after it: one
+        // barrier decides the visit (compute, skip, end of the item, or a wait ran out)
         const bool stop = !okw || (ki_blk < 0);
+        if (lane == 0) sm.stopf[X][vx & 1][warp & 3] = stop ? (okw ? 1 : 2) : 0;
         const bool compute = named_bar_red_or(bar_vote, 128, want || stop);
-        if (compute && named_bar_red_or(bar_stop, 128, stop)) {
-          if (named_bar_red_or(bar_vote, 128, !okw)) ok = false;
+        const uint32_t stops = compute ? *reinterpret_cast<const volatile uint32_t*>(&sm.stopf[X][vx & 1][0]) : 0u;
+        if (stops != 0) {
+          if (stops & 0x02020202u) ok = false;
           // the end of the item releases S_X for the next item's first product
           if (ok && leader) mbar_arrive(&sm.s_free[X]);
           ++vx;

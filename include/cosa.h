@@ -91,8 +91,9 @@ extern "C" {
 /* Stage-1 budget by top-p (cosa_proxy_select; the paper's Sec. 5.1 and App. D.1 use p = 0.95): budget_ppm
    holds p in parts per million and K_i is the length of the shortest prefix of rho_i (Eq. (13)) whose
    block scores s_ij (Eq. (11)) sum to at least p times the sum over all causal candidates j <= i.  The
-   cut is taken on the kernel's fp32 scores (summed in float64); mask_pitch must be >= ceil(max_seqlen /
-   block_size), since K_i can reach i + 1. */
+   length is certified from the error bounds of the fp32 scores; where those bounds leave it open, it is
+   taken from scores of every candidate evaluated at float64 accuracy.  mask_pitch must be >=
+   ceil(max_seqlen / block_size), since K_i can reach i + 1. */
 #define COSA_FLAG_TOP_P 8
 /* GQA page union (cosa_sparse_prefill; ignored by cosa_proxy_select).  PageWeaver notes, Sec. 2.2: the
    query heads of a kv group select largely the same pages, so one K load can serve several of them
@@ -156,12 +157,11 @@ const char* cosa_status_string(int status);
  *              its content on entry does not matter and is undefined on exit.
  *
  * Selections are exact: the fp32 tensor-core scores carry error bounds, and every
- * order or cut they cannot certify is settled with logits at float64 accuracy or
- * better, so the mask equals the one computed from exact real-number scores except
- * where two scores agree to within float64 rounding.  The top-p length is the
- * exception: it is decided on the fp32 scores, so it can differ from the exact one
- * where the prefix mass is within the scores' error of p times the total.  Stride
- * sampling keeps token positions 0, s, 2s, ...; ties in score go to the lower block ID.
+ * order or cut (fraction or top-p) they cannot certify is settled with logits at
+ * float64 accuracy or better, so the mask equals the one computed from exact
+ * real-number scores except where two scores, or a prefix mass and p times the total,
+ * agree to within float64 rounding.  Stride sampling keeps token positions 0, s, 2s,
+ * ...; ties in score go to the lower block ID.
  */
 /* Bytes of workspace cosa_proxy_select needs for `p`; 0 if cosa_proxy_select would refuse `p`. */
 size_t cosa_proxy_workspace_size(const cosa_params* p);

@@ -11,6 +11,13 @@ adversarial rows and compares every fp32 logit with the exact float64 dot produc
 
     worst |err| / (||q|| ||k||)       <= kappa / 2    (half the certified bound: margin for luck)
     worst |err| / sum_i |q_i k_i|     <= 48 * 2^-24   (the accumulation model itself)
+
+The block scores (Eqs. (9)-(11)) take each exp(bm - M_r) with the hardware base-2 exponential
+(ex2.approx.ftz.f32) and bound its relative error by EX2_REL; a second probe
+(tests/probes/ex2_error_probe.cu) measures that instruction's largest relative error over every fp32
+input whose result is a normal number (2^-126 .. 2^0.05), against the float64 exp2:
+
+    worst relative error of ex2.approx <= EX2_REL / 2
 """
 import ctypes
 import os
@@ -31,22 +38,29 @@ PROBE_SRC = os.path.join(ROOT, "tests", "probes", "umma_logits_probe.cu")
 PROBE_LIB = os.path.join(ROOT, "tests", "probes", "_build", "umma_logits_probe.so")
 KAPPA = 2.0 ** -18
 MODEL = 48 * 2.0 ** -24
+EX2_REL = 2.0 ** -21              # kEx2Rel in kap.cu
+EX2_SRC = os.path.join(ROOT, "tests", "probes", "ex2_error_probe.cu")
+EX2_LIB = os.path.join(ROOT, "tests", "probes", "_build", "ex2_error_probe.so")
 ROWS = 384                        # 3 x 3 tiles of 128 x 128 per case
 
 
-def build_probe() -> str:
-    srcs = [PROBE_SRC, os.path.join(ROOT, "block_sparse_long_gb300", "csrc", "ptx.cuh")]
-    if os.path.exists(PROBE_LIB) and all(os.path.getmtime(s) <= os.path.getmtime(PROBE_LIB) for s in srcs):
-        return PROBE_LIB
-    os.makedirs(os.path.dirname(PROBE_LIB), exist_ok=True)
+def build_probe(src: str = PROBE_SRC, lib: str = PROBE_LIB) -> str:
+    srcs = [src, os.path.join(ROOT, "block_sparse_long_gb300", "csrc", "ptx.cuh")]
+    if os.path.exists(lib) and all(os.path.getmtime(s) <= os.path.getmtime(lib) for s in srcs):
+        return lib
+    os.makedirs(os.path.dirname(lib), exist_ok=True)
     nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
     cmd = [nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O2", "-std=c++17", "-Xcompiler", "-fPIC",
            "-shared", "-cudart", "static", "-I", os.path.join(ROOT, "block_sparse_long_gb300", "csrc"),
-           PROBE_SRC, "-o", PROBE_LIB + ".tmp"]
+           src, "-o", lib + ".tmp"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     assert r.returncode == 0, r.stdout + r.stderr
-    os.replace(PROBE_LIB + ".tmp", PROBE_LIB)
-    return PROBE_LIB
+    os.replace(lib + ".tmp", lib)
+    return lib
+
+
+def build_ex2_probe() -> str:
+    return build_probe(EX2_SRC, EX2_LIB)
 
 
 def _bf16(x):
@@ -113,3 +127,25 @@ def test_tensor_core_logit_error_within_kappa(kind, d):
     gh.record("kappa", "tensor-core logits", case=f"{kind} d={d}", logits=int(err.size), r_norm=r_norm, r_abs=r_abs)
     assert r_norm <= KAPPA / 2, (kind, d, r_norm / 2.0 ** -24)
     assert r_abs <= MODEL, (kind, d, r_abs / 2.0 ** -24)
+
+
+def test_ex2_approx_error_within_kap_assumption():
+    """Every fp32 input of ex2.approx.ftz.f32 with a normal result: the exponents the block scores
+    take lie in [-126, 0] up to their error bound (block maxima never exceed the row maximum by more)."""
+    lib = ctypes.CDLL(build_ex2_probe())
+    lib.ex2_error_probe.restype = ctypes.c_int
+    lib.ex2_error_probe.argtypes = [ctypes.c_uint32, ctypes.c_uint32, ctypes.c_void_p, ctypes.c_void_p]
+    dev = torch.device("cuda")
+    worst, arg = 0.0, 0.0
+    # [-126, -0] and [+0, 0.05]
+    for lo, hi in ((0x80000000, 0xC2FC0000), (0x00000000, 0x3D4CCCCD)):
+        out = torch.zeros(2, dtype=torch.int64, device=dev)
+        rc = lib.ex2_error_probe(lo, hi, out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+        assert rc == 0, rc
+        torch.cuda.synchronize()
+        o = out.cpu().numpy()
+        rel = float(o[:1].view(np.float64)[0])
+        if rel > worst:
+            worst, arg = rel, float(np.array([o[1]], np.uint32).view(np.float32)[0])
+    gh.record("ex2", "tensor-core logits", inputs=int(0xC2FC0000 - 0x80000000 + 0x3D4CCCCD + 2), rel=worst, arg=arg)
+    assert 0.0 < worst <= EX2_REL / 2, (worst / 2.0 ** -24, arg)

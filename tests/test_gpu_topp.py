@@ -1,8 +1,8 @@
 """Top-p stage-1 budget (COSA_FLAG_TOP_P) on the GPU against the float64 oracle: K_i is the shortest
 prefix of rho_i (Eq. (13)) whose block scores (Eq. (11)) reach p of the row's total (CoSA Sec. 4.2,
-Sec. 5.1 and App. D.1, p = 0.95).  The order is exact as for the fraction rule; the cut is taken on the
-kernel's fp32 scores and may differ from the oracle's only where the prefix mass is within 1e-3 of
-the total from p times the total."""
+Sec. 5.1 and App. D.1, p = 0.95).  The order is exact as for the fraction rule, and so is the cut: the
+kernel certifies it from the scores' error bounds, or takes it from exact scores of every candidate when
+the bounds straddle p times the total; a length may differ from the oracle's only at a float64 tie."""
 import json
 import os
 
@@ -40,13 +40,13 @@ def _run(w, ppm, delta=-1.0, items=None):
 
 
 @pytest.mark.parametrize("name", sorted(SMALL))
-@pytest.mark.parametrize("ppm", [500_000, 950_000])
+@pytest.mark.parametrize("ppm", [500_000, 950_000, 990_000])
 def test_top_p_small(name, ppm):
     if SMALL[name]["block_size"] // SMALL[name]["stride"] not in (4, 8, 16):
         pytest.skip("stride ratio not supported")
     w = synth.make_workload(small_spec(name, seed=600 + len(name)))
     _, _, _, mask_g, len_g, rows, cuts = _run(w, ppm)
-    assert len(cuts) <= max(1, len(rows) // 100), cuts
+    assert len(cuts) <= max(1, len(rows) // 100), cuts    # float64 ties only
     sp = w.spec
     for b, L in enumerate(sp.lengths):
         nqb = -(-L // sp.block_size)
@@ -73,3 +73,20 @@ def test_top_p_full_pipeline_32k():
     rep = gh.compare_osk(w, prm, mask_o, len_g, out, flags, exact)
     gh.assert_osk_ok(rep)
     print(f"top-p 0.95 on {sp.name}: realised stage-1 budget {frac:.3f}, cut differences {len(cuts)}")
+
+
+@pytest.mark.parametrize("ppm", [500_000, 750_000])
+def test_top_p_constant_keys_exact_path(ppm):
+    """Every key equal: every block of a row scores the same (8 sampled rows, each at its maximum), so
+    p times the total falls exactly on a prefix boundary whenever p J_i is an integer.  The fp32 bounds
+    cannot settle such a cut; the kernel takes it from exact scores of every candidate, and any length
+    that differs from the oracle's must be a float64 tie."""
+    from tests.test_gpu_osk import small_spec as ss
+    sp = ss("d128_b128_P64", seed=611)
+    w = synth.make_workload(sp)
+    w.k_cache[...] = w.k_cache[0, 0, 0, :]
+    _, _, _, mask_g, len_g, rows, cuts = _run(w, ppm)
+    for (b, h, i), r in rows.items():
+        J = i + 1
+        want = -(-ppm * J // 1_000_000)
+        assert int(len_g[b, h, i]) in (max(1, want), want + 1), ((b, h, i), int(len_g[b, h, i]), want)
