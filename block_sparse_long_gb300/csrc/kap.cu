@@ -415,8 +415,16 @@ __global__ void __launch_bounds__(kLogitsThreads, 2)
     // stored one after another
     float* bm_row = a.bm + a.bm_off[b] + static_cast<int64_t>(h) * bm_block_base(nqb, KB) + bm_block_base(qblk, KB) +
                     static_cast<int64_t>(r - qblk * KB) * bm_pitch(qblk, KB);
+    // key validity words of this thread's half of key tile kt: loaded one tile ahead, so the L2
+    // latency overlaps the wait for the tile's product instead of following it
+    uint32_t nb0 = __ldg(kval + g * 2), nb1 = __ldg(kval + g * 2 + 1);
     for (int kt = 0; kt < nkt; ++kt) {
       const int ab = kt & 1;
+      const uint32_t bits0 = nb0, bits1 = nb1;
+      if (kt + 1 < nkt) {
+        nb0 = __ldg(kval + (kt + 1) * 4 + g * 2);
+        nb1 = __ldg(kval + (kt + 1) * 4 + g * 2 + 1);
+      }
       const bool okw = __all_sync(0xffffffffu,
                                   wait_parity_bounded(&sm.acc_full[ab], (kt >> 1) & 1, abort_flag, a.status));
       if (!okw) break;
@@ -435,8 +443,6 @@ __global__ void __launch_bounds__(kLogitsThreads, 2)
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.acc_free[ab]);
       const int c0 = kt * kKeyTile + g * 64;      // key index of this thread's first column
-      const uint32_t bits0 = __ldg(kval + ((kt * kKeyTile + g * 64) >> 5));
-      const uint32_t bits1 = __ldg(kval + ((kt * kKeyTile + g * 64) >> 5) + 1);
       const int last = r - c0;                    // causal: columns <= last
       // every column of this thread's half is visible: below the diagonal tile, all keys valid
       const bool interior = row_ok && kt < rt && (bits0 & bits1) == 0xffffffffu;
