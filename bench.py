@@ -71,8 +71,9 @@ def kap_flops(spec) -> float:
 
 def osk_flops_from_flags(spec, flags: np.ndarray) -> tuple:
     tile = 2.0 * spec.block_size * spec.block_size * spec.head_dim
-    visited = int((flags != 2).sum())
-    computed = int((flags == 0).sum())
+    f = flags & 3          # the GQA page-union kernel adds a shared-load bit (4)
+    visited = int((f != 2).sum())
+    computed = int((f == 0).sum())
     return tile * (visited + computed), visited, computed
 
 
@@ -371,14 +372,16 @@ def run_cosa(args, spec, workload_name, delta):
     cu = torch.from_numpy(w.cu_seqlens).to(dev)
     pitch = C.stage1_pitch(spec.budget_ppm, spec.max_seqlen, spec.block_size)
     p = C.params_for(q, k, pt, cu, block_size=spec.block_size, max_seqlen=spec.max_seqlen, stride=spec.stride,
-                     budget_ppm=spec.budget_ppm, mask_pitch=pitch, skip_delta=delta)
+                     budget_ppm=spec.budget_ppm, mask_pitch=pitch, skip_delta=delta,
+                     flags=C.COSA_FLAG_GQA_UNION if args.gqa_union else 0)
     nqb = -(-spec.max_seqlen // spec.block_size)
     mask = torch.empty((spec.num_reqs, spec.num_q_heads, nqb, pitch), dtype=torch.int32, device=dev)
     mask_len = torch.empty((spec.num_reqs, spec.num_q_heads, nqb), dtype=torch.int32, device=dev)
     ws = torch.empty(C.cosa_proxy_workspace_size(p), dtype=torch.uint8, device=dev)
     out = torch.empty_like(q)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    flags = torch.empty((spec.num_reqs, spec.num_q_heads, nqb, pitch), dtype=torch.uint8, device=dev)
+    # entries of absent query blocks (shorter requests) are not written: IGNORED marks them
+    flags = torch.full((spec.num_reqs, spec.num_q_heads, nqb, pitch), 2, dtype=torch.uint8, device=dev)
 
     def kap():
         C.cosa_proxy_select(p, q, cu, k, pt, mask=mask, mask_len=mask_len, workspace=ws, status=status)
@@ -519,7 +522,7 @@ def run_cosa(args, spec, workload_name, delta):
     osk_avg = statistics.mean(osk_ms)
     achieved = ofl / (osk_avg * 1e-3) / 1e12
     peak = float(pk["bf16_tflops"])
-    traffic = traffic_per_launch(workload_name)
+    traffic = None if args.gqa_union else traffic_per_launch(workload_name)
     cl = clk.summary()
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -531,6 +534,7 @@ def run_cosa(args, spec, workload_name, delta):
                    "head_dim": spec.head_dim,
                    "block_size": spec.block_size, "page_size": spec.page_size, "stride": spec.stride,
                    "stage1_budget": spec.budget_ppm / 1e6, "skip_delta": delta,
+                   **({"osk_variant": "gqa_union (two query heads per K stream)"} if args.gqa_union else {}),
                    "l2": "inputs larger than L2 (q, k, v = %.2f GiB)" % ((q.numel() + k.numel() + v.numel()) * 2 / 2**30),
                    "parallelism": (f"kv heads [{kv_range[0]}, {kv_range[1]}) of {w_full.spec.num_kv_heads} on rank 0, "
                                    f"{world} ranks" if by_heads else f"independent replicas per GPU x{world}")},
@@ -540,8 +544,10 @@ def run_cosa(args, spec, workload_name, delta):
         "visits": visited, "computed": computed, "realized_stage1": visited / causal,
         "realized_stage2": computed / causal,
         "roofline": {"bound": "tensor",
-                     "kernel": f"osk_kernel<{spec.block_size},{spec.head_dim},{spec.page_size},false,"
-                               f"{'true' if delta > 0 else 'false'},false>",
+                     "kernel": (f"osk_union_kernel<{spec.head_dim},{spec.page_size},"
+                                f"{'true' if delta > 0 else 'false'},false>" if args.gqa_union else
+                                f"osk_kernel<{spec.block_size},{spec.head_dim},{spec.page_size},false,"
+                                f"{'true' if delta > 0 else 'false'},false>"),
                      "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"bf16_tflops ({pk_src}, burst)"},
@@ -886,6 +892,9 @@ def main():
                          "for profiling); not a bench line of the whole workload")
     ap.add_argument("--gather-out", action="store_true",
                     help="with --shard heads: all-gather O over heads after the timed region (reported apart)")
+    ap.add_argument("--gqa-union", action="store_true",
+                    help="run the OSK as the GQA page-union kernel (COSA_FLAG_GQA_UNION: two query heads of a kv "
+                         "group share one K stream); a measurement of that variant, not the bench line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--clocks-log", default=None, help="also write the raw nvidia-smi clock samples here")
     ap.add_argument("--sweep", action="store_true",
