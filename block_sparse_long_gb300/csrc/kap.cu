@@ -280,6 +280,7 @@ __global__ void __launch_bounds__(256) kap_gather_kernel(KapArgs a) {
 // sampled logits on tcgen05: 128 sampled rows x all causal sampled keys
 // ---------------------------------------------------------------------------
 constexpr int kKeyStages = 2;           // K~ tiles in flight (two CTAs fit per SM)
+constexpr int kMaxKeyTiles = 512;       // key tiles of the longest request: 4096 query blocks of 16 sampled rows
 constexpr int kLogitsThreads = 320;      // warp 0 TMA, warp 1 UMMA, warps 2-9 epilogue
 
 template <int HD>
@@ -292,6 +293,7 @@ struct alignas(1024) KapTileSmem {
   uint64_t cleanup;
   float hv1[2][128], hv2[2][128];        // per column half: the row's largest and second largest logit
   int32_t hc1[2][128];
+  uint32_t kval[kMaxKeyTiles * 4];       // validity bits of the row tile's causal keys (4 words per key tile)
   uint32_t tmem_base;
   int32_t abort_flag;
 };
@@ -415,16 +417,12 @@ __global__ void __launch_bounds__(kLogitsThreads, 2)
     // stored one after another
     float* bm_row = a.bm + a.bm_off[b] + static_cast<int64_t>(h) * bm_block_base(nqb, KB) + bm_block_base(qblk, KB) +
                     static_cast<int64_t>(r - qblk * KB) * bm_pitch(qblk, KB);
-    // key validity words of this thread's half of key tile kt: loaded one tile ahead, so the L2
-    // latency overlaps the wait for the tile's product instead of following it
-    uint32_t nb0 = __ldg(kval + g * 2), nb1 = __ldg(kval + g * 2 + 1);
+    // the validity words of every causal key tile, staged once: their loads stay off the per-tile path
+    for (int e = threadIdx.x - 64; e < nkt * 4; e += 256) sm.kval[e] = __ldg(kval + e);
+    named_bar_sync(2, 256);
     for (int kt = 0; kt < nkt; ++kt) {
       const int ab = kt & 1;
-      const uint32_t bits0 = nb0, bits1 = nb1;
-      if (kt + 1 < nkt) {
-        nb0 = __ldg(kval + (kt + 1) * 4 + g * 2);
-        nb1 = __ldg(kval + (kt + 1) * 4 + g * 2 + 1);
-      }
+      const uint32_t bits0 = sm.kval[kt * 4 + g * 2], bits1 = sm.kval[kt * 4 + g * 2 + 1];
       const bool okw = __all_sync(0xffffffffu,
                                   wait_parity_bounded(&sm.acc_full[ab], (kt >> 1) & 1, abort_flag, a.status));
       if (!okw) break;
