@@ -123,14 +123,12 @@ __device__ __forceinline__ ReqInfo req_info(const KapArgs& a, int b) {
   return r;
 }
 
-// Block maxima layout: per (request, head), query block i holds its kb sampled rows one after
-// another, each padded to bm_pitch(i) = (i + 1) rounded up to 64 / kb floats, so that a thread of the
-// logits epilogue stores the 64 / kb block maxima of its columns as aligned 16-byte vectors.
-__host__ __device__ __forceinline__ int64_t bm_pitch(int i, int kb) {
-  const int ng = 64 / kb;
-  return (static_cast<int64_t>(i) + ng) / ng * ng;
-}
-// floats before query block i (sum over i' < i of kb * bm_pitch(i'))
+// Block maxima layout: per (request, head), query block i holds (i + 1) rounded up to 64 / kb key
+// blocks (its pitch), each as the kb maxima of its sampled rows in row order: the maximum of key
+// block j for row q of the query block is element j * kb + q.  The kb lanes of the logits epilogue
+// that hold a query block's rows then store each key block's maxima as kb consecutive floats, and
+// the block-score kernel reads them as one vector per key block.
+// floats before query block i (sum over i' < i of kb times the pitch of i')
 __host__ __device__ __forceinline__ int64_t bm_block_base(int i, int kb) {
   const int64_t ng = 64 / kb;
   const int64_t full = i / ng;                   // complete groups of ng query blocks
@@ -413,10 +411,9 @@ __global__ void __launch_bounds__(kLogitsThreads, 2)
     int rc1 = -1;
     const int nqb = ri.nqb;
     const int qblk = r / KB;
-    // this row's block maxima: blocks 0 .. qblk of its (request, head), rows of a query block
-    // stored one after another
+    // this row's block maxima: element j * KB + (r - qblk * KB) of its query block's region
     float* bm_row = a.bm + a.bm_off[b] + static_cast<int64_t>(h) * bm_block_base(nqb, KB) + bm_block_base(qblk, KB) +
-                    static_cast<int64_t>(r - qblk * KB) * bm_pitch(qblk, KB);
+                    (r - qblk * KB);
     // the validity words of every causal key tile, staged once: their loads stay off the per-tile path
     for (int e = threadIdx.x - 64; e < nkt * 4; e += 256) sm.kval[e] = __ldg(kval + e);
     named_bar_sync(2, 256);
@@ -483,11 +480,11 @@ __global__ void __launch_bounds__(kLogitsThreads, 2)
           r1 = fmaxf(r1, x);
         }
       }
-      // the group of NG blocks starts at a multiple of NG <= qblk, so it fits the padded row
+      // the group of NG blocks starts at a multiple of NG <= qblk, so it fits the padded region; the
+      // KB lanes of a query block write KB consecutive floats per key block (whole 32-byte sectors)
       if (row_ok && c0 / KB <= qblk) {
 #pragma unroll
-        for (int gg = 0; gg < NG; gg += 4)
-          *reinterpret_cast<float4*>(bm_row + c0 / KB + gg) = make_float4(bmg[gg], bmg[gg + 1], bmg[gg + 2], bmg[gg + 3]);
+        for (int gg = 0; gg < NG; ++gg) bm_row[static_cast<int64_t>(c0 / KB + gg) * KB] = bmg[gg];
       }
     }
     // merge the two column halves; half 0 writes the row's record
@@ -544,7 +541,6 @@ __global__ void __launch_bounds__(128) kap_block_scores_kernel(KapArgs a) {
   const float sl2 = static_cast<float>(a.sm_scale * 1.4426950408889634);
   const int64_t rbase = a.row_off[b] + static_cast<int64_t>(h) * ri.R;
   const float* bm_blk = a.bm + a.bm_off[b] + static_cast<int64_t>(h) * bm_block_base(nqb, KB) + bm_block_base(i, KB);
-  const int64_t pitch = bm_pitch(i, KB);
   const float* kbn = a.kbnorm + (static_cast<size_t>(b) * a.num_kv_heads + kvh) * a.nqb_max;
   const int64_t sbase = a.sc_off[b] + static_cast<int64_t>(h) * nqb * nqb + static_cast<int64_t>(i) * nqb;
   constexpr float kGrow = 1.0f + 1.0f / 524288.0f;   // 1 + 2^-19
@@ -585,10 +581,19 @@ __global__ void __launch_bounds__(128) kap_block_scores_kernel(KapArgs a) {
   const float C = kGrow * kRnd;
   for (int j = threadIdx.x; j <= i; j += blockDim.x) {
     const float kbv = __ldg(kbn + j);
-    // every row's block maximum is requested before any is used
+    // the key block's KB row maxima, as vectors; rows past the request's sampled rows hold nothing
     float bmv[KB];
 #pragma unroll
-    for (int q = 0; q < KB; ++q) bmv[q] = (i * KB + q < ri.R) ? __ldcs(bm_blk + q * pitch + j) : -INFINITY;
+    for (int q = 0; q < KB; q += 4) {
+      const float4 v4 = __ldcs(reinterpret_cast<const float4*>(bm_blk + static_cast<int64_t>(j) * KB + q));
+      bmv[q] = v4.x;
+      bmv[q + 1] = v4.y;
+      bmv[q + 2] = v4.z;
+      bmv[q + 3] = v4.w;
+    }
+#pragma unroll
+    for (int q = 0; q < KB; ++q)
+      if (i * KB + q >= ri.R) bmv[q] = -INFINITY;
     float x[KB];
     float xe = 0.0f;
     if (dl_max * kbv <= 0.013f && ml_max <= 1.0e5f) {
@@ -778,7 +783,7 @@ __global__ void __launch_bounds__(256) kap_rescan_kernel(KapArgs a) {
     const int rp = (ri.R + kRowTile - 1) / kRowTile * kRowTile;
     const int qblk = r / KB;
     const float* bm_row = a.bm + a.bm_off[b] + static_cast<int64_t>(h) * bm_block_base(ri.nqb, KB) +
-                          bm_block_base(qblk, KB) + static_cast<int64_t>(r - qblk * KB) * bm_pitch(qblk, KB);
+                          bm_block_base(qblk, KB) + (r - qblk * KB);   // block j at bm_row[j * KB]
     const float thr = a.v1[gw] - 3.0f * a.err[gw];
     float qf[PER];
     {
@@ -801,7 +806,7 @@ __global__ void __launch_bounds__(256) kap_rescan_kernel(KapArgs a) {
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
         const int j = g0 + c * 32 + lane;
-        const float bmj = (j <= qblk) ? bm_row[j] : -INFINITY;
+        const float bmj = (j <= qblk) ? bm_row[static_cast<int64_t>(j) * KB] : -INFINITY;
         cmk[c] = __ballot_sync(0xffffffffu, bmj != -INFINITY && bmj * sc >= thr);
       }
 #pragma unroll
@@ -841,7 +846,7 @@ __global__ void __launch_bounds__(256) kap_rescan_kernel(KapArgs a) {
     } else {
       for (int j0 = 0; j0 <= qblk; j0 += 32) {
         const int j = j0 + lane;
-        const float bmj = (j <= qblk) ? bm_row[j] : -INFINITY;
+        const float bmj = (j <= qblk) ? bm_row[static_cast<int64_t>(j) * KB] : -INFINITY;
         unsigned cm = __ballot_sync(0xffffffffu, bmj != -INFINITY && bmj * sc >= thr);
         while (cm) {
           const int jj = j0 + __ffs(cm) - 1;
@@ -2218,7 +2223,7 @@ WsLayout ws_layout(int num_reqs, int num_q_heads, int block_size, int stride, in
   w.scores = static_cast<size_t>(num_q_heads) * nqb_max * (static_cast<size_t>(total_tokens) / block_size + num_reqs);
   w.words = (nqb_max + 31) / 32;
   w.padded = static_cast<size_t>(total_tokens) / stride + static_cast<size_t>(num_reqs) * (kRowTile + 1);
-  // sum_b sum_{i < nqb_b} bm_pitch(i) <= sum_b nqb_b ((nqb_b + 1) / 2 + 16) <= (T / b + B) (nqb_max / 2 + 17)
+  // sum_b sum_{i < nqb_b} pitch(i) <= sum_b nqb_b ((nqb_b + 1) / 2 + 16) <= (T / b + B) (nqb_max / 2 + 17)
   w.bms = static_cast<size_t>(num_q_heads) * (block_size / stride) * (nqb_max / 2 + 17) *
           (static_cast<size_t>(total_tokens) / block_size + num_reqs);
   return w;
