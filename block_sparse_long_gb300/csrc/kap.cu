@@ -579,18 +579,29 @@ __global__ void __launch_bounds__(128) kap_block_scores_kernel(KapArgs a) {
     if (A[q] != 0.0f) ml_max = fmaxf(ml_max, fabsf(Ml2[q]));
   }
   const float C = kGrow * kRnd;
-  for (int j = threadIdx.x; j <= i; j += blockDim.x) {
-    const float kbv = __ldg(kbn + j);
-    // the key block's KB row maxima, as vectors; rows past the request's sampled rows hold nothing
-    float bmv[KB];
+  // a key block's KB row maxima, as vectors, and its largest key norm; the next key block's are
+  // requested before the current one is scored, so two blocks' loads are in flight per thread
+  float nbm[KB];
+  float nkb = 0.0f;
+  auto load_block = [&](int j) {
+    nkb = __ldg(kbn + j);
 #pragma unroll
     for (int q = 0; q < KB; q += 4) {
       const float4 v4 = __ldcs(reinterpret_cast<const float4*>(bm_blk + static_cast<int64_t>(j) * KB + q));
-      bmv[q] = v4.x;
-      bmv[q + 1] = v4.y;
-      bmv[q + 2] = v4.z;
-      bmv[q + 3] = v4.w;
+      nbm[q] = v4.x;
+      nbm[q + 1] = v4.y;
+      nbm[q + 2] = v4.z;
+      nbm[q + 3] = v4.w;
     }
+  };
+  if (static_cast<int>(threadIdx.x) <= i) load_block(threadIdx.x);
+  for (int j = threadIdx.x; j <= i; j += blockDim.x) {
+    const float kbv = nkb;
+    float bmv[KB];
+#pragma unroll
+    for (int q = 0; q < KB; ++q) bmv[q] = nbm[q];
+    if (j + static_cast<int>(blockDim.x) <= i) load_block(j + blockDim.x);
+    // rows past the request's sampled rows hold nothing
 #pragma unroll
     for (int q = 0; q < KB; ++q)
       if (i * KB + q >= ri.R) bmv[q] = -INFINITY;
