@@ -1731,17 +1731,54 @@ constexpr int kWarpSelMaxK = 128;
 constexpr int kWarpRepMax = 16;
 constexpr int kWarpSelWarps = 4;
 
-constexpr int kWarpCand = 64;            // float64 candidates of a row's repairs (more: block kernel)
+constexpr int kWarpCand = 64;            // float64-accuracy candidates of a row's repairs (more: block kernel)
+constexpr int kStageUnroll = 8;          // candidates a lane loads at once
 
-struct WarpSelSmem {
-  unsigned long long key[kWarpSelMaxK];   // selected keys, sorted descending
+// Shared state of one warp.  Regions whose uses do not overlap in time share storage: the candidate
+// words live until the certification, the repair's buffers after it; the radix histogram until the
+// compaction, the selected keys from it on.
+template <int HD, int KB>
+struct __align__(16) WarpSelSmem {
+  union {
+    uint32_t word[kWarpSelMaxJ];          // candidate j: HRM flag (bit 31) | fp32 bits of max(score, 0);
+                                          // from the compaction on, a selected one's error bound
+    struct {
+      float4 qrows[KB * HD / 4];          // the query block's sampled rows, widened to fp32: see q_chunk
+      double terms[kWarpRepMax * KB];     // (repaired position, sampled row): block maxima, then terms
+      uint32_t cand[kWarpCand];           // float64-accuracy candidates: (item << 16) | key
+    } rep;
+  } u;
+  union {
+    uint32_t hist[256];                   // radix select
+    unsigned long long key[kWarpSelMaxK]; // the selected keys, sorted descending
+  } v;
   double rep_val[kWarpRepMax];
-  double terms[kWarpRepMax * 16];         // (repaired position, sampled row): block maxima, then terms
-  uint32_t cand[kWarpCand];               // float64 candidates: (item << 16) | key
-  uint32_t hist[256];
   int32_t rep_pos[kWarpRepMax];
-  uint8_t hrm[kWarpSelMaxJ];
 };
+
+// Index of the four fp32 elements 4c .. 4c+3 of segment seg (of LPK segments of HD / LPK elements)
+// of sampled row rr in the repair's query rows: the same chunk of the LPK segments side by side, so
+// LPK lanes reading one chunk of their own segments hit distinct banks.
+template <int HD, int LPK>
+__device__ __forceinline__ int q_chunk(int rr, int seg, int c) {
+  return rr * (HD / 4) + c * LPK + seg;
+}
+
+// The radix key of candidate j: its word above the block index's complement, 63 bits in the order
+// of sort_key (HRM first, score descending, block ascending); sort_key moves the HRM bit to bit 63.
+__device__ __forceinline__ unsigned long long radix_key(uint32_t w, int j) {
+  return (static_cast<unsigned long long>(w) << 31) | static_cast<unsigned long long>(0x7FFFFFFF - j);
+}
+__device__ __forceinline__ unsigned long long sort_key_of_radix(unsigned long long k) {
+  return (k & ~(1ull << 62)) | ((k >> 62) << 63);
+}
+// the 8-bit digit of k whose lowest bit is bit `shift` (bits below 0 read as zero)
+__device__ __forceinline__ uint32_t radix_digit(unsigned long long k, int shift) {
+  return static_cast<uint32_t>((shift >= 0 ? (k >> shift) : (k << -shift)) & 255u);
+}
+__device__ __forceinline__ unsigned long long radix_bits(unsigned long long d, int shift) {
+  return shift >= 0 ? (d << shift) : (d >> -shift);
+}
 
 // bitonic sort (descending) of 32 * E keys held E per lane, lane l holding positions l*E .. l*E+E-1
 template <int E>
@@ -1807,9 +1844,9 @@ __device__ __forceinline__ int warp_excl_sum(int x, int lane) {
 
 template <int HD, int KB>
 __global__ void __launch_bounds__(kWarpSelWarps * 32, 8) kap_select_warp_kernel(KapArgs a) {
-  __shared__ WarpSelSmem wsm[kWarpSelWarps];
+  __shared__ WarpSelSmem<HD, KB> wsm[kWarpSelWarps];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  WarpSelSmem& sm = wsm[w];
+  WarpSelSmem<HD, KB>& sm = wsm[w];
   const long long nrow_all = static_cast<long long>(a.num_reqs) * a.num_q_heads * a.nqb_max;
   long long idx = static_cast<long long>(blockIdx.x) * kWarpSelWarps + w;
   if (idx >= nrow_all) return;
@@ -1846,45 +1883,94 @@ __global__ void __launch_bounds__(kWarpSelWarps * 32, 8) kap_select_warp_kernel(
   const float* sc = a.score + sbase;
   const float* se = a.score_err + sbase;
   const int r0 = i * a.kb, r1 = min((i + 1) * a.kb, ri.R);
+  const int nrows = r1 - r0;
   const int64_t rbase = a.row_off[b] + static_cast<int64_t>(h) * ri.R;
 
-  // HRM flags of the candidates (exact, from the float64 row maxima)
-  for (int j = lane; j < J; j += 32) sm.hrm[j] = 0;
-  __syncwarp();
-  if (lane < r1 - r0) {
-    const int r = r0 + lane;
-    const int fl = a.rflags[rbase + r];
-    if (fl & 1) {
-      const uint32_t* bits = a.hrm_bits + (rbase + r) * a.words_per_row;
-      for (int j = 0; j < J; ++j)
-        if ((bits[j >> 5] >> (j & 31)) & 1u) sm.hrm[j] = 1;
-    } else if (!(fl & 2)) {
-      sm.hrm[(a.c1[rbase + r] * a.stride) / a.block_size] = 1;
+  // Candidate words in shared memory: every score requested at once (kStageUnroll per lane in
+  // flight), with the row flags and arg maxima of the query block's sampled rows; the bits all
+  // radix keys share are gathered on the way (words and block-index complements are disjoint fields)
+  int fl = 2, cmax = 0;
+  if (lane < nrows) {
+    fl = a.rflags[rbase + r0 + lane];
+    cmax = a.c1[rbase + r0 + lane];
+  }
+  uint32_t wor = 0u, wand = 0x7FFFFFFFu, ior = 0u, iand = 0x7FFFFFFFu;
+  for (int j0 = 0; j0 < J; j0 += 32 * kStageUnroll) {
+    float sv[kStageUnroll];
+#pragma unroll
+    for (int u = 0; u < kStageUnroll; ++u) {
+      const int j = j0 + 32 * u + lane;
+      sv[u] = (j < J) ? __ldg(sc + j) : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < kStageUnroll; ++u) {
+      const int j = j0 + 32 * u + lane;
+      if (j < J) {
+        const uint32_t wd = __float_as_uint(fmaxf(sv[u], 0.0f)) & 0x7FFFFFFFu;
+        sm.u.word[j] = wd;
+        wor |= wd;
+        wand &= wd;
+        ior |= static_cast<uint32_t>(0x7FFFFFFF - j);
+        iand &= static_cast<uint32_t>(0x7FFFFFFF - j);
+      }
     }
   }
   __syncwarp();
-  // lane l owns candidates j = l, l + 32, ...; their keys are rebuilt from the scores (cached) each pass
-  auto key_of = [&](int j) { return sort_key(sm.hrm[j] != 0, fmaxf(sc[j], 0.0f), j); };
+  // HRM flags (exact, from the float64 row maxima): the blocks of the keys attaining each row's
+  // maximum; a block counts once, for the lane whose atomic sets its flag
   int nh_part = 0;
-  for (int j = lane; j < J; j += 32) nh_part += sm.hrm[j] != 0 ? 1 : 0;
+  if (fl & 1) {
+    const uint32_t* bits = a.hrm_bits + (rbase + r0 + lane) * a.words_per_row;
+    for (int q = 0; q < (J + 31) / 32; ++q) {
+      uint32_t bw = bits[q];
+      while (bw) {
+        const int j = q * 32 + __ffs(bw) - 1;
+        bw &= bw - 1;
+        if (j < J) nh_part += (atomicOr(&sm.u.word[j], 0x80000000u) >> 31) ^ 1u;
+      }
+    }
+  } else if (!(fl & 2)) {
+    nh_part += (atomicOr(&sm.u.word[(cmax * a.stride) / a.block_size], 0x80000000u) >> 31) ^ 1u;
+  }
   const int nh_all = __reduce_add_sync(0xffffffffu, nh_part);
+  __syncwarp();
+  wor = __reduce_or_sync(0xffffffffu, wor) | (nh_all > 0 ? 0x80000000u : 0u);
+  wand = __reduce_and_sync(0xffffffffu, wand) | (nh_all == J ? 0x80000000u : 0u);
+  ior = __reduce_or_sync(0xffffffffu, ior);
+  iand = __reduce_and_sync(0xffffffffu, iand);
+  const unsigned long long kor = (static_cast<unsigned long long>(wor) << 31) | ior;     // OR of every radix key
+  const unsigned long long kand = (static_cast<unsigned long long>(wand) << 31) | iand;  // AND of every radix key
+  const int top = 63 - __clzll(kor ^ kand);   // highest bit on which two keys differ (J >= 2 distinct keys)
 
-  // radix select of the K largest keys on 8-bit digits from the top
-  unsigned long long prefix = 0ull, pmask = 0ull;
+  // radix select of the K largest keys on 8-bit digits, from the highest differing bit down
+  unsigned long long pmask = (top >= 62) ? 0ull : ~((2ull << top) - 1ull);
+  unsigned long long prefix = kand & pmask;
   int krem = K;
 #pragma unroll 1
-  for (int shift = 56; shift >= 0; shift -= 8) {
-    for (int d = lane; d < 256; d += 32) sm.hist[d] = 0u;
+  for (int shift = top - 7; shift > -8; shift -= 8) {
+    for (int d = lane; d < 256; d += 32) sm.v.hist[d] = 0u;
     __syncwarp();
-    for (int j = lane; j < J; j += 32) {
-      const unsigned long long kv = key_of(j);
-      if ((kv & pmask) == prefix) atomicAdd(&sm.hist[(kv >> shift) & 255u], 1u);
+    if (shift >= 31) {
+      // digit and prefix within the words (the common case: scores differ)
+      const uint32_t pw = static_cast<uint32_t>(prefix >> 31), mw = static_cast<uint32_t>(pmask >> 31);
+      const int sw = shift - 31;
+#pragma unroll 4
+      for (int j = lane; j < J; j += 32) {
+        const uint32_t wd = sm.u.word[j];
+        if ((wd & mw) == pw) atomicAdd(&sm.v.hist[(wd >> sw) & 255u], 1u);
+      }
+    } else {
+#pragma unroll 4
+      for (int j = lane; j < J; j += 32) {
+        const unsigned long long kv = radix_key(sm.u.word[j], j);
+        if ((kv & pmask) == prefix) atomicAdd(&sm.v.hist[radix_digit(kv, shift)], 1u);
+      }
     }
     __syncwarp();
     // lane l holds digits 255 - 8l .. 248 - 8l (highest first)
     int cq[8], sum = 0;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) { cq[q] = static_cast<int>(sm.hist[255 - 8 * lane - q]); sum += cq[q]; }
+    for (int q = 0; q < 8; ++q) { cq[q] = static_cast<int>(sm.v.hist[255 - 8 * lane - q]); sum += cq[q]; }
     int run = warp_excl_sum(sum, lane);
     int dg = -1, ab = 0, ct = 0;
 #pragma unroll
@@ -1897,37 +1983,50 @@ __global__ void __launch_bounds__(kWarpSelWarps * 32, 8) kap_select_warp_kernel(
     ab = __shfl_sync(0xffffffffu, ab, src);
     ct = __shfl_sync(0xffffffffu, ct, src);
     krem -= ab;
-    prefix |= static_cast<unsigned long long>(dg) << shift;
-    pmask |= 0xFFull << shift;
+    prefix |= radix_bits(static_cast<unsigned long long>(dg), shift);
+    pmask |= radix_bits(0xFFull, shift);
     __syncwarp();
     if (ct == krem) break;   // every key with this prefix is among the K
   }
-  // compact the K winners; the largest upper bound of the unselected keys of each group
-  int cnt = 0;
+  // one pass: the K winners compacted (ballot positions), their words replaced by their error bounds
+  // (the score stays in the key), and the largest upper bound of the unselected keys of each group;
+  // the error bounds requested kStageUnroll at a time
   float hiR = -INFINITY, hiH = -INFINITY;
-  for (int j = lane; j < J; j += 32) {
-    const unsigned long long kv = key_of(j);
-    if ((kv & pmask) >= prefix) {
-      ++cnt;
-    } else {
-      const float hv = fmaxf(sc[j], 0.0f) + se[j];
-      if (kv >> 63) hiH = fmaxf(hiH, hv);
-      else hiR = fmaxf(hiR, hv);
+  {
+    int base = 0;
+    for (int j0 = 0; j0 < J; j0 += 32 * kStageUnroll) {
+      uint32_t wv[kStageUnroll];
+      float ev[kStageUnroll];
+#pragma unroll
+      for (int u = 0; u < kStageUnroll; ++u) {
+        const int j = j0 + 32 * u + lane;
+        wv[u] = (j < J) ? sm.u.word[j] : 0u;
+        ev[u] = (j < J) ? __ldg(se + j) : 0.0f;
+      }
+#pragma unroll
+      for (int u = 0; u < kStageUnroll; ++u) {
+        const int j = j0 + 32 * u + lane;
+        const unsigned long long kv = radix_key(wv[u], j);
+        const bool sel = (j < J) && ((kv & pmask) >= prefix);
+        const unsigned m = __ballot_sync(0xffffffffu, sel);
+        if (sel) {
+          sm.v.key[base + __popc(m & ((1u << lane) - 1u))] = sort_key_of_radix(kv);
+          sm.u.word[j] = __float_as_uint(ev[u]);
+        } else if (j < J) {
+          const float hv = __uint_as_float(wv[u] & 0x7FFFFFFFu) + ev[u];
+          if (wv[u] >> 31) hiH = fmaxf(hiH, hv);
+          else hiR = fmaxf(hiR, hv);
+        }
+        base += __popc(m);
+      }
     }
   }
   hiR = warp_max_f(hiR);
   hiH = warp_max_f(hiH);
-  {
-    int pos = warp_excl_sum(cnt, lane);
-    for (int j = lane; j < J; j += 32) {
-      const unsigned long long kv = key_of(j);
-      if ((kv & pmask) >= prefix) sm.key[pos++] = kv;
-    }
-  }
   __syncwarp();
-  if (K <= 32) warp_sort_keys<1>(sm.key, K, lane);
-  else if (K <= 64) warp_sort_keys<2>(sm.key, K, lane);
-  else warp_sort_keys<4>(sm.key, K, lane);
+  if (K <= 32) warp_sort_keys<1>(sm.v.key, K, lane);
+  else if (K <= 64) warp_sort_keys<2>(sm.v.key, K, lane);
+  else warp_sort_keys<4>(sm.v.key, K, lane);
 
   // certification over K + 1 positions: the K keys, then one sentinel with the unselected keys'
   // largest upper bound (in the HRM group iff HRM keys were left out)
@@ -1943,9 +2042,9 @@ __global__ void __launch_bounds__(kWarpSelWarps * 32, 8) kap_select_warp_kernel(
       lo[e] = -INFINITY;
       hi[e] = sentinel_hi;
     } else if (p < K) {
-      const int j = key_block(sm.key[p]);
-      const float s = fmaxf(sc[j], 0.0f);
-      const float er = se[j];
+      const unsigned long long kp = sm.v.key[p];
+      const float s = __uint_as_float(static_cast<uint32_t>(kp >> 31) & 0x7FFFFFFFu);
+      const float er = __uint_as_float(sm.u.word[key_block(kp)]);
       lo[e] = s - er;
       hi[e] = s + er;
     } else {
@@ -2059,28 +2158,47 @@ __global__ void __launch_bounds__(kWarpSelWarps * 32, 8) kap_select_warp_kernel(
       for (int e = 0; e < E3; ++e)
         if (mk[e]) sm.rep_pos[pos++] = lane * E3 + e;
     }
-    __syncwarp();
     // exact scores s_ij = sum over rows r (ascending) of exp(bm[r,j] - M_r), bm[r, j] the largest
-    // float64 logit of block j for row r.  Items are (repaired position, sampled row) pairs: (1) the
-    // fp32 logits of every item's keys; only keys within 2 e_r of their item's fp32 maximum can attain
-    // the exact block maximum and are listed; (2) the listed candidates get float64 logits, four lanes
-    // each, eight candidates at a time; (3) per item the largest is bm[r, j].
-    const int nrows = r1 - r0;
+    // float64-accurate logit of block j for row r.  Items are (repaired position, sampled row) pairs:
+    // (1) the fp32 logits of every item's keys; only keys within 2 e_r of their item's fp32 maximum
+    // can attain the exact block maximum and are listed; (2) the listed candidates get logits summed
+    // as three fp32 terms (float64 accuracy), four lanes each, eight candidates at a time; (3) per
+    // item the largest is bm[r, j].  The candidate words are dead from here on: their storage takes
+    // the query block's sampled rows, and lane rr holds row rr's M_r and e_r.
     const int n_items = n_rep * nrows;
     const int rp = (ri.R + kRowTile - 1) / kRowTile * kRowTile;
     const uint16_t* qbase = a.qs + (a.qs_off[b] + static_cast<int64_t>(h) * rp) * HD;
     const int64_t krow0 = a.ks_off[b] + static_cast<int64_t>(kvh) * rp;
     const float scl = static_cast<float>(a.sm_scale);
+    double m_lane = -INFINITY;
+    float e_lane = 0.0f;
+    if (lane < nrows) {
+      m_lane = a.M[rbase + r0 + lane];
+      e_lane = a.err[rbase + r0 + lane];
+    }
+    __syncwarp();   // every lane's certification reads of the candidate words are done
+    constexpr int LPK = 32 / KB;
+    constexpr int SL = HD / LPK;
+    {
+      const uint16_t* src = qbase + static_cast<int64_t>(r0) * HD;
+      for (int e = lane; e < nrows * HD / 8; e += 32) {
+        float f[8];
+        load8_bf16(src + 8 * e, f);
+        const int rr = e / (HD / 8), x = 8 * (e % (HD / 8));
+        const int seg = x / SL, c = (x % SL) / 4;
+        sm.u.rep.qrows[q_chunk<HD, LPK>(rr, seg, c)] = make_float4(f[0], f[1], f[2], f[3]);
+        sm.u.rep.qrows[q_chunk<HD, LPK>(rr, seg, c + 1)] = make_float4(f[4], f[5], f[6], f[7]);
+      }
+    }
+    __syncwarp();
     // (1) per repaired position, the fp32 logits of the query block's sampled rows against the block's
     // sampled keys: lane group kq (LPK lanes splitting d) keeps key j*KB + kq in registers and takes
     // the rows one after another (two interleaved partial sums: rounding depth SL/2 + 1 + log2(LPK),
-    // within e_r); each key row is loaded once per position, the query rows are shared through L1
-    constexpr int LPK = 32 / KB;
-    constexpr int SL = HD / LPK;
+    // within e_r); each key row is loaded once per position
     const int kq = lane / LPK, sub = lane % LPK;
     int ncand = 0;
     for (int m = 0; m < n_rep; ++m) {
-      const int kc = key_block(sm.key[sm.rep_pos[m]]) * KB + kq;
+      const int kc = key_block(sm.v.key[sm.rep_pos[m]]) * KB + kq;
       const bool kvis = (a.kvalid[(krow0 + kc) >> 5] >> ((krow0 + kc) & 31)) & 1u;
       float kf[SL];
       {
@@ -2095,18 +2213,17 @@ __global__ void __launch_bounds__(kWarpSelWarps * 32, 8) kap_select_warp_kernel(
       }
       for (int rr = 0; rr < nrows; ++rr) {
         const int r = r0 + rr, item = m * nrows + rr;
-        const bool vis = kvis && kc <= r && a.M[rbase + r] != -INFINITY;
-        const uint16_t* qr = qbase + static_cast<int64_t>(r) * HD + sub * SL;
+        const double m_r = __shfl_sync(0xffffffffu, m_lane, rr);
+        const float e_r = __shfl_sync(0xffffffffu, e_lane, rr);
+        const bool vis = kvis && kc <= r && m_r != -INFINITY;
         float p0 = 0.0f, p1 = 0.0f;
 #pragma unroll
-        for (int e = 0; e < SL; e += 8) {
-          float qv[8];
-          load8_bf16(qr + e, qv);
-#pragma unroll
-          for (int u = 0; u < 8; u += 2) {
-            p0 = fmaf(qv[u], kf[e + u], p0);
-            p1 = fmaf(qv[u + 1], kf[e + u + 1], p1);
-          }
+        for (int e = 0; e < SL; e += 4) {
+          const float4 qv = sm.u.rep.qrows[q_chunk<HD, LPK>(rr, sub, e / 4)];
+          p0 = fmaf(qv.x, kf[e], p0);
+          p1 = fmaf(qv.y, kf[e + 1], p1);
+          p0 = fmaf(qv.z, kf[e + 2], p0);
+          p1 = fmaf(qv.w, kf[e + 3], p1);
         }
         float part = p0 + p1;
 #pragma unroll
@@ -2115,11 +2232,11 @@ __global__ void __launch_bounds__(kWarpSelWarps * 32, 8) kap_select_warp_kernel(
         float mx = x;
 #pragma unroll
         for (int o = LPK; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        const bool cand = vis && sub == 0 && x >= mx - 2.0f * a.err[rbase + r];
-        if (lane == 0) sm.terms[item] = -INFINITY;
+        const bool cand = vis && sub == 0 && x >= mx - 2.0f * e_r;
+        if (lane == 0) sm.u.rep.terms[item] = -INFINITY;
         const unsigned cb = __ballot_sync(0xffffffffu, cand);
         const int slot = ncand + __popc(cb & ((1u << lane) - 1u));
-        if (cand && slot < kWarpCand) sm.cand[slot] = (static_cast<uint32_t>(item) << 16) | static_cast<uint32_t>(kc);
+        if (cand && slot < kWarpCand) sm.u.rep.cand[slot] = (static_cast<uint32_t>(item) << 16) | static_cast<uint32_t>(kc);
         ncand += __popc(cb);
       }
     }
@@ -2128,48 +2245,59 @@ __global__ void __launch_bounds__(kWarpSelWarps * 32, 8) kap_select_warp_kernel(
       return;
     }
     __syncwarp();
+    // (2) products of two bf16 values are exact in fp32; each candidate's sum is kept as three fp32
+    // terms on the FP32 pipe (GB300's FP64 pipe runs at a small fraction of that rate)
     for (int c0 = 0; c0 < ncand; c0 += 8) {
-      const int ci = c0 + lane / 4, sub = lane % 4;
+      const int ci = c0 + lane / 4, sub4 = lane % 4;
       int item = -1;
-      double dp = 0.0;
+      float shi = 0.0f, slo = 0.0f, scc = 0.0f;
       if (ci < ncand) {
-        const uint32_t cw = sm.cand[ci];
+        const uint32_t cw = sm.u.rep.cand[ci];
         item = static_cast<int>(cw >> 16);
-        const int r = r0 + item % nrows;
         const int kc = static_cast<int>(cw & 0xffffu);
-        const uint16_t* qrow = qbase + static_cast<int64_t>(r) * HD + sub * (HD / 4);
-        const uint16_t* krow = a.ks + (krow0 + kc) * HD + sub * (HD / 4);
-#pragma unroll 4
-        for (int e = 0; e < HD / 4; e += 2) {
-          const uint32_t qw = *reinterpret_cast<const uint32_t*>(qrow + e);
-          const uint32_t kw = *reinterpret_cast<const uint32_t*>(krow + e);
-          dp += static_cast<double>(__uint_as_float(qw << 16) * __uint_as_float(kw << 16));
-          dp += static_cast<double>(__uint_as_float(qw & 0xffff0000u) * __uint_as_float(kw & 0xffff0000u));
+        const int rr = item % nrows;
+        const uint16_t* krow = a.ks + (krow0 + kc) * HD + sub4 * (HD / 4);
+#pragma unroll
+        for (int e = 0; e < HD / 4; e += 8) {
+          float kv[8];
+          load8_bf16(krow + e, kv);
+          const int x = sub4 * (HD / 4) + e;   // 8 elements within one segment (SL is a multiple of 8)
+          const float4 q0 = sm.u.rep.qrows[q_chunk<HD, LPK>(rr, x / SL, (x % SL) / 4)];
+          const float4 q1 = sm.u.rep.qrows[q_chunk<HD, LPK>(rr, x / SL, (x % SL) / 4 + 1)];
+          const float qv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+          for (int u = 0; u < 8; ++u) sum3_add(shi, slo, scc, __fmul_rn(qv[u], kv[u]));
         }
       }
-      dp += __shfl_xor_sync(0xffffffffu, dp, 1);
-      dp += __shfl_xor_sync(0xffffffffu, dp, 2);
-      const double lx = dp * a.sm_scale;
+#pragma unroll
+      for (int o = 1; o < 4; o <<= 1) {
+        const float oh = __shfl_xor_sync(0xffffffffu, shi, o), ol = __shfl_xor_sync(0xffffffffu, slo, o);
+        const float oc = __shfl_xor_sync(0xffffffffu, scc, o);
+        sum3_add(shi, slo, scc, oh, ol, oc);
+      }
+      const double lx = ((static_cast<double>(shi) + static_cast<double>(slo)) + static_cast<double>(scc)) * a.sm_scale;
       // fold the round's candidates into their items' maxima, one after another
 #pragma unroll
       for (int t = 0; t < 8; ++t) {
         const double v = __shfl_sync(0xffffffffu, lx, 4 * t);
         const int it = __shfl_sync(0xffffffffu, item, 4 * t);
-        if (lane == 0 && it >= 0) sm.terms[it] = fmax(sm.terms[it], v);
+        if (lane == 0 && it >= 0) sm.u.rep.terms[it] = fmax(sm.u.rep.terms[it], v);
       }
     }
     __syncwarp();
-    for (int item = lane; item < n_items; item += 32) {
-      const double Mr = a.M[rbase + r0 + item % nrows];
-      const double bmx = sm.terms[item];
-      sm.terms[item] = (Mr == -INFINITY || bmx == -INFINITY) ? -INFINITY : bmx - Mr;
+    // (3) terms exp(bm[r, j] - M_r), summed over the rows in ascending order
+    for (int i0 = 0; i0 < n_items; i0 += 32) {
+      const int item = i0 + lane;
+      const double m_r = __shfl_sync(0xffffffffu, m_lane, item % nrows);
+      if (item < n_items) {
+        const double bmx = sm.u.rep.terms[item];
+        sm.u.rep.terms[item] = (m_r == -INFINITY || bmx == -INFINITY) ? 0.0 : exp(bmx - m_r);
+      }
     }
-    __syncwarp();
-    for (int item = lane; item < n_rep * nrows; item += 32) sm.terms[item] = exp(sm.terms[item]);
     __syncwarp();
     if (lane < n_rep) {
       double sum = 0.0;
-      for (int rr = 0; rr < nrows; ++rr) sum += sm.terms[lane * nrows + rr];
+      for (int rr = 0; rr < nrows; ++rr) sum += sm.u.rep.terms[lane * nrows + rr];
       sm.rep_val[lane] = sum;
     }
     __syncwarp();
@@ -2181,26 +2309,26 @@ __global__ void __launch_bounds__(kWarpSelWarps * 32, 8) kap_select_warp_kernel(
         while (m1 + 1 < n_rep && sm.rep_pos[m1 + 1] == sm.rep_pos[m1] + 1 && sm.rep_pos[m1 + 1] != nh) ++m1;
         for (int x = m0 + 1; x <= m1; ++x) {
           const double vx = sm.rep_val[x];
-          const unsigned long long kx = sm.key[sm.rep_pos[x]];
+          const unsigned long long kx = sm.v.key[sm.rep_pos[x]];
           int y = x - 1;
           while (y >= m0) {
             const double vy = sm.rep_val[y];
-            const unsigned long long ky = sm.key[sm.rep_pos[y]];
+            const unsigned long long ky = sm.v.key[sm.rep_pos[y]];
             const bool before = (vx > vy) || (vx == vy && key_block(kx) < key_block(ky));
             if (!before) break;
             sm.rep_val[y + 1] = vy;
-            sm.key[sm.rep_pos[y + 1]] = ky;
+            sm.v.key[sm.rep_pos[y + 1]] = ky;
             --y;
           }
           sm.rep_val[y + 1] = vx;
-          sm.key[sm.rep_pos[y + 1]] = kx;
+          sm.v.key[sm.rep_pos[y + 1]] = kx;
         }
         m0 = m1 + 1;
       }
     }
     __syncwarp();
   }
-  for (int k = lane; k < a.mask_pitch; k += 32) out[k] = (k < K) ? key_block(sm.key[k]) : -1;
+  for (int k = lane; k < a.mask_pitch; k += 32) out[k] = (k < K) ? key_block(sm.v.key[k]) : -1;
   if (lane == 0) a.mask_len[mrow] = K;
 }
 
