@@ -529,8 +529,10 @@ __global__ void __launch_bounds__(kLogitsThreads, 2)
 // ---------------------------------------------------------------------------
 constexpr float kEx2Rel = 8.0f / 16777216.0f;   // 2^-21: the relative error assumed of ex2.approx.ftz.f32
 
+constexpr int kScoreDepth = 3;   // key blocks in flight per thread in the block-score kernel
+
 template <int KB>
-__global__ void __launch_bounds__(128) kap_block_scores_kernel(KapArgs a) {
+__global__ void __launch_bounds__(128, 8) kap_block_scores_kernel(KapArgs a) {
   const int i = a.nqb_max - 1 - static_cast<int>(blockIdx.x);   // heaviest query blocks first
   const int h = blockIdx.y, b = blockIdx.z;
   const ReqInfo ri = req_info(a, b);
@@ -546,6 +548,21 @@ __global__ void __launch_bounds__(128) kap_block_scores_kernel(KapArgs a) {
   constexpr float kGrow = 1.0f + 1.0f / 524288.0f;   // 1 + 2^-19
   constexpr float kRnd = 8.5e-8f;                    // >= 1.02 ln 2 2^-23 (|u|)
   constexpr float kRndM = 1.7e-7f;                   // >= 1.02 ln 2 2^-22 (|M_r log2 e|)
+  // a key block's KB row maxima (KB / 4 16-byte vectors) are copied into this thread's slot of a
+  // kScoreDepth-stage ring in shared memory by asynchronous copies, kScoreDepth key blocks ahead of
+  // the one scored: the bytes in flight do not take registers, and no other thread reads the slot
+  __shared__ __align__(16) float s_ring[kScoreDepth][128 * KB];
+  auto issue = [&](int j, int st) {
+    const float* src = bm_blk + static_cast<int64_t>(j) * KB;
+#pragma unroll
+    for (int q = 0; q < KB; q += 4) cp_async16(&s_ring[st][threadIdx.x * KB + q], src + q);
+  };
+#pragma unroll
+  for (int k = 0; k < kScoreDepth; ++k) {
+    const int j = static_cast<int>(threadIdx.x) + k * static_cast<int>(blockDim.x);
+    if (j <= i) issue(j, k);
+    cp_async_commit();   // one group per stage, empty past the row
+  }
   // per sampled row of the query block, computed once per block (float64 is slow here): M_r log2 e
   // and the bound's parts.  A row without a visible key (M_r = -inf) gets +inf, which makes every u
   // -inf and its terms 0.
@@ -579,28 +596,19 @@ __global__ void __launch_bounds__(128) kap_block_scores_kernel(KapArgs a) {
     if (A[q] != 0.0f) ml_max = fmaxf(ml_max, fabsf(Ml2[q]));
   }
   const float C = kGrow * kRnd;
-  // a key block's KB row maxima, as vectors, and its largest key norm; the next key block's are
-  // requested before the current one is scored, so two blocks' loads are in flight per thread
-  float nbm[KB];
-  float nkb = 0.0f;
-  auto load_block = [&](int j) {
-    nkb = __ldg(kbn + j);
-#pragma unroll
-    for (int q = 0; q < KB; q += 4) {
-      const float4 v4 = __ldcs(reinterpret_cast<const float4*>(bm_blk + static_cast<int64_t>(j) * KB + q));
-      nbm[q] = v4.x;
-      nbm[q + 1] = v4.y;
-      nbm[q + 2] = v4.z;
-      nbm[q + 3] = v4.w;
-    }
-  };
-  if (static_cast<int>(threadIdx.x) <= i) load_block(threadIdx.x);
+  int st = 0;
   for (int j = threadIdx.x; j <= i; j += blockDim.x) {
-    const float kbv = nkb;
+    const float kbv = __ldg(kbn + j);
+    cp_async_wait<kScoreDepth - 1>();   // this key block's group is complete
     float bmv[KB];
 #pragma unroll
-    for (int q = 0; q < KB; ++q) bmv[q] = nbm[q];
-    if (j + static_cast<int>(blockDim.x) <= i) load_block(j + blockDim.x);
+    for (int q = 0; q < KB; q += 4) {
+      const float4 v4 = *reinterpret_cast<const float4*>(&s_ring[st][threadIdx.x * KB + q]);
+      bmv[q] = v4.x;
+      bmv[q + 1] = v4.y;
+      bmv[q + 2] = v4.z;
+      bmv[q + 3] = v4.w;
+    }
     // rows past the request's sampled rows hold nothing
 #pragma unroll
     for (int q = 0; q < KB; ++q)
@@ -638,6 +646,12 @@ __global__ void __launch_bounds__(128) kap_block_scores_kernel(KapArgs a) {
     a.score[sbase + j] = x[0];
     // the fmaf chain's own roundings, the pairwise sum's, and the flushed results
     a.score_err[sbase + j] = xe * kGrow + x[0] * (4.0f * 6.0e-8f) + KB * 2.36e-38f;
+    // refill the slot kScoreDepth key blocks ahead: issued after the stores above, which wait for
+    // the slot's values, so the copy cannot overtake their reads
+    const int jn = j + kScoreDepth * static_cast<int>(blockDim.x);
+    if (jn <= i) issue(jn, st);
+    cp_async_commit();
+    st = (st + 1 == kScoreDepth) ? 0 : st + 1;
   }
 }
 
