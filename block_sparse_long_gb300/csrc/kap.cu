@@ -156,6 +156,18 @@ __device__ __forceinline__ const uint16_t* query_ptr(const KapArgs& a, const Req
 __device__ __forceinline__ float bf16_to_f32(uint16_t x) { return __uint_as_float(static_cast<uint32_t>(x) << 16); }
 
 // eight bf16 values from a 16-byte aligned address, widened to fp32
+// per-thread asynchronous copies into shared memory (16 bytes each, both addresses 16-byte aligned),
+// completing in commit groups
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// wait until at most N of this thread's commit groups are still in flight
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ void load8_bf16(const uint16_t* p, float (&f)[8]) {
   const uint4 v = *reinterpret_cast<const uint4*>(p);
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};

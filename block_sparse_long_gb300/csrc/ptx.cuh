@@ -92,20 +92,6 @@ __device__ __forceinline__ bool wait_parity_bounded(uint64_t* bar, uint32_t pari
 }
 
 // ----------------------------------------------------------------------------
-// per-thread asynchronous copies into shared memory (16 bytes each, both addresses 16-byte aligned),
-// completing in commit groups
-// ----------------------------------------------------------------------------
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-// wait until at most N of this thread's commit groups are still in flight
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// ----------------------------------------------------------------------------
 // proxies and fences
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ void fence_proxy_async_smem() {
