@@ -876,6 +876,54 @@ def run_ablation(args):
     return 0
 
 
+def run_link_probe(args):
+    """Host-link bandwidth for one step's copies of a workload: its inputs (q, K and V caches) host to
+    device and its output device to host, from pinned memory, each alone and both at once, with one
+    or more copy streams per direction.  Prints one JSON line per configuration."""
+    import torch
+    spec = synth.spec_for(args.workload)
+    dev = torch.device("cuda", 0)
+    w = synth.make_workload(spec)
+    nb_in = int(w.q.nbytes + w.k_cache.nbytes + w.v_cache.nbytes)
+    nb_out = int(w.q.nbytes)
+    h_in = torch.empty(nb_in, dtype=torch.uint8).pin_memory()
+    h_out = torch.empty(nb_out, dtype=torch.uint8).pin_memory()
+    d_in = torch.empty(nb_in, dtype=torch.uint8, device=dev)
+    d_out = torch.empty(nb_out, dtype=torch.uint8, device=dev)
+    cur = torch.cuda.current_stream(dev)
+
+    def timed(n_h2d, n_d2h, reps=5):
+        streams = [torch.cuda.Stream(device=dev) for _ in range(n_h2d + n_d2h)]
+        jobs = [(d_in, h_in, nb_in, n_h2d, k) for k in range(n_h2d)] + \
+               [(h_out, d_out, nb_out, n_d2h, k) for k in range(n_d2h)]
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(cur)
+        for _ in range(reps):
+            done = []
+            for s, (dst, src, nb, parts, k) in zip(streams, jobs):
+                s.wait_event(e0)
+                with torch.cuda.stream(s):
+                    lo, hi = nb * k // parts, nb * (k + 1) // parts
+                    dst[lo:hi].copy_(src[lo:hi], non_blocking=True)
+                    ev = torch.cuda.Event()
+                    ev.record(s)
+                    done.append(ev)
+            for ev in done:
+                cur.wait_event(ev)
+        e1.record(cur)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    for n_h2d, n_d2h in [(1, 0), (2, 0), (4, 0), (0, 1), (0, 2), (0, 4), (1, 1), (2, 2)]:
+        ms = timed(n_h2d, n_d2h)
+        nbytes = (nb_in if n_h2d else 0) + (nb_out if n_d2h else 0)
+        print(json.dumps({"link_probe": spec.name, "h2d_bytes": nb_in if n_h2d else 0,
+                          "d2h_bytes": nb_out if n_d2h else 0, "h2d_streams": n_h2d, "d2h_streams": n_d2h,
+                          "ms": round(ms, 3), "GB_per_s": round(nbytes / ms / 1e6, 1)}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -904,7 +952,11 @@ def main():
                          "jump: physical jumps vs logical skipping of a binary mask; topp: the top-p stage-1 rule; "
                          "union: GQA page reuse rates; union-kernel: the GQA page-union OSK against the default OSK")
     ap.add_argument("--ablation-tokens", type=int, default=131072, help="context length of --ablation remap/topp")
+    ap.add_argument("--link-probe", action="store_true",
+                    help="host-link bandwidth of one step's input and output copies (the end-to-end floor)")
     args = ap.parse_args()
+    if args.link_probe:
+        return run_link_probe(args)
     if args.sweep:
         return run_sweep(args)
     if args.ablation:
