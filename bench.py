@@ -892,7 +892,9 @@ def run_link_probe(args):
     d_out = torch.empty(nb_out, dtype=torch.uint8, device=dev)
     cur = torch.cuda.current_stream(dev)
 
-    def timed(n_h2d, n_d2h, reps=5):
+    def timed(n_h2d, n_d2h, reps=5, warm=True):
+        if warm:
+            timed(n_h2d, n_d2h, reps=1, warm=False)   # one untimed pass of the same copies first
         streams = [torch.cuda.Stream(device=dev) for _ in range(n_h2d + n_d2h)]
         jobs = [(d_in, h_in, nb_in, n_h2d, k) for k in range(n_h2d)] + \
                [(h_out, d_out, nb_out, n_d2h, k) for k in range(n_d2h)]

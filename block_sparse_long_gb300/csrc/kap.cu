@@ -608,6 +608,7 @@ __global__ void __launch_bounds__(128, 8) kap_block_scores_kernel(KapArgs a) {
     if (A[q] != 0.0f) ml_max = fmaxf(ml_max, fabsf(Ml2[q]));
   }
   const float C = kGrow * kRnd;
+  const bool tail_rows = (i + 1) * KB > ri.R;
   int st = 0;
   for (int j = threadIdx.x; j <= i; j += blockDim.x) {
     const float kbv = __ldg(kbn + j);
@@ -621,10 +622,12 @@ __global__ void __launch_bounds__(128, 8) kap_block_scores_kernel(KapArgs a) {
       bmv[q + 2] = v4.z;
       bmv[q + 3] = v4.w;
     }
-    // rows past the request's sampled rows hold nothing
+    // rows past the request's sampled rows hold nothing (only a request's last query block has any)
+    if (tail_rows) {
 #pragma unroll
-    for (int q = 0; q < KB; ++q)
-      if (i * KB + q >= ri.R) bmv[q] = -INFINITY;
+      for (int q = 0; q < KB; ++q)
+        if (i * KB + q >= ri.R) bmv[q] = -INFINITY;
+    }
     float x[KB];
     float xe = 0.0f;
     if (dl_max * kbv <= 0.013f && ml_max <= 1.0e5f) {

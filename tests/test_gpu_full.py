@@ -31,19 +31,23 @@ def sampled_items(spec, n, seed):
     return sorted(items)
 
 
-def run_full(name, n_items, seed):
+def run_full(name, n_items, seed, n_mask_rows=0):
+    """n_items sampled items get the full check (mask row, skip decisions, outputs); n_mask_rows more
+    sampled mask rows are checked bit for bit against the oracle's KAP as well (the KAP oracle costs
+    far less per row than the OSK oracle)."""
     sp = synth.spec_for(name)
     delta = json.load(open(GOLDEN))["workloads"][name]["delta"]
     w = synth.make_workload(sp)
     prm = gh.oracle_params(sp, delta)
     pitch = gh.C.stage1_pitch(sp.budget_ppm, sp.max_seqlen, sp.block_size)
     items = sampled_items(sp, n_items, seed)
+    mask_items = sorted(set(items) | set(sampled_items(sp, n_mask_rows, seed + 1000))) if n_mask_rows else items
     dw = gh.to_device(w)
     p = gh.cosa_params(dw, delta=delta, mask_pitch=pitch + (4 if sp.mask_noise_frac else 0))
     mask_g, len_g = gh.run_kap(dw, p)
-    # oracle KAP on the sampled items only
+    # oracle KAP on the sampled rows only
     by = {}
-    for (b, h, i) in items:
+    for (b, h, i) in mask_items:
         by.setdefault((b, h), []).append(i)
     mask_o, len_o, rows = orc.kap_mask(w.q, w.k_cache, w.page_table, w.cu_seqlens, sp.num_q_heads,
                                        sp.num_kv_heads, prm, p.mask_pitch, qblocks=by)
@@ -64,19 +68,19 @@ def run_full(name, n_items, seed):
 
 def test_full_32k_shuffled():
     """32K tokens, shuffled physical pages, budgets 15 % / 5 %."""
-    rep, flags = run_full("32k_gqa_shuffled", 48, seed=3)
+    rep, flags = run_full("32k_gqa_shuffled", 48, seed=3, n_mask_rows=256)
     assert (flags == orc.SKIPPED).any()
 
 
 def test_full_128k_student_t():
     """128K tokens, Student-t keys, budgets 10 % / 3 %: the benchmark workload."""
-    rep, flags = run_full("128k_gqa_student_t", 64, seed=4)
+    rep, flags = run_full("128k_gqa_student_t", 64, seed=4, n_mask_rows=256)
     assert (flags == orc.SKIPPED).any()
 
 
 def test_full_ragged_batch():
     """Ragged batch {16K, 48K, 96K, 128K}, duplicate and invalid IDs in 5 % of the mask rows."""
-    rep, flags = run_full("ragged4_gqa_noisy_masks", 64, seed=5)
+    rep, flags = run_full("ragged4_gqa_noisy_masks", 64, seed=5, n_mask_rows=256)
     assert (flags == orc.IGNORED).sum() > 0
 
 
@@ -87,5 +91,5 @@ def test_full_32k_iid_queries():
     selected block: the rows of a query block have independent maxima, so some row always wants a
     block), so the parity here is of the masks (flat, near-tied scores) and the outputs, with the
     largest Delta of the grid."""
-    rep, flags = run_full("32k_gqa_shuffled_iidq", 48, seed=6)
+    rep, flags = run_full("32k_gqa_shuffled_iidq", 48, seed=6, n_mask_rows=256)
     assert rep.n_tested > 0
