@@ -448,43 +448,58 @@ def run_cosa(args, spec, workload_name, delta):
     houts = [hout, torch.empty_like(hout).pin_memory()]
     sets = [dict(q=q, k=k, v=v, pt=pt, cu=cu, out=out)]
     sets.append({name: torch.empty_like(t) for name, t in sets[0].items()})
-    h2d_stream, d2h_stream = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    # each direction's copies split over args.copy_streams streams (contiguous chunks of every tensor)
+    ncs = max(1, args.copy_streams)
+    h2d_streams = [torch.cuda.Stream(device=dev) for _ in range(ncs)]
+    d2h_streams = [torch.cuda.Stream(device=dev) for _ in range(ncs)]
+
+    def chunk(t, k):
+        flat = t.view(-1)
+        return flat[flat.numel() * k // ncs: flat.numel() * (k + 1) // ncs]
 
     def e2e_steps(n, start_event=None):
-        ev_done, ev_out = [None, None], [None, None]
+        ev_done, ev_out = [None, None], [[], []]
         if start_event is not None:
-            h2d_stream.wait_event(start_event)
-            d2h_stream.wait_event(start_event)
+            for cs in h2d_streams + d2h_streams:
+                cs.wait_event(start_event)
         for s in range(n):
             x = s % 2
             b = sets[x]
-            with torch.cuda.stream(h2d_stream):
-                if ev_done[x] is not None:
-                    h2d_stream.wait_event(ev_done[x])       # step s - 2 has finished with this set
-                for name, src in (("q", hq), ("k", hk), ("v", hv)):
-                    b[name].view(torch.int16).copy_(src, non_blocking=True)
-                b["pt"].copy_(hpt, non_blocking=True)
-                b["cu"].copy_(hcu, non_blocking=True)
-                ev_in = torch.cuda.Event()
-                ev_in.record(h2d_stream)
-            stream.wait_event(ev_in)
-            if ev_out[x] is not None:
-                stream.wait_event(ev_out[x])                # step s - 2's output has been read
+            ev_in = []
+            for k, cs in enumerate(h2d_streams):
+                with torch.cuda.stream(cs):
+                    if ev_done[x] is not None:
+                        cs.wait_event(ev_done[x])           # step s - 2 has finished with this set
+                    for name, src in (("q", hq), ("k", hk), ("v", hv)):
+                        chunk(b[name].view(torch.int16), k).copy_(chunk(src, k), non_blocking=True)
+                    if k == 0:
+                        b["pt"].copy_(hpt, non_blocking=True)
+                        b["cu"].copy_(hcu, non_blocking=True)
+                    ev = torch.cuda.Event()
+                    ev.record(cs)
+                    ev_in.append(ev)
+            for ev in ev_in:
+                stream.wait_event(ev)
+            for ev in ev_out[x]:
+                stream.wait_event(ev)                       # step s - 2's output has been read
             C.cosa_proxy_select(p, b["q"], b["cu"], b["k"], b["pt"], mask=mask, mask_len=mask_len, workspace=ws,
                                 status=status)
             C.cosa_sparse_prefill(p, b["q"], b["cu"], b["k"], b["v"], b["pt"], mask, mask_len, out=b["out"],
                                   status=status)
             ev_done[x] = torch.cuda.Event()
             ev_done[x].record(stream)
-            with torch.cuda.stream(d2h_stream):
-                d2h_stream.wait_event(ev_done[x])
-                houts[x].copy_(b["out"].view(torch.int16), non_blocking=True)
-                ev_out[x] = torch.cuda.Event()
-                ev_out[x].record(d2h_stream)
+            ev_out[x] = []
+            for k, cs in enumerate(d2h_streams):
+                with torch.cuda.stream(cs):
+                    cs.wait_event(ev_done[x])
+                    chunk(houts[x], k).copy_(chunk(b["out"].view(torch.int16), k), non_blocking=True)
+                    ev = torch.cuda.Event()
+                    ev.record(cs)
+                    ev_out[x].append(ev)
         # a step ends when its output is on the host
-        for e in ev_out:
-            if e is not None:
-                stream.wait_event(e)
+        for evs in ev_out:
+            for ev in evs:
+                stream.wait_event(ev)
 
     e2e_steps(max(2, args.warmup))
     if world > 1:
@@ -554,6 +569,7 @@ def run_cosa(args, spec, workload_name, delta):
         "e2e": {"value": job_flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
                 "pipelined": "two device input/output sets; step s's host-to-device copy and step s-1's "
                              "device-to-host read overlap the kernels",
+                "copy_streams_per_direction": max(1, args.copy_streams),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 9 * args.steps,
         "clocks": cl,
@@ -954,6 +970,8 @@ def main():
                          "jump: physical jumps vs logical skipping of a binary mask; topp: the top-p stage-1 rule; "
                          "union: GQA page reuse rates; union-kernel: the GQA page-union OSK against the default OSK")
     ap.add_argument("--ablation-tokens", type=int, default=131072, help="context length of --ablation remap/topp")
+    ap.add_argument("--copy-streams", type=int, default=1,
+                    help="copy streams per direction in the end-to-end loop (each tensor split into that many chunks)")
     ap.add_argument("--link-probe", action="store_true",
                     help="host-link bandwidth of one step's input and output copies (the end-to-end floor)")
     args = ap.parse_args()
