@@ -1433,30 +1433,37 @@ __device__ void kap_select_row(const KapArgs& a, int cap, int row) {
   const int nh_all = n_hrm_s;   // HRM keys sort first
   const float* sc = a.score + sbase;
   const float* se = a.score_err + sbase;
-  // Ordered list the certification runs on: either all J keys sorted (full path), or the K selected
-  // keys sorted plus one sentinel at position K that stands for every unselected key of its group
-  // (its upper bound is theirs, largest; it is never a candidate).  If the budget cut cannot be
-  // certified against the sentinel, the full path runs instead.
+  // Ordered list the certification runs on: either all J keys sorted (full path), or the ks largest
+  // keys sorted plus one sentinel at position ks that stands for every unselected key of its group
+  // (its upper bound is theirs, largest; it is never a candidate).  The first attempt takes ks = K;
+  // if the budget cut cannot be certified against that sentinel (an uncertain run reaches it), a
+  // second takes ks = K + 32, so that the run can close before the sentinel; then the full path.
   int Jl = J, nh = nh_all, n2 = 1, Nl = kSelectThreads;
+  int ks = K;                // selected keys (the sentinel's position) on the top-K paths
   bool sentinel = false;
   bool topp_exact = false;   // the top-p length is not certified by the bounds: exact scores below
   float sentinel_hi = -INFINITY;
-  for (int attempt = (!a.top_p && K <= kTopFast && K < J) ? 0 : 1; attempt < 2; ++attempt) {
+  for (int attempt = (!a.top_p && K <= kTopFast && K < J) ? 0 : 2; attempt < 3; ++attempt) {
     int N2 = 1;
     while (N2 < J) N2 <<= 1;
     const int N = N2 < kSelectThreads ? kSelectThreads : N2;
-    if (attempt == 0) {
+    if (attempt == 1) {
+      ks = min(min(K + 32, kTopFast), J - 1);
+      if (ks <= K) continue;   // no room to widen: the full path
+    }
+    if (attempt < 2) {
+      if (attempt == 0) ks = K;
       switch (N / kSelectThreads) {
-        case 1: select_top_dispatch<1>(key, hrm, sc, se, J, K, topk); break;
-        case 2: select_top_dispatch<2>(key, hrm, sc, se, J, K, topk); break;
-        case 4: select_top_dispatch<4>(key, hrm, sc, se, J, K, topk); break;
-        case 8: select_top_dispatch<8>(key, hrm, sc, se, J, K, topk); break;
-        default: select_top_dispatch<16>(key, hrm, sc, se, J, K, topk); break;
+        case 1: select_top_dispatch<1>(key, hrm, sc, se, J, ks, topk); break;
+        case 2: select_top_dispatch<2>(key, hrm, sc, se, J, ks, topk); break;
+        case 4: select_top_dispatch<4>(key, hrm, sc, se, J, ks, topk); break;
+        case 8: select_top_dispatch<8>(key, hrm, sc, se, J, ks, topk); break;
+        default: select_top_dispatch<16>(key, hrm, sc, se, J, ks, topk); break;
       }
       sentinel = true;
-      Jl = K + 1;
-      nh = (nh_all > K) ? K + 1 : nh_all;   // the sentinel joins the HRM group iff HRM keys were left out
-      sentinel_hi = __int_as_float(topk.hi_out[(nh_all > K) ? 1 : 0]);
+      Jl = ks + 1;
+      nh = (nh_all > ks) ? ks + 1 : nh_all;   // the sentinel joins the HRM group iff HRM keys were left out
+      sentinel_hi = __int_as_float(topk.hi_out[(nh_all > ks) ? 1 : 0]);
       Nl = kSelectThreads;
     } else {
       switch (N / kSelectThreads) {
@@ -1486,7 +1493,7 @@ __device__ void kap_select_row(const KapArgs& a, int cap, int row) {
     }
     // score intervals per listed position
     for (int p = tid; p < n2; p += blockDim.x) {
-      if (sentinel && p == K) {
+      if (sentinel && p == ks) {
         lo[p] = -INFINITY;
         hi[p] = sentinel_hi;
       } else if (p < Jl) {
@@ -1560,7 +1567,7 @@ __device__ void kap_select_row(const KapArgs& a, int cap, int row) {
         if (mk) {
           bits |= 1u << e;
           ++cnt;
-          if (sentinel && x == K) sentinel_marked_s = 1;
+          if (sentinel && x == ks) sentinel_marked_s = 1;
         }
       }
       const int lane = tid & 31, w = tid >> 5;
