@@ -9,7 +9,8 @@ cut trusts that bound, so it is checked here on the same fp32 arithmetic (numpy 
 multiply-adds taken exactly in float64 and rounded once), with the fp32 block maximum placed at the
 edge of the logit error the kernel assumes and the exponential's error at the edge of its assumed
 2^-21, against exp(L - M) in float64 for the exact block-maximum logit L and the float64 row maximum M.
-Dropping the exponential's share from A breaks the bound, so the check has teeth."""
+Dropping the exponential's share from A breaks the bound, so the check has teeth.  The kernel's
+expm1f branch (large norms or row maxima) is checked the same way."""
 import numpy as np
 
 F = np.float32
@@ -90,3 +91,37 @@ def test_bound_without_the_exponential_share_breaks():
     live = u >= -120.0
     err = np.abs(x.astype(np.float64) - exact)
     assert np.any(err[live] > bound[live].astype(np.float64))
+
+
+def test_block_score_term_bound_holds_on_the_expm1_branch():
+    """Large norms (dl ||k|| > 0.013): the kernel bounds the relative error of each term by
+    expm1(ln 2 D) * 1.01 + 2^-21 * 1.01 with D the exponent's error bound, scaled by 1 + 2^-19."""
+    rng = np.random.default_rng(9)
+    n = 200_000
+    qn = f32(np.exp(rng.uniform(np.log(200.0), np.log(2000.0), n)))
+    kn = f32(np.exp(rng.uniform(np.log(200.0), np.log(2000.0), n)))
+    err_raw = KAPPA.astype(np.float64) * qn * kn
+    dot = rng.uniform(-1.0, 1.0, n) * qn * kn
+    L = dot * SCALE
+    M = L + np.where(rng.random(n) < 0.1, 0.0, rng.uniform(0.0, 60.0, n))
+    bm = f32(dot + rng.choice([-1.0, 1.0], n) * rng.uniform(0.9, 1.0, n) * err_raw)
+    keep = np.abs(bm.astype(np.float64) - dot) <= err_raw
+    M, L, qn, kn, bm = M[keep], L[keep], qn[keep], kn[keep], bm[keep]
+    eps = ex2_errors(rng, M.size)
+    sl2 = f32(SCALE * 1.4426950408889634)
+    ml2 = f32(f32(M) * F(1.44269504))
+    dl = f32(f32(f32(KAPPA * F(SCALE)) * qn) * F(1.001))
+    b = f32(f32(GROW * F(1.02)) * dl)
+    u = f32(bm.astype(np.float64) * sl2.astype(np.float64) - ml2.astype(np.float64))
+    x = f32(np.exp2(u.astype(np.float64)) * (1.0 + eps))
+    slow = (dl.astype(np.float64) * kn > 0.013) | (np.abs(ml2) > 1e5)
+    d = f32(f32(f32(F(1.4426950408889634) * b) / f32(GROW * F(1.02))) * kn) + \
+        f32(F(1.2e-7) * f32(f32(F(2.0) * np.abs(ml2)) + np.minimum(np.abs(u), F(1.0e30))))
+    d = f32(d)
+    rel = f32(f32(np.expm1(f32(F(0.6931472) * d)) * F(1.01)) + f32(EX2_REL * F(1.01)))
+    bound = f32(x.astype(np.float64) * f32(GROW * rel).astype(np.float64))
+    exact = np.exp(L - M)
+    live = slow & (u >= -120.0)
+    assert live.sum() > 0.5 * M.size
+    err = np.abs(x.astype(np.float64) - exact)
+    assert np.all(err[live] <= bound[live].astype(np.float64))
