@@ -1749,10 +1749,11 @@ __device__ void kap_select_row(const KapArgs& a, int cap, int row) {
 
 // ---------------------------------------------------------------------------
 // The same selection, one warp per mask row, for the common rows: fraction budget, J <= 1024,
-// K <= 128 and K < J.  The K largest keys are found by radix select, sorted, certified against one
-// sentinel standing for every unselected key (as in kap_select_kernel's top-K path) and up to
-// kWarpRepMax uncertain positions are repaired in float64.  Every other row (and a row whose cut
-// the sentinel cannot certify) is left to kap_select_kernel, marked by mask_len = -1.
+// K <= 128 and K < J.  The row's scores are staged in shared memory once; the K largest keys are
+// found by radix select, sorted, certified against one sentinel standing for every unselected key
+// (as in kap_select_kernel's top-K path) and up to kWarpRepMax uncertain positions are repaired at
+// float64 accuracy.  Every other row (and a row whose cut the sentinel cannot certify) is left to
+// kap_select_kernel, marked by mask_len = -1.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ size_t mrow_of(const KapArgs& a, int row) {
   const int h = row % a.num_q_heads;
